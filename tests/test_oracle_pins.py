@@ -1,0 +1,404 @@
+"""Pins of the CPU oracle against what the pages and mathematics fix.
+
+Each test checks the oracle against something other than itself: printed
+arithmetic from the pages (golden fixtures), closed forms, invariants, library
+routines for special cases, or brute force on tiny inputs.
+"""
+import math
+
+import numpy as np
+import pytest
+import scipy.linalg
+import torch
+
+import oracle
+from oracle.block import BlockWeightsOracle, decode_block, rms_factor
+from oracle.kv import KVCacheOracle, kv_quantize
+from synth import BlockShape
+from tests.conftest import golden_path
+
+
+# ---------------------------------------------------------------- nibble decode
+def test_nibble_decode_all_16_codes_golden():
+    rows = [l.split() for l in open(golden_path("nibble_decode.txt")) if l.strip() and not l.startswith("#")]
+    assert len(rows) == 16
+    for code, bits, val, dec in rows:
+        c = int(code)
+        assert int(bits, 16) == 0x4300 | c
+        assert float(oracle.bf16_from_bits(np.array([int(bits, 16)], np.uint16))[0]) == float(val)
+        assert oracle.nibble_decode_via_bf16(c) == float(dec) == c - 8
+        # the oracle's dequantiser agrees with the pages' construction (scale 1)
+        assert oracle.dequantize_groups(np.array([[c]], np.uint8), np.array([[1.0]]), 1)[0, 0] == c - 8
+
+
+# ---------------------------------------------------------------- BF16 rounding
+def test_bf16_rne_hand_cases():
+    one = np.float32(1.0)
+    cases = [
+        (1.0, 1.0),
+        (1.0 + 2.0 ** -8, 1.0),                        # exact tie -> even (1.0)
+        (1.0 + 3 * 2.0 ** -8, 1.0 + 2.0 ** -6),        # exact tie -> even mantissa 2
+        (1.0 + 2.0 ** -8 + 2.0 ** -20, 1.0 + 2.0 ** -7),  # just above the tie
+        (-(1.0 + 2.0 ** -8 + 2.0 ** -20), -(1.0 + 2.0 ** -7)),
+        (0.0, 0.0),
+    ]
+    for x, want in cases:
+        assert float(oracle.bf16_rne(np.float32(x))) == want, x
+    assert one == 1.0
+
+
+def test_bf16_rne_matches_torch_conversion():
+    g = np.random.default_rng(0)
+    x = (g.standard_normal(100000) * np.exp(g.uniform(-20, 20, 100000))).astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.bfloat16).to(torch.float32).numpy()
+    np.testing.assert_array_equal(oracle.bf16_rne(x), ref)
+
+
+# ---------------------------------------------------------------- quantiser
+def test_quantizer_golden_hand_cases():
+    for line in open(golden_path("quantizer_hand_cases.txt")):
+        if not line.strip() or line.startswith("#"):
+            continue
+        vals, scale, codes = [p.split() for p in line.split("|")]
+        x = np.array([float(v) for v in vals], np.float32)
+        c, s = oracle.quantize_groups(x[None], 4)
+        assert float(s[0, 0]) == float(scale[0])
+        assert c[0].tolist() == [int(v) for v in codes]
+
+
+def test_quantizer_brute_force_nearest_code():
+    """Every unclamped code is the nearest representable (c-8)*s (ties to even)."""
+    g = np.random.default_rng(1)
+    x = (g.standard_normal((500, 128)) * g.uniform(0.001, 10, (500, 1))).astype(np.float32)
+    x[0, :] = 0.0
+    codes, s = oracle.quantize_groups(x, 128)
+    assert np.all(codes[0] == 8) and s[0, 0] == 0
+    for r in range(1, 60):
+        sr = np.float32(s[r, 0])
+        for i in range(128):
+            t = np.float32(x[r, i] / sr)                 # FP32 decision, as stated
+            cand = np.arange(-8, 8, dtype=np.float64)
+            dist = np.abs(cand - float(t))
+            best = cand[dist == dist.min()]
+            want = best[0] if len(best) == 1 else best[np.argmin(np.abs(best) % 2)]  # tie -> even
+            assert int(codes[r, i]) - 8 == want
+
+
+def test_quantizer_invariants():
+    g = np.random.default_rng(2)
+    x = (g.standard_normal((300, 128)) * 3).astype(np.float32)
+    codes, s = oracle.quantize_groups(x, 128)
+    xh = oracle.dequantize_groups(codes, s, 128)
+    # the element of largest magnitude decodes to +-7 s (amax/7 rounded to BF16 is within 2^-8)
+    am = np.argmax(np.abs(x), axis=1)
+    assert np.all(np.abs(codes[np.arange(300), am].astype(int) - 8) == 7)
+    # reconstruction error of every element is at most s/2
+    assert np.all(np.abs(x - xh) <= s / 2 + 1e-12)
+    # scale is BF16 and within 2^-8 relative of amax/7
+    amax = np.max(np.abs(x), axis=1, keepdims=True)
+    assert np.all(np.abs(s - amax / 7) <= (amax / 7) * 2.0 ** -8)
+    assert np.all(oracle.bf16_rne(s) == s)
+
+
+# ---------------------------------------------------------------- Hadamard
+def _golden_hadamards():
+    mats, cur, rows = {}, None, []
+    for line in open(golden_path("hadamard_small.txt")):
+        if line.startswith("#") or not line.strip():
+            continue
+        if line.startswith("order"):
+            if cur:
+                mats[cur] = np.array(rows, float)
+            cur, rows = int(line.split()[1]), []
+        else:
+            rows.append([float(v) for v in line.split()])
+    mats[cur] = np.array(rows, float)
+    return mats
+
+
+def test_hadamard_small_orders_golden():
+    for n, m in _golden_hadamards().items():
+        np.testing.assert_array_equal(oracle.sylvester(n) * np.sqrt(n), m)
+
+
+@pytest.mark.parametrize("n", [1, 2, 4, 16, 64, 128])
+def test_hadamard_orthogonal_symmetric_and_scipy(n):
+    h = oracle.sylvester(n)
+    np.testing.assert_allclose(h @ h.T, np.eye(n), atol=1e-15)
+    np.testing.assert_array_equal(h, h.T)
+    np.testing.assert_array_equal(h * np.sqrt(n), scipy.linalg.hadamard(n))
+
+
+def test_rotation_preserves_dot_products_and_norms():
+    g = np.random.default_rng(3)
+    q, k = g.standard_normal((2, 50, 128))
+    for hb in (16, 64, 128):
+        qh, kh = oracle.blockdiag_apply(q, hb), oracle.blockdiag_apply(k, hb)
+        np.testing.assert_allclose(np.sum(qh * kh, -1), np.sum(q * k, -1), rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(np.linalg.norm(qh, axis=-1), np.linalg.norm(q, axis=-1), rtol=1e-13)
+        # self-inverse
+        np.testing.assert_allclose(oracle.blockdiag_apply(qh, hb), q, atol=1e-13)
+
+
+def test_rotation_is_block_diagonal():
+    x = np.zeros(128)
+    x[64:] = np.arange(64) + 1.0
+    y = oracle.blockdiag_apply(x, 64)
+    assert np.all(y[:64] == 0)
+    np.testing.assert_allclose(y[64:], oracle.sylvester(64) @ x[64:], atol=1e-13)
+
+
+# ---------------------------------------------------------------- RoPE
+def test_rope_hand_case_and_complex_form():
+    x = np.array([1.0, 0.0, 0.0, 0.0])
+    np.testing.assert_allclose(oracle.rope_apply(x, 1, 100.0), [math.cos(1), 0, math.sin(1), 0], atol=1e-15)
+    np.testing.assert_allclose(oracle.inv_freq(4, 100.0), [1.0, 0.1])
+    g = np.random.default_rng(4)
+    v = g.standard_normal(64)
+    z = (v[:32] + 1j * v[32:]) * np.exp(1j * 37 * oracle.inv_freq(64, 10000.0))
+    np.testing.assert_allclose(oracle.rope_apply(v, 37, 10000.0), np.concatenate([z.real, z.imag]), atol=1e-13)
+
+
+def test_rope_identity_norm_and_relative_position():
+    g = np.random.default_rng(5)
+    q, k = g.standard_normal((2, 128))
+    np.testing.assert_array_equal(oracle.rope_apply(q, 0, 5e5), q)
+    np.testing.assert_allclose(np.linalg.norm(oracle.rope_apply(q, 999, 5e5)), np.linalg.norm(q), rtol=1e-13)
+    a = oracle.rope_apply(q, 1000, 5e5) @ oracle.rope_apply(k, 990, 5e5)
+    b = oracle.rope_apply(q, 13, 5e5) @ oracle.rope_apply(k, 3, 5e5)
+    assert abs(a - b) < 1e-10
+
+
+# ---------------------------------------------------------------- gain folding / row factor
+def test_gain_folding_and_deferred_row_factor():
+    g = np.random.default_rng(6)
+    w = g.standard_normal((96, 256))
+    gamma = g.uniform(0.5, 1.5, 256)
+    x = g.standard_normal(256) * 5
+    rho = 1.0 / np.sqrt(np.mean(x * x) + 1e-5)
+    explicit = w @ (gamma * (rho * x))          # RMSNorm then matmul
+    folded = rho * ((w * gamma[None, :]) @ x)    # W' = W diag(gamma), rho after accumulation
+    np.testing.assert_allclose(folded, explicit, rtol=1e-12)
+    # RMSNorm is scale invariant (eps -> 0)
+    assert abs(rms_factor(3 * x, 0.0) * 3 - rms_factor(x, 0.0)) < 1e-12
+    assert abs(rms_factor(np.array([3.0, 4.0]), 0.0) - 1 / math.sqrt(12.5)) < 1e-15
+
+
+def test_int4_matvec_matches_dense_and_brute_force():
+    g = np.random.default_rng(7)
+    w = g.normal(0, 0.02, (40, 384)).astype(np.float32)
+    gamma = g.uniform(0.5, 1.5, 384).astype(np.float32)
+    codes, s = oracle.quantize_weight(w, gamma)
+    x = g.standard_normal((3, 384))
+    dense = oracle.dequantize_groups(codes, s, 128) @ x.T
+    np.testing.assert_allclose(oracle.int4_matvec(codes, s, x, row_chunk=7), dense.T, rtol=1e-12)
+    # brute force, one output
+    o, b = 5, 1
+    acc = 0.0
+    for gi in range(3):
+        part = sum((int(codes[o, gi * 128 + i]) - 8) * x[b, gi * 128 + i] for i in range(128))
+        acc += float(s[o, gi]) * part
+    assert abs(acc - oracle.int4_matvec(codes, s, x)[b, o]) < 1e-12
+    # gamma is folded in FP32 before quantising
+    c2, s2 = oracle.quantize_groups((w * gamma[None]).astype(np.float32), 128)
+    np.testing.assert_array_equal(c2, codes)
+
+
+# ---------------------------------------------------------------- attention
+def _brute_attention(q, K, V):
+    d = len(q)
+    sc = [sum(q[c] * K[j][c] for c in range(d)) / math.sqrt(d) for j in range(len(K))]
+    m = max(sc)
+    e = [math.exp(v - m) for v in sc]
+    z = sum(e)
+    return [sum(e[j] * V[j][c] for j in range(len(K))) / z for c in range(d)]
+
+
+def test_attention_brute_force_tiny():
+    g = np.random.default_rng(8)
+    q, K, V = g.standard_normal(8), g.standard_normal((5, 8)) * 2, g.standard_normal((5, 8))
+    np.testing.assert_allclose(oracle.attend(q, K, V), _brute_attention(q, K, V), rtol=1e-13)
+
+
+def test_attention_special_cases():
+    g = np.random.default_rng(9)
+    q, v = g.standard_normal(16), g.standard_normal(16)
+    np.testing.assert_allclose(oracle.attend(q, g.standard_normal((1, 16)), v[None]), v, rtol=1e-15)
+    k = g.standard_normal(16)
+    V = g.standard_normal((6, 16))
+    np.testing.assert_allclose(oracle.attend(q, np.tile(k, (6, 1)), V), V.mean(0), rtol=1e-13)
+
+
+@pytest.mark.parametrize("n_split", [1, 2, 7, 64])
+def test_split_kv_merge_invariance(n_split):
+    g = np.random.default_rng(10)
+    q, K, V = g.standard_normal(128), g.standard_normal((300, 128)) * 3, g.standard_normal((300, 128))
+    np.testing.assert_allclose(oracle.attend_split(q, K, V, n_split), oracle.attend(q, K, V), rtol=1e-12, atol=1e-14)
+
+
+def test_rotated_attention_equals_unrotated_without_quantisation():
+    g = np.random.default_rng(11)
+    q, K, V = g.standard_normal(128), g.standard_normal((40, 128)) * 2, g.standard_normal((40, 128))
+    for hb in (32, 128):
+        R = lambda a: oracle.blockdiag_apply(a, hb)
+        ot = oracle.attend(R(q), R(K), R(V))
+        np.testing.assert_allclose(R(ot), oracle.attend(q, K, V), rtol=1e-12, atol=1e-14)
+
+
+def test_swiglu_closed_form():
+    gg = np.array([0.0, 1.0, -2.0])
+    u = np.array([3.0, 2.0, 1.0])
+    a = gg / (1.0 + np.exp(-gg)) * u
+    np.testing.assert_allclose(a, [0.0, 2.0 / (1.0 + math.exp(-1.0)), -2.0 / (1.0 + math.exp(2.0))], rtol=1e-15)
+
+
+# ---------------------------------------------------------------- whole block
+MINI = BlockShape(hidden=256, n_q=8, n_kv=2, head_dim=16, inter=256, rope_base=10000.0)
+
+
+def _mini_setup(shape=MINI, B=2, L=5, seed=12, zero=()):
+    g = np.random.default_rng(seed)
+    w = {
+        "wqkv": g.normal(0, 0.05, (shape.n_qkv, shape.hidden)).astype(np.float32),
+        "wo": g.normal(0, 0.05, (shape.hidden, shape.n_q * shape.head_dim)).astype(np.float32),
+        "wgu": g.normal(0, 0.05, (2 * shape.inter, shape.hidden)).astype(np.float32),
+        "wdown": g.normal(0, 0.05, (shape.hidden, shape.inter)).astype(np.float32),
+        "gamma_attn": g.uniform(0.5, 1.5, shape.hidden).astype(np.float32),
+        "gamma_ffn": g.uniform(0.5, 1.5, shape.hidden).astype(np.float32),
+    }
+    for z in zero:
+        w[z][:] = 0
+    wts = BlockWeightsOracle(shape, w)
+    cache = KVCacheOracle(B, shape.n_kv, L + 4, shape.head_dim, shape.hb, shape.kvg)
+    if L:
+        cache.append(g.standard_normal((B, L, shape.n_kv, shape.head_dim)),
+                     g.standard_normal((B, L, shape.n_kv, shape.head_dim)), np.zeros(B, int))
+    x = g.standard_normal((B, shape.hidden)) * 2
+    return w, wts, cache, x
+
+
+def test_block_residual_only_when_output_weights_zero():
+    w, wts, cache, x = _mini_setup(zero=("wo", "wdown"))
+    r = decode_block(MINI, wts, cache, x, np.array([5, 5]))
+    np.testing.assert_array_equal(r["out"], x)
+    w, wts, cache, x = _mini_setup(zero=("wdown",))
+    r = decode_block(MINI, wts, cache, x, np.array([5, 5]))
+    np.testing.assert_array_equal(r["out"], r["h1"])
+
+
+def test_block_single_key_closed_form():
+    """L_b = 0: each head attends to the new token only, so o_h = H * dequant(quant(H v))."""
+    w, wts, cache, x = _mini_setup(L=0)
+    r = decode_block(MINI, wts, cache, x, np.array([0, 0]))
+    s = MINI
+    for i in range(2):
+        rho = 1 / np.sqrt(np.mean(x[i] ** 2) + s.rms_eps)
+        wv = oracle.dequantize_groups(*wts.qkv, 128)[(s.n_q + s.n_kv) * s.head_dim:]
+        v = (rho * (wv @ x[i])).reshape(s.n_kv, s.head_dim)
+        for j in range(s.n_kv):
+            c, sc, _ = kv_quantize(v[j], s.hb, s.kvg)
+            vh = oracle.sylvester(s.hb) @ oracle.dequantize_groups(c, sc, s.kvg)
+            for hh in range(s.n_q // s.n_kv):
+                h = j * (s.n_q // s.n_kv) + hh
+                np.testing.assert_allclose(r["o"][i, h * 16:(h + 1) * 16], vh, rtol=1e-12, atol=1e-14)
+
+
+def test_block_output_projection_orientation():
+    """A single nonzero W_o[r, c] moves exactly one residual channel by w * o[c]."""
+    w, wts, cache, x = _mini_setup(zero=("wdown",))
+    w["wo"][:] = 0
+    w["wo"][7, 19] = 0.5
+    wts = BlockWeightsOracle(MINI, w)
+    r = decode_block(MINI, wts, cache, x, np.array([5, 5]))
+    delta = r["h1"] - x
+    assert np.count_nonzero(np.abs(delta) > 0) <= 2
+    w_hat = oracle.dequantize_groups(*wts.o, 128)[7, 19]      # 0.5 after INT4 quantisation
+    assert abs(w_hat - 0.5) <= 0.5 * 2.0 ** -8
+    np.testing.assert_allclose(delta[:, 7], w_hat * r["o"][:, 19], rtol=1e-12)
+
+
+def test_block_gqa_head_mapping():
+    """Query head h reads KV head h // G (contiguous groups, no head expansion).
+
+    KV head 1's history keys are made huge and its values constant, so any query
+    head reading KV head 1 returns (almost exactly) that constant; heads of group 0
+    must not."""
+    w, wts, cache, x = _mini_setup(L=6)
+    s = MINI
+    G = s.n_q // s.n_kv
+    cache.kc[:, 1] = 15
+    cache.ks[:, 1] = 0.0
+    cache.vc[:, 1] = 15                 # decoded value 7 * 0.25 = 1.75 in every rotated channel
+    cache.vs[:, 1] = 0.25
+    # zero keys for KV head 1 history -> uniform attention over history + new token
+    r = decode_block(s, wts, cache, x, np.array([6, 6]), write_cache=False)
+    const = oracle.sylvester(s.hb) @ np.full(s.head_dim, 1.75)
+    for i in range(2):
+        vnew = oracle.dequantize_groups(r["v_codes"][i, 1], r["v_scales"][i, 1], s.kvg)
+        for h in range(G, 2 * G):
+            # scores: history keys decode to 0 -> score 0; the new key has its own score
+            qkv = r["qkv"][i]
+            qt = oracle.blockdiag_apply(oracle.rope_apply(qkv[h * 16:(h + 1) * 16], 6, s.rope_base), s.hb)
+            kn = oracle.dequantize_groups(r["k_codes"][i, 1], r["k_scales"][i, 1], s.kvg)
+            sn = qt @ kn / 4.0
+            p_new = math.exp(sn) / (6 + math.exp(sn))
+            want = (1 - p_new) * const + p_new * (oracle.sylvester(s.hb) @ vnew)
+            np.testing.assert_allclose(r["o"][i, h * 16:(h + 1) * 16], want, rtol=1e-12, atol=1e-13)
+        for h in range(G):
+            assert not np.allclose(r["o"][i, h * 16:(h + 1) * 16], const, atol=1e-3)
+
+
+def _brute_block(shape, wts, cache, x, L):
+    """Explicit-loop evaluation of the block for one request (tiny shapes only)."""
+    s = shape
+    H, d, nq, nkv = s.hidden, s.head_dim, s.n_q, s.n_kv
+    G = nq // nkv
+    W = {k: oracle.dequantize_groups(*getattr(wts, k), 128) for k in ("qkv", "o", "gu", "down")}
+    rho = 1 / math.sqrt(sum(v * v for v in x) / H + s.rms_eps)
+    y = [rho * sum(W["qkv"][r][i] * x[i] for i in range(H)) for r in range(s.n_qkv)]
+
+    def rope(vec):
+        out = [0.0] * d
+        for i in range(d // 2):
+            a = L * s.rope_base ** (-2.0 * i / d)
+            out[i] = vec[i] * math.cos(a) - vec[i + d // 2] * math.sin(a)
+            out[i + d // 2] = vec[i + d // 2] * math.cos(a) + vec[i] * math.sin(a)
+        return out
+
+    def had(vec):
+        n = s.hb
+        out = []
+        for b0 in range(0, d, n):
+            for i in range(n):
+                out.append(sum((-1) ** bin(i & j).count("1") * vec[b0 + j] for j in range(n)) / math.sqrt(n))
+        return out
+
+    def quant(vec):
+        amax = max(abs(v) for v in vec)
+        sc = float(oracle.bf16_rne(np.float32(np.float32(amax) / np.float32(7))))
+        if sc == 0:
+            return [0.0] * len(vec)
+        return [sc * max(-8, min(7, float(np.rint(np.float32(np.float32(v) / np.float32(sc)))))) for v in vec]
+
+    o = []
+    for h in range(nq):
+        j = h // G
+        q = had(rope(y[h * d:(h + 1) * d]))
+        kn = quant(had(rope(y[(nq + j) * d:(nq + j + 1) * d])))
+        vn = quant(had(y[(nq + nkv + j) * d:(nq + nkv + j + 1) * d]))
+        Ks = [list(cache.k_hat(0, j, L)[p]) for p in range(L)] + [kn]
+        Vs = [list(cache.v_hat(0, j, L)[p]) for p in range(L)] + [vn]
+        o += had(_brute_attention(q, Ks, Vs))
+    h1 = [x[r] + sum(W["o"][r][c] * o[c] for c in range(nq * d)) for r in range(H)]
+    rho2 = 1 / math.sqrt(sum(v * v for v in h1) / H + s.rms_eps)
+    gu = [rho2 * sum(W["gu"][r][i] * h1[i] for i in range(H)) for r in range(2 * s.inter)]
+    a = [gu[i] / (1 + math.exp(-gu[i])) * gu[s.inter + i] for i in range(s.inter)]
+    return [h1[r] + sum(W["down"][r][i] * a[i] for i in range(s.inter)) for r in range(H)]
+
+
+def test_block_brute_force_tiny():
+    shape = BlockShape(hidden=128, n_q=16, n_kv=4, head_dim=8, inter=128, rope_base=10000.0)
+    w, wts, cache, x = _mini_setup(shape=shape, B=1, L=3, seed=13)
+    r = decode_block(shape, wts, cache, x, np.array([3]), write_cache=False)
+    want = _brute_block(shape, wts, cache, list(x[0]), 3)
+    np.testing.assert_allclose(r["out"][0], want, rtol=1e-11, atol=1e-12)
