@@ -1,0 +1,413 @@
+"""Benchmark of the INT4-weight / rotated-INT4-KV decode block on GB300.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+One step = one ft_decode_block call (prep, QKV, attention with the new token's
+cache write, O, gate/up + SwiGLU, down) over one batch of seeded synthetic
+inputs of the workload's shape (default: Llama-3-8B layer shape, batch 1,
+context 1024).  The timed region replays a CUDA graph of R consecutive steps
+over R distinct replicas of weights + KV cache + workspace, R chosen so the
+replicas together are >= 4x the L2 size (each step's inputs are cold in L2).
+Rank 0 prints one JSON line.  Under torchrun (N > 1) every rank runs its own
+replica on its own GPU (the path has no cross-GPU exchange: replicas only) and
+the reported time is the maximum over ranks.
+
+--impl reference times the CPU oracle (the reference implementation of this
+build) on the same workload, on the host cores, one bounded sample per step.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np
+
+METRIC = "decode-block µs/step and achieved HBM GB/s (% of GB300 roofline), batch 1–32"
+DEFAULT_WORKLOAD = "8b_b1_ctx1024"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ---------------------------------------------------------------------------- helpers
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f)
+    return {}
+
+
+def hbm_peak() -> tuple[float, str]:
+    pk = measured_peaks()
+    if "hbm_gbs" in pk:
+        return float(pk["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def algorithmic_bytes(shape, B: int, ctx: int) -> dict:
+    """Minimum bytes one step must move: INT4 codes + BF16 group scales of every
+    weight, the KV history read (codes + scales) and the new entry written, and
+    the BF16 activations in and out."""
+    import int4_weight_kv_gb300 as ft
+    cfg = ft.cfg_from_shape(shape)
+    w = {r: ft.ft_packed_weight_bytes(cfg, r) for r in ft.ROLES}
+    kv_tok = shape.n_kv * 2 * (shape.head_dim // 2 + 2 * (shape.head_dim // shape.kvg))
+    kv = B * ctx * kv_tok + B * kv_tok
+    act = B * shape.hidden * 2 * 2
+    return {"weights": sum(w.values()), "per_role": w, "kv": kv, "act": act,
+            "total": sum(w.values()) + kv + act}
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled while the GPU works."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.t:
+            self.t.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------- our arm
+def setup_replicas(wl, R: int, device):
+    import torch
+    import synth
+    import int4_weight_kv_gb300 as ft
+    from int4_weight_kv_gb300 import runtime as rt
+    s = wl.shape
+    cfg = ft.cfg_from_shape(s)
+    w = synth.layer_weights(s, wl.config_id, 0)
+    packed = rt.pack_layer(cfg, w, device=device)
+    del w
+    B, ctx = wl.batch, wl.ctx
+    max_ctx = ctx + 1
+    kb, _ = synth.kv_history(s, wl.config_id, B, ctx, which="k")
+    vb, _ = synth.kv_history(s, wl.config_id, B, ctx, which="v")
+    cache = rt.alloc_cache(cfg, B, max_ctx, device=device)
+    rt.fill_history(cfg, cache, B, max_ctx, kb, vb)
+    del kb, vb
+    xb, _ = synth.activations(s, wl.config_id, B)
+    reps = []
+    for r in range(R):
+        reps.append({
+            "w": packed if r == 0 else {k: v.clone() for k, v in packed.items()},
+            "cache": cache if r == 0 else cache.clone(),
+            "x": rt.bits_tensor(xb, device=device),
+            "y": torch.empty((B, s.hidden), dtype=torch.int16, device=device),
+            "ws": rt.alloc_workspace(cfg, B, max_ctx, device=device),
+        })
+    pos = torch.full((B,), ctx, dtype=torch.int32, device=device)
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    return cfg, reps, pos, status, max_ctx, xb
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    import synth
+    import int4_weight_kv_gb300 as ft
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    from int4_weight_kv_gb300 import build
+    if rank == 0 or world == 1:
+        build.build()
+    if world > 1:
+        dist.barrier(device_ids=[local])
+    ft.lib()
+
+    wl = synth.workload(args.workload)
+    s, B, ctx = wl.shape, wl.batch, wl.ctx
+    ab = algorithmic_bytes(s, B, ctx)
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    footprint = ab["weights"] + ab["kv"]
+    R = max(2, int(np.ceil(4 * l2 / footprint)))
+    cfg, reps, pos, status, max_ctx, xb = setup_replicas(wl, R, device)
+    stream = torch.cuda.current_stream(device)
+
+    def step(r):
+        p = reps[r]
+        ft.check(ft.ft_decode_block(cfg, p["w"], p["cache"], B, max_ctx, p["x"], p["y"], ft.FT_BF16, pos, B, p["ws"],
+                                    status), "ft_decode_block")
+
+    for r in range(R):     # eager warm-up: sets kernel attributes before capture
+        step(r)
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream(device)
+    side.wait_stream(stream)
+    graphs = {}
+
+    def graph_of(n):
+        if n not in graphs:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                for i in range(n):
+                    step(i % R)
+            graphs[n] = g
+        return graphs[n]
+
+    def run_steps(k):
+        full, rem = divmod(k, R)
+        for _ in range(full):
+            graph_of(R).replay()
+        if rem:
+            graph_of(rem).replay()
+
+    run_steps(max(args.warmup, 3))
+    torch.cuda.synchronize()
+
+    # timed region: exactly K steps, barrier + synchronize on both sides
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier(device_ids=[local])
+    torch.cuda.synchronize()
+    e0.record(stream)
+    run_steps(args.steps)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier(device_ids=[local])
+    ms = e0.elapsed_time(e1)
+    # keep the GPU under the same load long enough for the clock sampler
+    t_end = time.time() + max(0.0, 1.0 - ms / 1000.0)
+    while time.time() < t_end:
+        run_steps(R * 50)
+        torch.cuda.synchronize()
+    clk = clocks.stop()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {status.item()}")
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms = float(t.item())
+    us_step = ms * 1000.0 / args.steps
+
+    # dominant kernel (gate/up projection) timed alone with CUDA events on its stream
+    dom_role = max(ab["per_role"], key=lambda r: ab["per_role"][r])
+    stage = {ft.FT_W_QKV: ft.FT_STAGE_QKV, ft.FT_W_O: ft.FT_STAGE_O, ft.FT_W_GATEUP: ft.FT_STAGE_GU,
+             ft.FT_W_DOWN: ft.FT_STAGE_DOWN}[dom_role]
+    n_dom = max(R * 20, min(args.steps, 2000))
+    for i in range(R):
+        p = reps[i]
+        ft.check(ft.ft_decode_block_stages(cfg, p["w"], p["cache"], B, max_ctx, p["x"], p["y"], ft.FT_BF16, pos, B,
+                                           p["ws"], stage, status))
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for i in range(n_dom):
+        p = reps[i % R]
+        ft.ft_decode_block_stages(cfg, p["w"], p["cache"], B, max_ctx, p["x"], p["y"], ft.FT_BF16, pos, B, p["ws"],
+                                  stage, status)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    dom_us = e0.elapsed_time(e1) * 1000.0 / n_dom
+    dom_bytes = ab["per_role"][dom_role] + B * (s.hidden * 2 + s.inter * 2)
+    peak, peak_kind = hbm_peak()
+    achieved = dom_bytes / dom_us / 1e3
+    traffic = None
+    tr_path = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tr_path):
+        with open(tr_path) as f:
+            traffic = json.load(f).get(args.workload)
+
+    # end to end through the C ABI with host buffers (pinned), copies inside the timed region
+    n_e2e = min(args.steps, 500)
+    x_host = torch.from_numpy(np.ascontiguousarray(xb).view(np.int16)).pin_memory()
+    pos_host = torch.full((B,), ctx, dtype=torch.int32).pin_memory()
+    y_host = torch.empty((B, s.hidden), dtype=torch.int16).pin_memory()
+    for i in range(R):
+        step(i)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for i in range(n_e2e):
+        p = reps[i % R]
+        p["x"].copy_(x_host, non_blocking=True)
+        pos.copy_(pos_host, non_blocking=True)
+        step(i % R)
+        y_host.copy_(p["y"], non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_us = e0.elapsed_time(e1) * 1000.0 / n_e2e
+
+    line = {
+        "metric": METRIC, "value": round(us_step, 3), "unit": "us/step", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": us_step / 1000.0, "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16", "data": "synthetic (seeded N(0,0.02) weights, outlier-laden BF16 "
+                                                  "activations and K/V history)",
+        "config": {"workload": args.workload, "hidden": s.hidden, "n_q": s.n_q, "n_kv": s.n_kv,
+                   "head_dim": s.head_dim, "inter": s.inter, "batch": B, "ctx": ctx, "replicas": R,
+                   "l2": f"inputs larger than L2: {R} replicas of weights+KV ({R * footprint / 1e6:.0f} MB) cycled",
+                   "graph": True, "pdl": True, "precision": "INT4 weights and KV (BF16 scales), FP16 MMA "
+                                                            "operands, FP32 accumulate, BF16 block I/O"},
+        "block_gbs": round(ab["total"] / us_step / 1e3, 1),
+        "pct_of_8tbs": round(100.0 * ab["total"] / us_step / 1e3 / NOMINAL_HBM_GBS, 1),
+        "pct_of_measured_hbm": round(100.0 * ab["total"] / us_step / 1e3 / peak, 1),
+        "algorithmic_bytes_per_step": ab["total"],
+        "roofline": {"bound": "hbm", "kernel": "gemv_kernel (gate/up + SwiGLU)", "achieved": round(achieved, 1),
+                     "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 3), "traffic": traffic,
+                     "peak_kind": f"{peak_kind} copy bandwidth (burst; kernel timed alone)",
+                     "launch_us": round(dom_us, 3), "algorithmic_bytes": dom_bytes},
+        "e2e": {"value": round(e2e_us, 3), "unit": "us/step", "h2d_bytes_per_step": B * s.hidden * 2 + B * 4,
+                "d2h_bytes_per_step": B * s.hidden * 2},
+        "gpu_launches": ft.ft_decode_block_launches() * args.steps,
+        "clocks": clk,
+    }
+    if rank == 0:
+        line["cpu_baseline"] = cpu_baseline(wl)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier(device_ids=[local])
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------- oracle timing
+def _oracle_inputs(wl):
+    import synth
+    from oracle.block import BlockWeightsOracle
+    from oracle.kv import KVCacheOracle
+    s = wl.shape
+    w = synth.layer_weights(s, wl.config_id, 0)
+    wts = BlockWeightsOracle(s, w)
+    B, ctx = wl.batch, wl.ctx
+    kb, kf = synth.kv_history(s, wl.config_id, B, ctx, which="k")
+    vb, vf = synth.kv_history(s, wl.config_id, B, ctx, which="v")
+    cache = KVCacheOracle(B, s.n_kv, ctx + 1, s.head_dim, s.hb, s.kvg)
+    cache.append(kf, vf, np.zeros(B, int))
+    _, x = synth.activations(s, wl.config_id, B)
+    return wts, cache, x.astype(np.float64), np.full(B, ctx, np.int32)
+
+
+def oracle_sample_us(wl, inputs, rows=1) -> tuple[float, str]:
+    """One bounded sample of the oracle: the full block for `rows` request(s),
+    scaled to the whole batch (requests are independent)."""
+    from oracle.block import decode_block
+    wts, cache, x, pos = inputs
+    t0 = time.perf_counter()
+    decode_block(wl.shape, wts, cache, x, pos, batch_idx=list(range(min(rows, wl.batch))), write_cache=False)
+    dt = time.perf_counter() - t0
+    n = min(rows, wl.batch)
+    return dt * 1e6 * wl.batch / n, f"full FP64 oracle block for {n} of {wl.batch} request(s), scaled to the batch"
+
+
+def _cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(wl) -> dict:
+    inputs = _oracle_inputs(wl)
+    us, sample = oracle_sample_us(wl, inputs)
+    return {"value": round(us, 1), "unit": "us/step", "cores": _cores(), "kind": "oracle", "sample": sample}
+
+
+def run_reference(args):
+    import synth
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    wl = synth.workload(args.workload)
+    inputs = _oracle_inputs(wl)
+    for _ in range(max(0, min(args.warmup, 1))):
+        oracle_sample_us(wl, inputs)
+    # each step is one bounded sample; cap the run at a few minutes of CPU time
+    budget_s, times, sample = 150.0, [], ""
+    t_start = time.perf_counter()
+    for i in range(args.steps):
+        us, sample = oracle_sample_us(wl, inputs)
+        times.append(us)
+        if time.perf_counter() - t_start > budget_s:
+            break
+    val = float(np.mean(times))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(val, 1), "unit": "us/step", "n_gpus": 1,
+        "steps": len(times), "warmup": args.warmup, "ms_per_step": val / 1000.0, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "hidden": wl.shape.hidden, "batch": wl.batch, "ctx": wl.ctx},
+        "cpu_baseline": {"value": round(val, 1), "unit": "us/step", "cores": _cores(), "kind": "oracle",
+                         "sample": sample + (f"; {len(times)} of {args.steps} steps within {budget_s:.0f} s"
+                                             if len(times) < args.steps else "")},
+        "e2e": {"value": round(val, 1), "unit": "us/step", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

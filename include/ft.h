@@ -1,0 +1,206 @@
+/*
+ * ft.h -- C ABI of the INT4-weight / Hadamard-rotated INT4-KV decode block.
+ *
+ * One Llama-style Transformer block, one new token per request, on one GPU
+ * (sm_103a).  The operations follow the statement of the problem on the pages
+ * "FuTransformer: FP8 prefill and INT4 decode for Llama-style inference on
+ * Hopper" (summary page on onedev.kr, sections "어떻게 동작하나" / how it
+ * works, "무엇과 다른가" / what differs, "전제와 한계" / premises and limits).
+ *
+ * Conventions (all calls):
+ *  - Every pointer argument is a DEVICE pointer unless stated otherwise.  The
+ *    caller allocates and owns all memory; the library never allocates.
+ *  - Calls are asynchronous on the caller's stream and return an ft_status
+ *    code.  Host-side argument checks happen before anything is enqueued; a
+ *    failed check enqueues nothing.
+ *  - Conditions only the device can see (a position beyond the cache capacity,
+ *    an activation outside the FP16 range, a bounded wait that ran out) are
+ *    OR-ed into the caller's int32 device status word (may be NULL) as
+ *    FT_DEV_* bits; read it after synchronising.  Kernels never trap.
+ *  - No exception or abort crosses this boundary.
+ */
+#ifndef FT_H_
+#define FT_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t; 0 is the legacy default stream. */
+typedef struct CUstream_st *ft_stream;
+
+/* ---- status codes ------------------------------------------------------ */
+enum {
+  FT_OK = 0,
+  FT_ERR_INVALID_ARG = -1, /* NULL/misaligned pointer, bad size, overlap    */
+  FT_ERR_UNSUPPORTED = -2, /* shape or option this build does not implement */
+  FT_ERR_WORKSPACE = -3,   /* workspace or packed buffer too small          */
+  FT_ERR_CAPACITY = -4,    /* batch larger than the cache's max_batch       */
+  FT_ERR_CUDA = -5         /* a CUDA runtime call failed (launch, attrs)    */
+};
+
+/* bits OR-ed into the device status word */
+enum {
+  FT_DEV_CAPACITY = 1, /* pos[b] (+T) outside [0, max_ctx): that request skipped */
+  FT_DEV_TIMEOUT = 2,  /* a bounded pipeline wait ran out; outputs invalid       */
+  FT_DEV_RANGE = 4     /* an activation exceeded the FP16 operand range          */
+};
+
+/* activation dtypes of the block input/output */
+enum { FT_BF16 = 0, FT_F32 = 1 };
+
+/* ---- configuration ------------------------------------------------------ */
+typedef struct {
+  int32_t hidden;    /* H; multiple of 128                                      */
+  int32_t n_q;       /* query heads; multiple of n_kv, n_q / n_kv <= 8          */
+  int32_t n_kv;      /* KV heads                                               */
+  int32_t head_dim;  /* d in {64, 128}                                          */
+  int32_t inter;     /* SwiGLU intermediate I; multiple of 128                  */
+  int32_t w_group;   /* weight group along the input axis; must be 128         */
+  int32_t had_block; /* Hadamard block h_b: power of two dividing d (1 = none) */
+  int32_t kv_group;  /* channels per KV scale; must equal head_dim             */
+  float rms_eps;     /* RMSNorm epsilon                                        */
+  float rope_base;   /* RoPE base                                              */
+} ft_block_cfg;
+
+/* Projection roles.  Weights are given in the logical row-major [N_out, K_in]
+ * orientation:  QKV [(n_q+2 n_kv) d, H] (q rows, then k, then v);
+ * O [H, n_q d];  GATEUP [2 I, H] (I gate rows, then I up rows);  DOWN [H, I]. */
+typedef enum { FT_W_QKV = 0, FT_W_O = 1, FT_W_GATEUP = 2, FT_W_DOWN = 3 } ft_wrole;
+
+/* Describes a status code; never NULL. */
+const char *ft_status_string(int status);
+
+/* Host-only check of a configuration (FT_OK, FT_ERR_INVALID_ARG, FT_ERR_UNSUPPORTED). */
+int ft_validate_cfg(const ft_block_cfg *cfg);
+
+/* Logical shape [n_out, k_in] of a role's weight matrix (host pointers out). */
+int ft_weight_shape(const ft_block_cfg *cfg, int role, int32_t *n_out, int32_t *k_in);
+
+/* ---- weights ------------------------------------------------------------
+ * Packing (summary page, "어떻게 동작하나": the fixed RMSNorm gain is folded
+ * into the weights before quantisation, W' = gamma W; "무엇과 다른가": INT4
+ * values with group scales applied after accumulation, stored in the order the
+ * kernel consumes them).  For each output row o and each group of 128
+ * consecutive input channels: W'[o,i] = W[o,i] * gamma[i] (FP32 product),
+ * s = bf16_rne(amax / 7), code = clamp(rne(W' / s), -8, 7) + 8 (FP32
+ * decisions; s = 0 gives code 8).  The packed buffer is opaque: 128-row blocks,
+ * 16-row tiles, per (tile, group) 1024 bytes of nibbles in the tensor-core
+ * fragment order the decode kernels read, followed by the 16 BF16 scales. */
+
+/* Bytes of one packed role (codes P/2 + scales P/64 for P = N_out * K_in). */
+size_t ft_packed_weight_bytes(const ft_block_cfg *cfg, int role);
+
+/* W: FP32 [N_out, K_in] row-major.  gamma: FP32 [K_in] or NULL (treated as 1);
+ * use gamma_attn for QKV and gamma_ffn for GATEUP.  packed: >= 16-byte aligned,
+ * packed_bytes >= ft_packed_weight_bytes().  Overwrites packed entirely. */
+int ft_pack_weights_int4(const ft_block_cfg *cfg, int role, const float *W, const float *gamma,
+                         void *packed, size_t packed_bytes, ft_stream stream);
+
+/* Inverse view for tests: codes uint8 [N_out, K_in] in [0,15] (value code-8)
+ * and scales as BF16 bits [N_out, K_in/128], logical orientation. */
+int ft_unpack_weights_int4(const ft_block_cfg *cfg, int role, const void *packed, uint8_t *codes,
+                           uint16_t *scales_bf16, ft_stream stream);
+
+/* ---- KV cache -----------------------------------------------------------
+ * One layer's cache for max_batch requests x n_kv heads x max_ctx positions.
+ * Entry (request, head, position) holds d/2 bytes of K nibbles, d/2 bytes of V
+ * nibbles and one BF16 scale each for K and V (kv_group = d), addressed by
+ * offset(request, head, position, channel) (summary page, "어떻게 동작하나":
+ * direct placement, no dense K/V tensors).  Within an entry the nibbles are
+ * permuted into the tensor-core fragment order of the attention kernel; the
+ * buffer is opaque to callers. */
+
+size_t ft_kv_cache_bytes(const ft_block_cfg *cfg, int max_batch, int max_ctx);
+
+/* Append T tokens per request (summary page, "무엇과 다른가": block-diagonal
+ * Hadamard rotation of the new K and V, then INT4 quantisation with BF16
+ * scales; H is the normalised Sylvester matrix of order had_block).
+ * k_bf16, v_bf16: BF16 bits [B, T, n_kv, d] (post-RoPE).  pos: device int32
+ * [B], first position of request b.  Positions pos[b]..pos[b]+T-1 are written;
+ * a request with pos[b] < 0 or pos[b]+T > max_ctx is skipped and sets
+ * FT_DEV_CAPACITY.  B <= max_batch or FT_ERR_CAPACITY. */
+int ft_kv_append_int4(const ft_block_cfg *cfg, void *cache, int max_batch, int max_ctx,
+                      const uint16_t *k_bf16, const uint16_t *v_bf16, const int32_t *pos, int B,
+                      int T, int32_t *dev_status, ft_stream stream);
+
+/* Inverse view for tests: positions [0, len) of requests [0, B).  codes uint8
+ * [B, n_kv, len, d] in logical channel order; scales BF16 bits [B, n_kv, len, 1]. */
+int ft_kv_unpack_int4(const ft_block_cfg *cfg, const void *cache, int max_batch, int max_ctx, int B,
+                      int len, uint8_t *k_codes, uint8_t *v_codes, uint16_t *k_scales,
+                      uint16_t *v_scales, ft_stream stream);
+
+/* ---- the decode block ---------------------------------------------------
+ * One token per request b < B at position pos[b] (= L_b, its history length):
+ *   rho1 = (mean x^2 + eps)^-1/2;  [q;k;v] = rho1 * W'_qkv x      (row factor
+ *      applied after the projection's accumulation, "어떻게 동작하나")
+ *   RoPE(q, k) at L_b;  k~ = H k, v~ = H v quantised and written at L_b
+ *   q~ = H q;  per query head h (KV head h / G, no head expansion,
+ *      "전제와 한계"): softmax over positions 0..L_b of q~.k^/sqrt(d) against
+ *      the INT4 cache (split across CTAs and merged for long contexts,
+ *      "무엇과 다른가"), o = H o~ (inverse rotation)
+ *   h1 = x + W_o o;  rho2 = (mean h1^2 + eps)^-1/2;
+ *   a = silu(rho2 W'_g h1) * (rho2 W'_u h1);  out = h1 + W_down a.
+ * The new token's K/V are written before attending; attention covers
+ * positions 0..pos[b] inclusive; the caller advances pos.
+ * x_in, x_out: [B, H] of act_dtype (FT_BF16 bits or FT_F32), must not overlap.
+ * Arithmetic: tensor-core FP16 operands (codes exact, activations rounded to
+ * FP16), FP32 accumulation, epilogues and softmax.  Activations must stay
+ * within the FP16 range (|x| < 65504; FT_DEV_RANGE otherwise).
+ * 1 <= B <= min(32, max_batch); larger B -> FT_ERR_UNSUPPORTED. */
+typedef struct {
+  const void *qkv, *o, *gateup, *down; /* each from ft_pack_weights_int4 */
+} ft_layer_weights;
+
+size_t ft_decode_workspace_bytes(const ft_block_cfg *cfg, int B, int max_ctx);
+
+int ft_decode_block(const ft_block_cfg *cfg, const ft_layer_weights *w, void *cache, int max_batch,
+                    int max_ctx, const void *x_in, void *x_out, int act_dtype, const int32_t *pos,
+                    int B, void *workspace, size_t ws_bytes, int32_t *dev_status, ft_stream stream);
+
+/* Stage selection for ft_decode_block_stages (bit mask). */
+enum {
+  FT_STAGE_PREP = 1,  /* input -> FP16 operand, rho1, zero the counters      */
+  FT_STAGE_QKV = 2,   /* QKV projection (x rho1)                             */
+  FT_STAGE_ATTN = 4,  /* RoPE, rotation, cache write, split-KV attention     */
+  FT_STAGE_O = 8,     /* O projection + residual                              */
+  FT_STAGE_GU = 16,   /* gate/up projection + SwiGLU                          */
+  FT_STAGE_DOWN = 32, /* down projection + residual -> x_out                  */
+  FT_STAGE_ALL = 63
+};
+
+/* Runs a subset of the block's stages on a workspace left by a previous full
+ * call with the same arguments (each stage reads what the earlier stages
+ * wrote there).  Used to time one stage alone; FT_STAGE_ALL equals
+ * ft_decode_block. */
+int ft_decode_block_stages(const ft_block_cfg *cfg, const ft_layer_weights *w, void *cache,
+                           int max_batch, int max_ctx, const void *x_in, void *x_out, int act_dtype,
+                           const int32_t *pos, int B, void *workspace, size_t ws_bytes,
+                           int32_t *dev_status, unsigned stage_mask, ft_stream stream);
+
+/* Byte offsets of intermediate tensors inside the workspace (host struct out),
+ * for tests:  qkv FP32 [B, (n_q+2n_kv) d] (rho1 applied, before RoPE);
+ * o FP16 [B, n_q d] (attention output after the inverse rotation);
+ * h1 FP32 [B, H];  a FP16 [B, I]. */
+typedef struct {
+  size_t qkv, o, h1, a;
+  int32_t n_split; /* split-KV chunks per (request, KV head) */
+} ft_ws_layout;
+
+int ft_decode_workspace_layout(const ft_block_cfg *cfg, int B, int max_ctx, ft_ws_layout *out);
+
+/* Number of kernels one ft_decode_block call launches. */
+int ft_decode_block_launches(void);
+
+/* Programmatic dependent launch between the block's kernels (default on).
+ * Returns the previous setting. */
+int ft_set_pdl(int enabled);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FT_H_ */

@@ -1,0 +1,341 @@
+// Internal helpers shared by the library's kernels: inline-PTX wrappers for
+// sm_103a (bulk async copies, mbarriers, programmatic dependent launch,
+// tensor-core MMA, warp matrix transpose), nibble decoding, the packed-weight
+// and KV-entry layouts, and host-side launch utilities.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "ft.h"
+
+namespace ft {
+
+// ------------------------------------------------------------------ layout
+constexpr int kWGroup = 128;         // weight group along the input axis
+constexpr int kRowTile = 16;         // rows per MMA tile
+constexpr int kRowBlock = 128;       // rows per packed row block (8 tiles)
+constexpr int kTilesPerBlock = 8;
+constexpr int kSlabCodes = 1024;     // nibbles of one (row tile, group): 16 x 128 / 2
+constexpr int kSlabBytes = 1056;     // + 16 BF16 scales
+constexpr int kBlockGroupBytes = kTilesPerBlock * kSlabBytes;  // one (row block, group)
+
+// bounded waits: a wait that exceeds this many nanoseconds gives up
+constexpr unsigned long long kWaitLimitNs = 4000000000ull;
+
+// ------------------------------------------------------------------ PTX
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long globaltimer() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_fence_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+// Waits for the phase with the given parity to complete; false on timeout.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 255u) == 0 && globaltimer() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+// 1-D bulk copy global -> shared, completion signalled on an mbarrier.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// Streamed read-once data (KV cache): skip L1.
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint2 ld_stream_v2(const void* p) {
+  uint2 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_stream_u32(const void* p) {
+  uint32_t v;
+  asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+__device__ __forceinline__ uint16_t ld_stream_u16(const void* p) {
+  uint16_t v;
+  asm volatile("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(v) : "l"(p));
+  return v;
+}
+// Data written by an earlier kernel of the same dependent chain or by another
+// CTA of this kernel: read at L2 (coherent point), never from L1.
+__device__ __forceinline__ float ld_cg_f32(const float* p) { return __ldcg(p); }
+
+// D = A(16x16, f16, row) * B(16x8, f16, col) + C  (FP32 accumulate)
+__device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// Same with C = 0.
+__device__ __forceinline__ void mma_f16_zc(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%10,%10,%10,%10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.0f));
+}
+
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t lop3_or_and(uint32_t x, uint32_t mask, uint32_t orv) {
+  // (x & mask) | orv
+  uint32_t r;
+  asm("lop3.b32 %0, %1, %2, %3, 0xea;" : "=r"(r) : "r"(x), "r"(mask), "r"(orv));
+  return r;
+}
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
+}
+__device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+__device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t r;
+  asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+  return r;
+}
+
+// Nibble decode.  The 4-bit code c sits in the mantissa of FP16 1024.0
+// (0x6400), whose mantissa step is 1, giving 1024 + c; subtracting 1032 yields
+// c - 8 exactly.  A nibble at bits 4..7 of a 16-bit half lands as 1024 + 16c,
+// which (v / 16) - 72 maps to c - 8 exactly.  From one 32-bit word with
+// nibbles n0..n7 (bits 4i..4i+3) this yields four f16x2 registers:
+//   r0 = (n0, n4) - 8,  r1 = (n1, n5) - 8,  r2 = (n2, n6) - 8,  r3 = (n3, n7) - 8
+// (low half first).
+constexpr uint32_t kH1024 = 0x64006400u;   // (1024, 1024)
+constexpr uint32_t kH1032 = 0x64086408u;   // (1032, 1032)
+constexpr uint32_t kH1_16 = 0x2C002C00u;   // (1/16, 1/16)
+constexpr uint32_t kHm72 = 0xD480D480u;    // (-72, -72)
+
+__device__ __forceinline__ void dequant_word(uint32_t w, uint32_t (&r)[4]) {
+  const uint32_t w8 = w >> 8;
+  r[0] = hsub2(lop3_or_and(w, 0x000F000Fu, kH1024), kH1032);
+  r[1] = hfma2(lop3_or_and(w, 0x00F000F0u, kH1024), kH1_16, kHm72);
+  r[2] = hsub2(lop3_or_and(w8, 0x000F000Fu, kH1024), kH1032);
+  r[3] = hfma2(lop3_or_and(w8, 0x00F000F0u, kH1024), kH1_16, kHm72);
+}
+
+// ------------------------------------------------------------------ packed weights
+// Nibble i of the word for (lane = 4g + tig, k-step ks) of a row tile holds
+// row  g + (i & 1 ? 8 : 0)  and column  16 ks + 2 tig + (i & 2 ? 8 : 0) + (i & 4 ? 1 : 0),
+// which dequant_word() turns into the m16n8k16 A-fragment {a0, a1, a2, a3}.
+__host__ __device__ __forceinline__ int wslab_word_offset(int lane, int ks) {
+  return (ks >> 2) * 512 + lane * 16 + (ks & 3) * 4;
+}
+__host__ __device__ __forceinline__ int wnib_row(int g, int i) { return g + ((i & 1) ? 8 : 0); }
+__host__ __device__ __forceinline__ int wnib_col(int ks, int tig, int i) {
+  return 16 * ks + 2 * tig + ((i & 2) ? 8 : 0) + ((i & 4) ? 1 : 0);
+}
+
+// Logical row of packed row r (0..15) of global row tile T for a role.
+__host__ __device__ __forceinline__ int64_t packed_row_to_logical(int role, int inter, int64_t T, int r) {
+  if (role == FT_W_GATEUP) return (r < 8) ? (8 * T + r) : (int64_t)inter + 8 * T + (r - 8);
+  return T * kRowTile + r;
+}
+
+// ------------------------------------------------------------------ KV entries
+// K entry (d/2 bytes): chunk tig (d/8 bytes) word j, nibble i holds channel
+//   16 (2j + ((i >> 1) & 1)) + 2 tig + (i & 1 ? 8 : 0) + ((i >> 2) & 1)
+// V entry (d/2 bytes): chunk g (d/16 bytes) word j, nibble i holds channel
+//   16 (4j + (i >> 1)) + g + (i & 1 ? 8 : 0)
+__host__ __device__ __forceinline__ int kv_k_channel(int tig, int j, int i) {
+  return 16 * (2 * j + ((i >> 1) & 1)) + 2 * tig + ((i & 1) ? 8 : 0) + ((i >> 2) & 1);
+}
+__host__ __device__ __forceinline__ int kv_v_channel(int g, int j, int i) {
+  return 16 * (4 * j + (i >> 1)) + g + ((i & 1) ? 8 : 0);
+}
+
+struct KVLayout {
+  int d, nkv, max_batch, max_ctx;
+  size_t entry;        // d/2 bytes of one K (or V) entry
+  size_t kc, vc, ks, vs, total;
+  __host__ __device__ size_t row(int b, int h, int p) const {
+    return ((size_t)(b * nkv + h) * (size_t)max_ctx + (size_t)p);
+  }
+};
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+inline KVLayout kv_layout(const ft_block_cfg& c, int max_batch, int max_ctx) {
+  KVLayout L;
+  L.d = c.head_dim;
+  L.nkv = c.n_kv;
+  L.max_batch = max_batch;
+  L.max_ctx = max_ctx;
+  L.entry = (size_t)c.head_dim / 2;
+  const size_t n = (size_t)max_batch * c.n_kv * (size_t)max_ctx;
+  L.kc = 0;
+  L.vc = align_up(n * L.entry, 256);
+  L.ks = L.vc + align_up(n * L.entry, 256);
+  L.vs = L.ks + align_up(n * 2, 256);
+  L.total = L.vs + align_up(n * 2, 256);
+  return L;
+}
+
+// ------------------------------------------------------------------ misc device
+__device__ __forceinline__ void set_status(int32_t* st, int bits) {
+  if (st) atomicOr(st, bits);
+}
+
+__device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
+
+// Symmetric INT4 quantiser decision (FP32): s = bf16_rne(amax / 7); code =
+// clamp(rne(x / s), -8, 7) + 8; s = 0 gives code 8.
+__device__ __forceinline__ uint16_t quant_scale_bits(float amax) {
+  const float q = __fdiv_rn(amax, 7.0f);
+  return __bfloat16_as_ushort(__float2bfloat16_rn(q));
+}
+__device__ __forceinline__ uint32_t quant_code(float x, float s) {
+  if (s == 0.0f) return 8u;
+  float t = rintf(__fdiv_rn(x, s));
+  t = fminf(fmaxf(t, -8.0f), 7.0f);
+  return (uint32_t)((int)t + 8);
+}
+
+// Fast Walsh-Hadamard transform of a d-vector held stride-32 across a warp:
+// lane l owns channels l + 32 m (m < NPL = d / 32).  Butterflies for strides
+// < hb give the natural-order Sylvester transform on each hb block; the
+// result is scaled by 1 / sqrt(hb).
+template <int NPL>
+__device__ __forceinline__ void warp_fwht(float (&v)[NPL], int hb) {
+  const int lane = threadIdx.x & 31;
+  for (int s = 1; s < hb && s < 32; s <<= 1) {
+#pragma unroll
+    for (int m = 0; m < NPL; ++m) {
+      const float o = __shfl_xor_sync(0xffffffffu, v[m], s);
+      v[m] = (lane & s) ? (o - v[m]) : (v[m] + o);
+    }
+  }
+#pragma unroll
+  for (int sm = 1; sm < NPL; sm <<= 1) {
+    if (sm * 32 >= hb) break;
+#pragma unroll
+    for (int m = 0; m < NPL; ++m) {
+      if (m & sm) continue;
+      const float a = v[m], b = v[m + sm];
+      v[m] = a + b;
+      v[m + sm] = a - b;
+    }
+  }
+  const float sc = __frsqrt_rn((float)hb);
+#pragma unroll
+  for (int m = 0; m < NPL; ++m) v[m] *= sc;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Quantise one rotated d-vector (stride-32 ownership, kv_group = d) and write
+// its K- or V-entry nibbles and BF16 scale.  Returns the decoded values
+// (c - 8) * s in v.  `codes` is a warp-private staging area of d bytes.
+template <int NPL>
+__device__ __forceinline__ void warp_quant_store(float (&v)[NPL], bool is_k, uint8_t* codes,
+                                                 uint8_t* entry, uint16_t* scale_out) {
+  const int lane = threadIdx.x & 31;
+  constexpr int D = NPL * 32;
+  float am = 0.0f;
+#pragma unroll
+  for (int m = 0; m < NPL; ++m) am = fmaxf(am, fabsf(v[m]));
+  am = warp_max(am);
+  const uint16_t sb = quant_scale_bits(am);
+  const float s = bf16_bits_to_f32(sb);
+#pragma unroll
+  for (int m = 0; m < NPL; ++m) {
+    const uint32_t c = quant_code(v[m], s);
+    codes[lane + 32 * m] = (uint8_t)c;
+    v[m] = (float)((int)c - 8) * s;
+  }
+  __syncwarp();
+  constexpr int WORDS = D / 8;  // 32-bit words per entry
+  if (lane < WORDS) {
+    uint32_t w = 0;
+    if (is_k) {
+      const int tig = lane / (D / 32), j = lane % (D / 32);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) w |= (uint32_t)codes[kv_k_channel(tig, j, i)] << (4 * i);
+      *reinterpret_cast<uint32_t*>(entry + tig * (D / 8) + 4 * j) = w;
+    } else {
+      const int g = lane / (D / 64), j = lane % (D / 64);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) w |= (uint32_t)codes[kv_v_channel(g, j, i)] << (4 * i);
+      *reinterpret_cast<uint32_t*>(entry + g * (D / 16) + 4 * j) = w;
+    }
+  }
+  if (lane == 0) *scale_out = sb;
+  __syncwarp();
+}
+
+}  // namespace ft
+
+// ------------------------------------------------------------------ host utils
+namespace ft_host {
+
+int num_sms();
+bool pdl_enabled();
+int check_cfg(const ft_block_cfg* c);
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace ft_host

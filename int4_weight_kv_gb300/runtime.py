@@ -1,0 +1,60 @@
+"""Device-memory helpers around the C ABI: allocate packed weights, the KV
+cache and the workspace with PyTorch, and fill them through the library's own
+entry points.  No arithmetic of the method happens here."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import (FT_W_QKV, FT_W_O, FT_W_GATEUP, FT_W_DOWN, check, ft_decode_workspace_bytes, ft_kv_append_int4,
+               ft_kv_cache_bytes, ft_pack_weights_int4, ft_packed_weight_bytes)
+
+ROLE_KEYS = {FT_W_QKV: ("wqkv", "gamma_attn"), FT_W_O: ("wo", None), FT_W_GATEUP: ("wgu", "gamma_ffn"),
+             FT_W_DOWN: ("wdown", None)}
+ROLE_NAMES = {FT_W_QKV: "qkv", FT_W_O: "o", FT_W_GATEUP: "gateup", FT_W_DOWN: "down"}
+
+
+def _dev(a, dtype=None, device="cuda"):
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    if dtype is not None:
+        t = t.to(dtype)
+    return t.to(device)
+
+
+def pack_layer(cfg, w: dict, device="cuda", stream=None) -> dict:
+    """Pack the four projections of one layer from FP32 host arrays (synth layout)."""
+    out = {}
+    for role, (wk, gk) in ROLE_KEYS.items():
+        W = _dev(w[wk], device=device)
+        g = _dev(w[gk], device=device) if gk else None
+        packed = torch.empty(ft_packed_weight_bytes(cfg, role), dtype=torch.uint8, device=device)
+        check(ft_pack_weights_int4(cfg, role, W, g, packed, stream), "ft_pack_weights_int4")
+        out[ROLE_NAMES[role]] = packed
+        del W, g
+    return out
+
+
+def alloc_cache(cfg, max_batch: int, max_ctx: int, device="cuda") -> torch.Tensor:
+    return torch.zeros(ft_kv_cache_bytes(cfg, max_batch, max_ctx), dtype=torch.uint8, device=device)
+
+
+def alloc_workspace(cfg, B: int, max_ctx: int, device="cuda") -> torch.Tensor:
+    return torch.empty(ft_decode_workspace_bytes(cfg, B, max_ctx), dtype=torch.uint8, device=device)
+
+
+def bits_tensor(bits: np.ndarray, device="cuda") -> torch.Tensor:
+    """uint16 BF16 bit patterns -> int16 device tensor (same bytes)."""
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device)
+
+
+def fill_history(cfg, cache, max_batch, max_ctx, k_bits: np.ndarray, v_bits: np.ndarray, status=None,
+                 stream=None, chunk: int = 4096) -> None:
+    """Append a [B, T, n_kv, d] BF16 history at positions 0..T-1 through ft_kv_append_int4."""
+    B, T = k_bits.shape[:2]
+    for t0 in range(0, T, chunk):
+        t1 = min(T, t0 + chunk)
+        k = bits_tensor(k_bits[:, t0:t1])
+        v = bits_tensor(v_bits[:, t0:t1])
+        pos = torch.full((B,), t0, dtype=torch.int32, device=k.device)
+        check(ft_kv_append_int4(cfg, cache, max_batch, max_ctx, k, v, pos, B, t1 - t0, status, stream),
+              "ft_kv_append_int4")

@@ -1,0 +1,116 @@
+"""The C-ABI library loads, exports every symbol include/ft.h declares, and its
+host-side size queries and argument checks behave (no GPU needed: every call
+here returns before touching the device)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def ft():
+    from int4_weight_kv_gb300 import build as b
+    b.build()
+    import int4_weight_kv_gb300 as m
+    return m
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "ft.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(ft_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(ft):
+    names = _declared()
+    assert len(names) >= 15
+    so = ctypes.CDLL(ft.LIB_PATH)
+    for n in names:
+        assert hasattr(so, n), n
+    assert set(names) == set(ft.exported_symbols())
+
+
+def test_status_strings(ft):
+    for s in (0, -1, -2, -3, -4, -5, 7):
+        assert isinstance(ft.ft_status_string(s), str) and ft.ft_status_string(s)
+
+
+def _cfg8b(ft, **kw):
+    c = dict(hidden=4096, n_q=32, n_kv=8, head_dim=128, inter=14336)
+    c.update(kw)
+    return ft.make_cfg(**c)
+
+
+def test_cfg_validation(ft):
+    assert ft.ft_validate_cfg(_cfg8b(ft)) == ft.FT_OK
+    assert ft.ft_validate_cfg(ft.make_cfg(512, 8, 2, 64, 1408, rope_base=1e4)) == ft.FT_OK
+    assert ft.ft_validate_cfg(_cfg8b(ft, n_q=30)) == ft.FT_ERR_INVALID_ARG          # n_q % n_kv
+    assert ft.ft_validate_cfg(_cfg8b(ft, head_dim=96)) == ft.FT_ERR_UNSUPPORTED
+    assert ft.ft_validate_cfg(_cfg8b(ft, had_block=48)) == ft.FT_ERR_INVALID_ARG    # not a power of two
+    assert ft.ft_validate_cfg(_cfg8b(ft, hidden=4000)) == ft.FT_ERR_UNSUPPORTED
+    assert ft.ft_validate_cfg(_cfg8b(ft, n_q=128, n_kv=8)) == ft.FT_ERR_UNSUPPORTED  # G > 8
+    assert ft.ft_validate_cfg(_cfg8b(ft, w_group=64)) == ft.FT_ERR_UNSUPPORTED
+    assert ft.ft_validate_cfg(_cfg8b(ft, had_block=1)) == ft.FT_OK                   # rotation off
+
+
+def test_weight_shapes_and_packed_bytes(ft):
+    c = _cfg8b(ft)
+    shapes = {ft.FT_W_QKV: (6144, 4096), ft.FT_W_O: (4096, 4096), ft.FT_W_GATEUP: (28672, 4096),
+              ft.FT_W_DOWN: (4096, 14336)}
+    total = 0
+    for role, (n, k) in shapes.items():
+        assert ft.ft_weight_shape(c, role) == (n, k)
+        nb = ft.ft_packed_weight_bytes(c, role)
+        assert nb == n * k // 2 + n * k // 64        # nibbles + BF16 group-128 scales
+        total += nb
+    assert total == 112_459_776                      # 8B layer: codes + scales
+    assert ft.ft_packed_weight_bytes(c, 9) == 0
+
+
+def test_kv_and_workspace_sizes(ft):
+    c = _cfg8b(ft)
+    nb = ft.ft_kv_cache_bytes(c, 1, 1025)
+    assert nb >= 1025 * 8 * (64 + 64 + 2 + 2)        # 1056 B per token per layer
+    assert nb < 1025 * 8 * (64 + 64 + 2 + 2) + 4 * 256
+    assert ft.ft_decode_workspace_bytes(c, 1, 1025) > 0
+    assert ft.ft_decode_workspace_bytes(c, 33, 1025) == 0
+    assert ft.ft_decode_workspace_bytes(c, 32, 4097) > ft.ft_decode_workspace_bytes(c, 1, 4097)
+    lay = ft.ft_decode_workspace_layout(c, 4, 2048)
+    assert lay.n_split >= 1 and lay.qkv < lay.o < lay.h1 < lay.a
+
+
+def test_argument_errors_return_before_launch(ft):
+    c = _cfg8b(ft)
+    lw = ft.LayerWeights(16, 16, 16, 16)
+    lib = ft.lib()
+    args = lambda **o: dict(dict(cache=4096, max_batch=4, max_ctx=64, x_in=8192, x_out=1 << 20, dt=ft.FT_BF16,
+                                 pos=256, B=1, ws=1 << 24, wsb=1 << 30), **o)
+
+    def call(**o):
+        a = args(**o)
+        return lib.ft_decode_block(ctypes.byref(c), ctypes.byref(lw), a["cache"], a["max_batch"], a["max_ctx"],
+                                   a["x_in"], a["x_out"], a["dt"], a["pos"], a["B"], a["ws"], a["wsb"], None, None)
+    assert call(B=33) == ft.FT_ERR_UNSUPPORTED
+    assert call(B=5) == ft.FT_ERR_CAPACITY
+    assert call(B=0) == ft.FT_ERR_INVALID_ARG
+    assert call(cache=None) == ft.FT_ERR_INVALID_ARG
+    assert call(x_in=8193) == ft.FT_ERR_INVALID_ARG           # misaligned
+    assert call(x_out=8192 + 64) == ft.FT_ERR_INVALID_ARG     # overlaps x_in
+    assert call(dt=7) == ft.FT_ERR_INVALID_ARG
+    assert call(wsb=16) == ft.FT_ERR_WORKSPACE
+    assert lib.ft_decode_block_stages(ctypes.byref(c), ctypes.byref(lw), 4096, 4, 64, 8192, 1 << 20, 0, 256, 1,
+                                      1 << 24, 1 << 30, None, 0, None) == ft.FT_ERR_INVALID_ARG
+    # pack / append / unpack argument checks
+    assert lib.ft_pack_weights_int4(ctypes.byref(c), 0, None, None, 4096, 1 << 30, None) == ft.FT_ERR_INVALID_ARG
+    assert lib.ft_pack_weights_int4(ctypes.byref(c), 0, 4096, None, 8192, 16, None) == ft.FT_ERR_WORKSPACE
+    assert lib.ft_pack_weights_int4(ctypes.byref(c), 5, 4096, None, 8192, 1 << 30, None) == ft.FT_ERR_INVALID_ARG
+    assert lib.ft_kv_append_int4(ctypes.byref(c), 4096, 2, 64, 16, 16, 16, 3, 1, None, None) == ft.FT_ERR_CAPACITY
+    assert lib.ft_kv_append_int4(ctypes.byref(c), 4096, 2, 64, 16, 16, 16, 1, 65, None, None) == ft.FT_ERR_CAPACITY
+    assert lib.ft_kv_append_int4(ctypes.byref(c), 4097, 2, 64, 16, 16, 16, 1, 1, None, None) == ft.FT_ERR_INVALID_ARG
+    assert lib.ft_kv_unpack_int4(ctypes.byref(c), 4096, 2, 64, 3, 8, 16, 16, 16, 16, None) == ft.FT_ERR_INVALID_ARG
+    assert ft.ft_decode_block_launches() == 6
+    prev = ft.ft_set_pdl(False)
+    assert ft.ft_set_pdl(prev) is False

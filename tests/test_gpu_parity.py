@@ -1,0 +1,188 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Codes: bit-exact up to the +-1 / scale-step rule at rounding boundaries.
+Block outputs: relative RMS <= 5e-3 and max |err| <= 2e-2 * RMS(out) on `out`,
+and the same relative RMS on the two sublayer deltas.  Block outputs are taken
+in FP32 output mode so the gate measures the kernels' arithmetic; a separate
+test checks that BF16 output mode is the BF16 rounding of the FP32 output.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+import int4_weight_kv_gb300 as ft
+from int4_weight_kv_gb300 import runtime as rt
+from tests import gpu_harness as H
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from int4_weight_kv_gb300 import build
+    build.build()
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    return H.make_layer(synth.TINY, 1)
+
+
+@pytest.fixture(scope="module")
+def l8b():
+    return H.make_layer(synth.L8B, 2)
+
+
+# ---------------------------------------------------------------- weights
+@pytest.mark.parametrize("role", ft.ROLES)
+def test_pack_codes_bit_exact_tiny(tiny, role):
+    codes, scales = H.unpack_weights(tiny, role)
+    wk, gk = rt.ROLE_KEYS[role]
+    ref_c, ref_s = oracle.quantize_weight(tiny.w32[wk], tiny.w32[gk] if gk else None)
+    np.testing.assert_array_equal(codes, ref_c)
+    np.testing.assert_array_equal(synth.bf16_bits_to_f32(scales), ref_s)
+
+
+@pytest.mark.parametrize("role", ft.ROLES)
+def test_pack_codes_bit_exact_8b(l8b, role):
+    codes, scales = H.unpack_weights(l8b, role)
+    wk, gk = rt.ROLE_KEYS[role]
+    ref_c, ref_s = oracle.quantize_weight(l8b.w32[wk], l8b.w32[gk] if gk else None)
+    np.testing.assert_array_equal(codes, ref_c)
+    np.testing.assert_array_equal(synth.bf16_bits_to_f32(scales), ref_s)
+
+
+def test_pack_handles_zero_groups_and_no_gamma(tiny):
+    w = dict(tiny.w32)
+    w["wo"] = w["wo"].copy()
+    w["wo"][:16, :128] = 0.0                     # whole groups of zeros -> code 8, scale 0
+    packed = rt.pack_layer(tiny.cfg, w)
+    lay = H.Layer(tiny.shape, tiny.cfg, w, packed)
+    codes, scales = H.unpack_weights(lay, ft.FT_W_O)
+    assert np.all(codes[:16, :128] == 8) and np.all(scales[:16, 0] == 0)
+    ref_c, _ = oracle.quantize_weight(w["wo"], None)
+    np.testing.assert_array_equal(codes, ref_c)
+
+
+# ---------------------------------------------------------------- KV append
+@pytest.mark.parametrize("shape,cid,B,T", [(synth.TINY, 1, 2, 37), (synth.L8B, 2, 3, 70)])
+def test_kv_append_codes(shape, cid, B, T):
+    cfg = ft.cfg_from_shape(shape)
+    max_ctx = T + 5
+    kb, kf = synth.kv_history(shape, cid, B, T, which="k")
+    vb, vf = synth.kv_history(shape, cid, B, T, which="v")
+    cache = rt.alloc_cache(cfg, B, max_ctx)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    # two appends: positions 0..T-1 in two pieces (ragged start)
+    rt.fill_history(cfg, cache, B, max_ctx, kb, vb, st, chunk=23)
+    kc, vc, ks, vs = H.unpack_cache(H.Layer(shape, cfg, {}, {}), cache, B, max_ctx, B, T)
+    assert st.item() == 0
+    for codes, scales, vals in ((kc, ks, kf), (vc, vs, vf)):
+        rot = oracle.blockdiag_apply(vals.astype(np.float64), shape.hb).astype(np.float32)   # [B, T, h, d]
+        rot = rot.transpose(0, 2, 1, 3)                                                       # [B, h, T, d]
+        n_diff, n_sc = H.compare_codes(codes, scales, rot, shape.kvg)
+        assert n_diff <= max(4, codes.size // 20000)
+
+
+def test_kv_append_capacity_flag(tiny):
+    cfg = tiny.cfg
+    cache = rt.alloc_cache(cfg, 2, 16)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    k = torch.zeros((2, 4, cfg.n_kv, cfg.head_dim), dtype=torch.int16, device="cuda")
+    pos = torch.tensor([0, 14], dtype=torch.int32, device="cuda")      # request 1 overflows
+    ft.check(ft.ft_kv_append_int4(cfg, cache, 2, 16, k, k, pos, 2, 4, st))
+    torch.cuda.synchronize()
+    assert st.item() & ft.FT_DEV_CAPACITY
+
+
+# ---------------------------------------------------------------- the block
+def test_block_tiny(tiny):
+    pb = H.make_problem(tiny, 1, B=1, ctx=128)
+    g = H.run_gpu(pb)
+    o = H.run_oracle(pb)
+    rep = H.assert_block_close(g, o, range(1))
+    assert rep["qkv_rel_rms"] < 1e-3
+
+
+def test_block_tiny_ragged_batch(tiny):
+    pos = np.array([0, 1, 15, 16, 17, 100, 128, 129], np.int32)
+    pb = H.make_problem(tiny, 1, B=8, ctx=129, pos=pos, max_ctx=140)
+    g = H.run_gpu(pb)
+    o = H.run_oracle(pb)
+    H.assert_block_close(g, o, range(8))
+
+
+def test_block_tiny_bf16_io_is_rounding_of_f32(tiny):
+    pb = H.make_problem(tiny, 1, B=3, ctx=40)
+    g32 = H.run_gpu(pb, ft.FT_F32)
+    g16 = H.run_gpu(pb, ft.FT_BF16)
+    want = oracle.bf16_rne(g32.out)
+    # identical arithmetic up to the last rounding of the residual stream
+    np.testing.assert_allclose(g16.out, want, rtol=2 ** -7, atol=0)
+    assert H.rel_rms(g16.out, g32.out) < 3e-3
+
+
+def test_block_tiny_new_token_codes_teacher_forced(tiny):
+    """The new token's cache codes equal the oracle's quantisation of the GPU's own k/v."""
+    pb = H.make_problem(tiny, 1, B=2, ctx=50, pos=np.array([50, 7]), max_ctx=60)
+    g = H.run_gpu(pb)
+    s = tiny.shape
+    kc, vc, ks, vs = H.unpack_cache(tiny, g.cache, 2, 60, 2, 51)
+    d, nq, nkv = s.head_dim, s.n_q, s.n_kv
+    for b, L in enumerate(pb.pos):
+        k = g.qkv[b, nq * d:(nq + nkv) * d].reshape(nkv, d).astype(np.float64)
+        v = g.qkv[b, (nq + nkv) * d:].reshape(nkv, d).astype(np.float64)
+        kr = oracle.rope_apply(k, int(L), s.rope_base)
+        for codes, scales, vals in ((kc, ks, kr), (vc, vs, v)):
+            rot = oracle.blockdiag_apply(vals, s.hb).astype(np.float32)
+            H.compare_codes(codes[b, :, L], scales[b, :, L], rot, s.kvg)
+
+
+def test_block_split_invariance(tiny):
+    """The same problem with different split-KV chunkings agrees to FP32 rounding."""
+    pos = np.array([127, 60], np.int32)
+    a = H.make_problem(tiny, 1, B=2, ctx=127, pos=pos, max_ctx=128)
+    b = H.make_problem(tiny, 1, B=2, ctx=127, pos=pos, max_ctx=3000)
+    ga, gb = H.run_gpu(a), H.run_gpu(b)
+    na = ft.ft_decode_workspace_layout(tiny.cfg, 2, 128).n_split
+    nb = ft.ft_decode_workspace_layout(tiny.cfg, 2, 3000).n_split
+    assert na != nb
+    assert H.rel_rms(ga.o, gb.o) < 2e-3
+    assert H.rel_rms(ga.out, gb.out) < 1e-5
+
+
+def test_block_capacity_flag(tiny):
+    pb = H.make_problem(tiny, 1, B=1, ctx=10, max_ctx=11)
+    pb.pos = np.array([11], np.int32)           # position == max_ctx: no room
+    cache = pb.cache.clone()
+    pos = torch.from_numpy(pb.pos).cuda()
+    x = torch.from_numpy(pb.x_f32).cuda()
+    y = torch.empty_like(x)
+    ws = rt.alloc_workspace(tiny.cfg, 1, 11)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ft.check(ft.ft_decode_block(tiny.cfg, tiny.packed, cache, 1, 11, x, y, ft.FT_F32, pos, 1, ws, st))
+    torch.cuda.synchronize()
+    assert st.item() & ft.FT_DEV_CAPACITY
+
+
+def test_block_8b_b1_ctx1024(l8b):
+    """Llama-3-8B layer shape, batch 1, context 1024 (the timed workload)."""
+    pb = H.make_problem(l8b, 2, B=1, ctx=1024)
+    g = H.run_gpu(pb)
+    o = H.run_oracle(pb)
+    H.assert_block_close(g, o, range(1))
+
+
+@pytest.mark.parametrize("B", [2, 9, 17, 32])
+def test_block_8b_batch_sweep(l8b, B):
+    """8B shape at several batch sizes (all MMA column-tile counts), ragged lengths."""
+    pos = synth.positions(B, 300, ragged=True, seed=B)
+    pb = H.make_problem(l8b, 2, B=B, ctx=300, pos=pos)
+    g = H.run_gpu(pb)
+    rows = sorted({0, B // 2, B - 1})
+    o = H.run_oracle(pb, rows=rows)
+    H.assert_block_close(g, o, rows)
