@@ -167,9 +167,10 @@ enum {
   FT_STAGE_QKV = 2,   /* QKV projection (x rho1)                             */
   FT_STAGE_ATTN = 4,  /* RoPE, rotation, cache write, split-KV attention     */
   FT_STAGE_O = 8,     /* O projection + residual                              */
-  FT_STAGE_GU = 16,   /* gate/up projection + SwiGLU                          */
-  FT_STAGE_DOWN = 32, /* down projection + residual -> x_out                  */
-  FT_STAGE_ALL = 63
+  FT_STAGE_MID = 16,  /* h1 -> gate/up operand, rho2, down accumulator        */
+  FT_STAGE_GU = 32,   /* gate/up projection + SwiGLU                          */
+  FT_STAGE_DOWN = 64, /* down projection + residual -> x_out                  */
+  FT_STAGE_ALL = 127
 };
 
 /* Runs a subset of the block's stages on a workspace left by a previous full
@@ -182,11 +183,14 @@ int ft_decode_block_stages(const ft_block_cfg *cfg, const ft_layer_weights *w, v
                            int32_t *dev_status, unsigned stage_mask, ft_stream stream);
 
 /* Byte offsets of intermediate tensors inside the workspace (host struct out),
- * for tests:  qkv FP32 [B, (n_q+2n_kv) d] (rho1 applied, before RoPE);
- * o FP16 [B, n_q d] (attention output after the inverse rotation);
- * h1 FP32 [B, H];  a FP16 [B, I]. */
+ * for tests:  qkv FP32 [B, (n_q+2n_kv) d] (the projection before rho1 and
+ * RoPE);  rho1 FP32 [B];  o FP16 [B, n_q d] (attention output after the
+ * inverse rotation);  h1 FP32 [B, H];  a FP16 [B, I] (SwiGLU output).
+ * o and a are stored in the projections' operand layout: within every 16
+ * consecutive inputs the order is 0,1,8,9,2,3,10,11,4,5,12,13,6,7,14,15 and
+ * inputs 8..15 hold value / 16. */
 typedef struct {
-  size_t qkv, o, h1, a;
+  size_t qkv, rho1, o, h1, a;
   int32_t n_split; /* split-KV chunks per (request, KV head) */
 } ft_ws_layout;
 

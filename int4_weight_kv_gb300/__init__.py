@@ -19,7 +19,8 @@ FT_OK, FT_ERR_INVALID_ARG, FT_ERR_UNSUPPORTED, FT_ERR_WORKSPACE, FT_ERR_CAPACITY
 FT_DEV_CAPACITY, FT_DEV_TIMEOUT, FT_DEV_RANGE = 1, 2, 4
 FT_BF16, FT_F32 = 0, 1
 FT_W_QKV, FT_W_O, FT_W_GATEUP, FT_W_DOWN = 0, 1, 2, 3
-FT_STAGE_PREP, FT_STAGE_QKV, FT_STAGE_ATTN, FT_STAGE_O, FT_STAGE_GU, FT_STAGE_DOWN, FT_STAGE_ALL = 1, 2, 4, 8, 16, 32, 63
+FT_STAGE_PREP, FT_STAGE_QKV, FT_STAGE_ATTN, FT_STAGE_O = 1, 2, 4, 8
+FT_STAGE_MID, FT_STAGE_GU, FT_STAGE_DOWN, FT_STAGE_ALL = 16, 32, 64, 127
 ROLES = (FT_W_QKV, FT_W_O, FT_W_GATEUP, FT_W_DOWN)
 
 
@@ -34,7 +35,8 @@ class LayerWeights(ctypes.Structure):
 
 
 class WsLayout(ctypes.Structure):
-    _fields_ = [("qkv", c_size_t), ("o", c_size_t), ("h1", c_size_t), ("a", c_size_t), ("n_split", c_int32)]
+    _fields_ = [("qkv", c_size_t), ("rho1", c_size_t), ("o", c_size_t), ("h1", c_size_t), ("a", c_size_t),
+                ("n_split", c_int32)]
 
 
 class FTError(RuntimeError):

@@ -14,10 +14,12 @@
 // The K entry's nibbles are stored so that a 16-byte load per thread is the
 // A fragment of two k-steps; the V entry's nibbles so that two positions' bytes
 // combine (prmt) into A fragments of V^T.  Per-position scales multiply the
-// scores (K) and the probabilities (V).  Each CTA writes (max, sum, acc)
-// partials; the last CTA of (b, h) to finish (atomic ticket, never waits)
-// quantises and writes the new token's K/V at position L_b, adds the new token
-// as one more partial, merges in split order, undoes the rotation and writes o.
+// scores (K) and the probabilities (V).  The n_split CTAs of one (b, h) form a
+// thread-block cluster: each keeps its (max, sum, acc) partial in shared
+// memory, a cluster barrier publishes them, and CTA r merges heads r, r+n_split,
+// ... by reading its peers' partials through distributed shared memory, adds
+// the new token (quantised and written to the cache at L_b by CTA 0, decoded
+// identically by every CTA), undoes the rotation and writes o.
 #include "ft_block.cuh"
 
 namespace ft {
@@ -96,11 +98,14 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnParams p) {
   constexpr int NPL = D / 32;
   constexpr int KT = D / 16;  // k-tiles of q.K == m-tiles of P.V
   constexpr int PARTF = 16 + 8 * D;
-  __shared__ float qt[8][D];            // rotated, scaled query (FP32)
+  __shared__ float qt[8][D];            // rotated, scaled query (FP16 values)
+  __shared__ float qoff[8];             // its operand offsets (magic-number decode)
   __shared__ float mrg[4][PARTF];       // per-warp partials for the CTA merge
   __shared__ float knew[D], vnew[D];
+  __shared__ float cpart[16 + 8 * D];    // this CTA's merged partial, read by the cluster
   __shared__ uint8_t stage[2][D];
-  __shared__ uint32_t s_last;
+  __shared__ __align__(16) uint8_t stage_out[2][D / 2];
+  __shared__ uint16_t stage_sc[2];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, tig = lane & 3;
   const int split = blockIdx.x % p.nsplit;
@@ -109,6 +114,7 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnParams p) {
   const int G = p.G;
   const int Lb = p.pos[b];
   if (Lb < 0 || Lb >= p.L.max_ctx) {
+    // every CTA of this cluster serves the same request, so all leave here together
     if (tid == 0 && split == 0 && h == 0) set_status(p.status, FT_DEV_CAPACITY);
     griddep_launch();
     return;
@@ -125,16 +131,28 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnParams p) {
 
   griddep_wait();
 
-  // ---- rotated query of the G heads: RoPE, Hadamard, softmax scale
+  // ---- rotated query of the G heads: rho1, RoPE, Hadamard, softmax scale
+  const float rho1 = p.rho1[b];
   for (int hh = warp; hh < G; hh += 4) {
     float v[NPL];
     const float* src = p.qkv + (size_t)b * p.Nqkv + (size_t)(h * G + hh) * D;
 #pragma unroll
-    for (int m = 0; m < NPL; ++m) v[m] = __ldcg(src + lane + 32 * m);
+    for (int m = 0; m < NPL; ++m) v[m] = __ldcg(src + lane + 32 * m) * rho1;
     warp_rope<NPL>(v, Lb, p.inv_freq);
     warp_fwht<NPL>(v, p.hb);
+    // q~ as the FP16 B operand (channels c % 16 >= 8 hold q / 16) and its offset
+    float sq = 0.0f;
 #pragma unroll
-    for (int m = 0; m < NPL; ++m) qt[hh][lane + 32 * m] = __half2float(__float2half_rn(v[m] * p.qscale));
+    for (int m = 0; m < NPL; ++m) {
+      const int c = lane + 32 * m;
+      const float q = __half2float(__float2half_rn(v[m] * p.qscale));
+      qt[hh][c] = q;
+      float st;
+      (void)op_encode(q, c, st);
+      sq += st;
+    }
+    sq = warp_sum(sq);
+    if (lane == 0) qoff[hh] = sq;
   }
   __syncthreads();
   uint32_t bq[KT][2];
@@ -143,15 +161,21 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnParams p) {
     if (g < G) {
       const int c = 16 * kt + 2 * tig;
       bq[kt][0] = pack_half2(qt[g][c], qt[g][c + 1]);
-      bq[kt][1] = pack_half2(qt[g][c + 8], qt[g][c + 9]);
+      bq[kt][1] = pack_half2(qt[g][c + 8] * 0.0625f, qt[g][c + 9] * 0.0625f);
     } else {
       bq[kt][0] = bq[kt][1] = 0u;
     }
   }
+  const float qo0 = (2 * tig < G) ? qoff[2 * tig] : 0.0f;
+  const float qo1 = (2 * tig + 1 < G) ? qoff[2 * tig + 1] : 0.0f;
 
   float acc[KT][4];
 #pragma unroll
   for (int mt = 0; mt < KT; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.0f;
+  // offset accumulator: the same P.V product with every V code replaced by its
+  // decode offset (rows of constant 1032 / 1152), rescaled like acc
+  float kacc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  const uint32_t kappa[4] = {kHOffLo, kHOffLo, kHOffHi, kHOffHi};
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
 
   for (; ti < t1; ti += 4) {
@@ -164,8 +188,8 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnParams p) {
 #pragma unroll
     for (int j = 0; j < D / 32; ++j) {
       uint32_t dg[4], dg8[4];
-      dequant_word(cur.k[0][j], dg);
-      dequant_word(cur.k[1][j], dg8);
+      magic_word(cur.k[0][j], dg);
+      magic_word(cur.k[1][j], dg8);
       const uint32_t a0[4] = {dg[0], dg8[0], dg[1], dg8[1]};
       const uint32_t a1[4] = {dg[2], dg8[2], dg[3], dg8[3]};
       mma_f16(sacc, a0, bq[2 * j][0], bq[2 * j][1]);
@@ -173,10 +197,10 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnParams p) {
     }
     const bool va = (p0 + g) < p1, vb = (p0 + g + 8) < p1;
     const float ks0 = bf16_bits_to_f32(cur.ks[0]), ks1 = bf16_bits_to_f32(cur.ks[1]);
-    const float s0 = va ? sacc[0] * ks0 : -INFINITY;
-    const float s1 = va ? sacc[1] * ks0 : -INFINITY;
-    const float s2 = vb ? sacc[2] * ks1 : -INFINITY;
-    const float s3 = vb ? sacc[3] * ks1 : -INFINITY;
+    const float s0 = va ? (sacc[0] - qo0) * ks0 : -INFINITY;
+    const float s1 = va ? (sacc[1] - qo1) * ks0 : -INFINITY;
+    const float s2 = vb ? (sacc[2] - qo0) * ks1 : -INFINITY;
+    const float s3 = vb ? (sacc[3] - qo1) * ks1 : -INFINITY;
     float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
 #pragma unroll
     for (int o = 4; o < 32; o <<= 1) {
@@ -197,20 +221,24 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnParams p) {
       acc[mt][2] *= al0;
       acc[mt][3] *= al1;
     }
+    kacc[0] *= al0;
+    kacc[1] *= al1;
+    kacc[2] *= al0;
+    kacc[3] *= al1;
     const float vs0 = va ? bf16_bits_to_f32(cur.vs[0]) : 0.0f;
-    const float vs1 = vb ? bf16_bits_to_f32(cur.vs[1]) : 0.0f;
+    const float vs1 = vb ? bf16_bits_to_f32(cur.vs[1]) * 0.0625f : 0.0f;  // positions 8..15: operand / 16
     const uint32_t P0 = pack_half2(e0 * vs0, e1 * vs0);  // position g,   heads 2tig, 2tig+1
     const uint32_t P1 = pack_half2(e2 * vs1, e3 * vs1);  // position g+8
     const uint32_t pb0 = movmatrix_trans(P0);            // positions 2tig, 2tig+1 of head g
     const uint32_t pb1 = movmatrix_trans(P1);            // positions 2tig+8, 2tig+9
-    // O += V^T . P
+    // O += V^T . P  (positions 2tig, 2tig+1 decode at 1024 + c, positions +8 at 1024 + 16 c)
 #pragma unroll
     for (int j = 0; j < D / 64; ++j) {
       uint32_t lo01[4], hi01[4], lo23[4], hi23[4];
-      dequant_word(prmt(cur.v[0][j], cur.v[1][j], 0x5410u), lo01);
-      dequant_word(prmt(cur.v[0][j], cur.v[1][j], 0x7632u), hi01);
-      dequant_word(prmt(cur.v[2][j], cur.v[3][j], 0x5410u), lo23);
-      dequant_word(prmt(cur.v[2][j], cur.v[3][j], 0x7632u), hi23);
+      magic_low4(prmt(cur.v[0][j], cur.v[1][j], 0x5410u), lo01);
+      magic_low4(prmt(cur.v[0][j], cur.v[1][j], 0x7632u), hi01);
+      magic_high4(prmt(cur.v[2][j], cur.v[3][j], 0x5410u), lo23);
+      magic_high4(prmt(cur.v[2][j], cur.v[3][j], 0x7632u), hi23);
       const uint32_t A0[4] = {lo01[0], lo01[1], lo23[0], lo23[1]};
       const uint32_t A1[4] = {lo01[2], lo01[3], lo23[2], lo23[3]};
       const uint32_t A2[4] = {hi01[0], hi01[1], hi23[0], hi23[1]};
@@ -220,11 +248,21 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnParams p) {
       mma_f16(acc[4 * j + 2], A2, pb0, pb1);
       mma_f16(acc[4 * j + 3], A3, pb0, pb1);
     }
+    mma_f16(kacc, kappa, pb0, pb1);
     if (more) cur = nxt;
   }
   griddep_launch();
 
-  // ---- merge the 4 warps of the CTA
+  // remove the decode offsets (every row of kacc carries the same value)
+#pragma unroll
+  for (int mt = 0; mt < KT; ++mt) {
+    acc[mt][0] -= kacc[0];
+    acc[mt][1] -= kacc[1];
+    acc[mt][2] -= kacc[0];
+    acc[mt][3] -= kacc[1];
+  }
+
+  // ---- merge the 4 warps of the CTA into this CTA's partial (kept in smem)
 #pragma unroll
   for (int o = 4; o < 32; o <<= 1) {
     l0 += __shfl_xor_sync(0xffffffffu, l0, o);
@@ -246,12 +284,8 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnParams p) {
     mw[16 + (2 * tig + 1) * D + c1] = acc[mt][3];
   }
   __syncthreads();
-  float* part = p.part + ((size_t)(b * p.nkv + h) * p.nsplit + split) * PARTF;
   for (int i = tid; i < 8 * D + 16; i += 128) {
-    // i < 8: max; 8..15: sum; then acc[head][ch]
-    int hh;
-    if (i < 16) hh = i & 7;
-    else hh = (i - 16) / D;
+    const int hh = (i < 16) ? (i & 7) : (i - 16) / D;
     float M = -INFINITY;
     for (int w = 0; w < 4; ++w) M = fmaxf(M, mrg[w][hh]);
     float v;
@@ -265,76 +299,92 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnParams p) {
           if (mw2 != -INFINITY) v += mrg[w][i] * exp2f(mw2 - M);
         }
     }
-    __stcg(part + i, v);
+    cpart[i] = v;
   }
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) s_last = (atomicAdd(p.tick + b * p.nkv + h, 1u) == (uint32_t)(p.nsplit - 1)) ? 1u : 0u;
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  if (tid == 0) p.tick[b * p.nkv + h] = 0u;
 
-  // ---- finisher: the new token's K/V (RoPE on k, rotation, INT4, cache write)
-  const size_t row = p.L.row(b, h, Lb);
+  // ---- the new token: RoPE on k, rotation, INT4 (cache write by split 0), decode
   if (warp < 2) {
     float v[NPL];
     const int off = (warp == 0) ? (p.nq + h) * D : (p.nq + p.nkv + h) * D;
     const float* src = p.qkv + (size_t)b * p.Nqkv + off;
 #pragma unroll
-    for (int m = 0; m < NPL; ++m) v[m] = __ldcg(src + lane + 32 * m);
+    for (int m = 0; m < NPL; ++m) v[m] = __ldcg(src + lane + 32 * m) * rho1;
     if (warp == 0) warp_rope<NPL>(v, Lb, p.inv_freq);
     warp_fwht<NPL>(v, p.hb);
-    uint8_t* entry = p.cache + (warp == 0 ? p.L.kc : p.L.vc) + row * p.L.entry;
-    uint16_t* sc = reinterpret_cast<uint16_t*>(p.cache + (warp == 0 ? p.L.ks : p.L.vs)) + row;
+    const size_t row = p.L.row(b, h, Lb);
+    uint8_t* entry = (split == 0) ? p.cache + (warp == 0 ? p.L.kc : p.L.vc) + row * p.L.entry : stage_out[warp];
+    uint16_t* sc = (split == 0) ? reinterpret_cast<uint16_t*>(p.cache + (warp == 0 ? p.L.ks : p.L.vs)) + row
+                                : &stage_sc[warp];
     warp_quant_store<NPL>(v, warp == 0, stage[warp], entry, sc);
     float* dst = (warp == 0) ? knew : vnew;
 #pragma unroll
     for (int m = 0; m < NPL; ++m) dst[lane + 32 * m] = v[m];
   }
   __syncthreads();
-  // ---- merge all splits and the new token per head, inverse rotation, write o
-  for (int hh = warp; hh < G; hh += 4) {
+  cluster_sync();  // every CTA's partial is now visible to the cluster
+
+  // ---- CTA r merges heads r, r + n_split, ...: peers' partials via DSMEM
+  const uint32_t cp_local = smem_u32(cpart);
+  for (int hh = split + p.nsplit * warp; hh < G; hh += p.nsplit * 4) {
     float sn = 0.0f;
 #pragma unroll
     for (int m = 0; m < NPL; ++m) sn += qt[hh][lane + 32 * m] * knew[lane + 32 * m];
     sn = warp_sum(sn);
-    const float* pb = p.part + ((size_t)(b * p.nkv + h) * p.nsplit) * PARTF;
     float M = sn;
-    for (int s = 0; s < p.nsplit; ++s) M = fmaxf(M, __ldcg(pb + (size_t)s * PARTF + hh));
+    for (int r = 0; r < p.nsplit; ++r) M = fmaxf(M, ld_dsmem_f32(cp_local + 4 * hh, r));
     const float wn = exp2f(sn - M);
     float lsum = wn;
     float o[NPL];
 #pragma unroll
     for (int m = 0; m < NPL; ++m) o[m] = wn * vnew[lane + 32 * m];
-    for (int s = 0; s < p.nsplit; ++s) {
-      const float* ps = pb + (size_t)s * PARTF;
-      const float ms = __ldcg(ps + hh);
+    for (int r = 0; r < p.nsplit; ++r) {
+      const float ms = ld_dsmem_f32(cp_local + 4 * hh, r);
       if (ms == -INFINITY) continue;
       const float w = exp2f(ms - M);
-      lsum += w * __ldcg(ps + 8 + hh);
+      lsum += w * ld_dsmem_f32(cp_local + 4 * (8 + hh), r);
 #pragma unroll
-      for (int m = 0; m < NPL; ++m) o[m] += w * __ldcg(ps + 16 + hh * D + lane + 32 * m);
+      for (int m = 0; m < NPL; ++m) o[m] += w * ld_dsmem_f32(cp_local + 4 * (16 + hh * D + lane + 32 * m), r);
     }
     const float inv = 1.0f / lsum;
 #pragma unroll
     for (int m = 0; m < NPL; ++m) o[m] *= inv;
     warp_fwht<NPL>(o, p.hb);
-    __half* dst = p.o_h + (size_t)b * p.nq * D + (size_t)(h * G + hh) * D;
+    const int kbase = (h * G + hh) * D;  // input index of channel 0 of this head in the O projection
+    __half* dst = p.o_h + (size_t)b * p.nq * D;
     bool bad = false;
+    float so = 0.0f;
 #pragma unroll
     for (int m = 0; m < NPL; ++m) {
+      const int k = kbase + lane + 32 * m;
       bad |= !(fabsf(o[m]) <= 65504.0f);
-      dst[lane + 32 * m] = __float2half_rn(o[m]);
+      float st;
+      dst[op_slot(k)] = op_encode(o[m], k, st);
+      so += st;
     }
+    so = warp_sum(so);  // a head (d <= 128 channels) lies inside one 128-input group
+    if (lane == 0) atomicAdd(p.s_o + (kbase / kWGroup) * 32 + b, so);
     if (bad) set_status(p.status, FT_DEV_RANGE);
   }
+  cluster_sync();  // keep this CTA's shared memory alive until every peer has read it
 }
 
 cudaError_t launch_attn(const AttnParams& p, int head_dim, cudaStream_t st, bool pdl) {
-  const dim3 grid((unsigned)(p.B * p.nkv * p.nsplit));
-  if (head_dim == 128) return launch_ex(attn_kernel<128>, grid, dim3(128), 0, st, pdl, p);
-  return launch_ex(attn_kernel<64>, grid, dim3(128), 0, st, pdl, p);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(p.B * p.nkv * p.nsplit));
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)p.nsplit;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 2 : 1;
+  if (head_dim == 128) return cudaLaunchKernelEx(&cfg, attn_kernel<128>, p);
+  return cudaLaunchKernelEx(&cfg, attn_kernel<64>, p);
 }
 
 }  // namespace ft

@@ -1,30 +1,98 @@
-// The decode block: input preparation and the host-side orchestration of the
-// six kernels (prep, QKV, attention, O, gate/up, down) on the caller's stream,
-// chained with programmatic dependent launch so each kernel's weight stream
-// starts while its predecessor finishes.
+// The decode block: input preparation, the h1 finalisation between O and
+// gate/up, and the host-side orchestration of the seven kernels (prep, QKV,
+// attention, O, mid, gate/up, down) on the caller's stream, chained with
+// programmatic dependent launch so each projection's weight stream starts while
+// its predecessor finishes.
 #include <cmath>
 
 #include "ft_block.cuh"
 
 namespace ft {
 
-// Block input -> FP16 MMA operand, RMSNorm row factor rho1 (applied later in
-// the QKV epilogue, summary page "어떻게 동작하나"), and the per-call counters
-// cleared.  One CTA per request.
+// Encodes 8 consecutive inputs 8 ch .. 8 ch + 7 of one row into the operand
+// layout (op_slot) and returns their contribution to the group offset S.
+__device__ __forceinline__ float encode_chunk8(const float (&v)[8], int ch, __half* row) {
+  const bool high = (ch & 1) != 0;
+  const int base = (ch >> 1) * 16 + (high ? 2 : 0);
+  float s = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float s0, s1;
+    const __half h0 = op_encode(v[2 * i], 8 * ch + 2 * i, s0);
+    const __half h1 = op_encode(v[2 * i + 1], 8 * ch + 2 * i + 1, s1);
+    *reinterpret_cast<__half2*>(row + base + 4 * i) = __halves2half2(h0, h1);
+    s += s0 + s1;
+  }
+  return s;
+}
+
+// Sums a per-thread value over the 16 consecutive threads that hold one group
+// (16 chunks of 8 = 128 inputs) and returns it in every lane of the 16.
+__device__ __forceinline__ float group16_sum(float v) {
+#pragma unroll
+  for (int o = 1; o < 16; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Block input -> QKV operand + offsets, rho1 (applied after the QKV
+// accumulation, summary page "어떻게 동작하나"), h1 accumulator <- x, and this
+// call's accumulators cleared.  One CTA (256 threads) per request.
 __global__ void __launch_bounds__(256) prep_kernel(const PrepParams p) {
-  griddep_wait();  // the previous block's kernels may still read the workspace
+  griddep_wait();  // the previous kernel may have produced x_in or still read the workspace
   griddep_launch();
   __shared__ float red[8];
   const int b = blockIdx.x, tid = threadIdx.x;
-  for (int i = b * 256 + tid; i < p.nzero; i += gridDim.x * 256) p.zero[i] = 0u;
+  for (int i = tid; i < p.nqkv; i += 256) p.qkv[(size_t)b * p.nqkv + i] = 0.0f;
+  for (int i = tid; i < p.nkg_o; i += 256) p.s_o[i * 32 + b] = 0.0f;
+  for (int i = tid; i < p.nkg_a; i += 256) p.s_a[i * 32 + b] = 0.0f;
+  if (b == 0)
+    for (int i = tid; i < p.ntick; i += 256) p.tick[i] = 0u;
+  constexpr int MAXC = 4;
+  const int nchunk = p.H / 8;  // a multiple of 16
   float ss = 0.0f;
   bool bad = false;
-  for (int i = tid; i < p.H; i += 256) {
-    const float x = (p.act_dtype == FT_F32) ? static_cast<const float*>(p.x_in)[(size_t)b * p.H + i]
-                                            : bf16_bits_to_f32(static_cast<const uint16_t*>(p.x_in)[(size_t)b * p.H + i]);
-    ss = fmaf(x, x, ss);
-    bad |= !(fabsf(x) <= 65504.0f);
-    p.x_h[(size_t)b * p.H + i] = __float2half_rn(x);
+  for (int base = 0; base < nchunk; base += 256 * MAXC) {
+    float v[MAXC][8];
+#pragma unroll
+    for (int c = 0; c < MAXC; ++c) {
+      const int ch = base + tid + 256 * c;
+      if (ch < nchunk) {
+        if (p.act_dtype == FT_F32) {
+          const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(p.x_in) + (size_t)b * p.H) + 2 * ch;
+          const float4 a = __ldcg(src), d = __ldcg(src + 1);
+          v[c][0] = a.x; v[c][1] = a.y; v[c][2] = a.z; v[c][3] = a.w;
+          v[c][4] = d.x; v[c][5] = d.y; v[c][6] = d.z; v[c][7] = d.w;
+        } else {
+          const uint4 a =
+              __ldcg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.x_in) + (size_t)b * p.H) + ch);
+          const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            v[c][2 * k] = __uint_as_float(w[k] << 16);
+            v[c][2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int c = 0; c < MAXC; ++c) {
+      const int ch = base + tid + 256 * c;
+      float sterm = 0.0f;
+      if (ch < nchunk) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          ss = fmaf(v[c][k], v[c][k], ss);
+          bad |= !(fabsf(v[c][k]) <= 65504.0f);
+        }
+        float4* h1 = reinterpret_cast<float4*>(p.h1 + (size_t)b * p.H) + 2 * ch;
+        h1[0] = make_float4(v[c][0], v[c][1], v[c][2], v[c][3]);
+        h1[1] = make_float4(v[c][4], v[c][5], v[c][6], v[c][7]);
+        sterm = encode_chunk8(v[c], ch, p.x_h + (size_t)b * p.H);
+      }
+      // whole warps stay converged here: nchunk and 256 * MAXC are multiples of 16
+      const float gs = group16_sum(sterm);
+      if (ch < nchunk && (ch & 15) == 0) p.s_x[(ch >> 4) * 32 + b] = gs;
+    }
   }
   ss = warp_sum(ss);
   if ((tid & 31) == 0) red[tid >> 5] = ss;
@@ -37,10 +105,63 @@ __global__ void __launch_bounds__(256) prep_kernel(const PrepParams p) {
   if (bad) set_status(p.status, FT_DEV_RANGE);
 }
 
+// h1 (complete after the O projection) -> gate/up operand + offsets, rho2
+// (applied after the gate/up accumulation), and the down accumulator <- h1.
+__global__ void __launch_bounds__(256) mid_kernel(const MidParams p) {
+  griddep_wait();
+  griddep_launch();
+  __shared__ float red[8];
+  const int b = blockIdx.x, tid = threadIdx.x;
+  constexpr int MAXC = 4;
+  const int nchunk = p.H / 8;
+  float ss = 0.0f;
+  bool bad = false;
+  for (int base = 0; base < nchunk; base += 256 * MAXC) {
+    float v[MAXC][8];
+#pragma unroll
+    for (int c = 0; c < MAXC; ++c) {
+      const int ch = base + tid + 256 * c;
+      if (ch < nchunk) {
+        const float4* src = reinterpret_cast<const float4*>(p.h1 + (size_t)b * p.H) + 2 * ch;
+        const float4 a = __ldcg(src), d = __ldcg(src + 1);
+        v[c][0] = a.x; v[c][1] = a.y; v[c][2] = a.z; v[c][3] = a.w;
+        v[c][4] = d.x; v[c][5] = d.y; v[c][6] = d.z; v[c][7] = d.w;
+      }
+    }
+#pragma unroll
+    for (int c = 0; c < MAXC; ++c) {
+      const int ch = base + tid + 256 * c;
+      float sterm = 0.0f;
+      if (ch < nchunk) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          ss = fmaf(v[c][k], v[c][k], ss);
+          bad |= !(fabsf(v[c][k]) <= 65504.0f);
+        }
+        float4* dst = reinterpret_cast<float4*>(p.out_acc + (size_t)b * p.H) + 2 * ch;
+        dst[0] = make_float4(v[c][0], v[c][1], v[c][2], v[c][3]);
+        dst[1] = make_float4(v[c][4], v[c][5], v[c][6], v[c][7]);
+        sterm = encode_chunk8(v[c], ch, p.h1_h + (size_t)b * p.H);
+      }
+      const float gs = group16_sum(sterm);
+      if (ch < nchunk && (ch & 15) == 0) p.s_h1[(ch >> 4) * 32 + b] = gs;
+    }
+  }
+  ss = warp_sum(ss);
+  if ((tid & 31) == 0) red[tid >> 5] = ss;
+  __syncthreads();
+  if (tid == 0) {
+    float t = 0.0f;
+    for (int w = 0; w < 8; ++w) t += red[w];
+    p.rho2[b] = rsqrtf(t / (float)p.H + p.eps);
+  }
+  if (bad) set_status(p.status, FT_DEV_RANGE);
+}
+
 struct WsPlan {
   GemvPlan g[4];
   int nsplit;
-  size_t x_h, rho1, zero, nzero_words, sumsq2, attn_tick, gtick[4], qkv, o_h, h1, h1_h, a_h, attn_part, slots, total;
+  size_t x_h, s_x, rho1, h1, qkv, o_h, s_o, h1_h, s_h1, rho2, a_h, s_a, out_acc, tick, total;
 };
 
 static int attn_splits(int B, int nkv, int max_ctx, int sms) {
@@ -49,7 +170,7 @@ static int attn_splits(int B, int nkv, int max_ctx, int sms) {
   int ns = (target + pairs - 1) / pairs;
   const int cap = (max_ctx + 63) / 64;
   if (ns > cap) ns = cap;
-  if (ns > 48) ns = 48;
+  if (ns > 8) ns = 8;  // the splits of one (request, KV head) form one portable cluster
   if (ns < 1) ns = 1;
   return ns;
 }
@@ -59,10 +180,11 @@ static WsPlan make_plan(const ft_block_cfg& c, int B, int max_ctx) {
   int sms = ft_host::num_sms();
   if (sms <= 0) sms = 148;
   const int nqkv = (c.n_q + 2 * c.n_kv) * c.head_dim;
-  w.g[kRoleQKV] = make_gemv_plan(nqkv, c.hidden, B, sms);
-  w.g[kRoleO] = make_gemv_plan(c.hidden, c.n_q * c.head_dim, B, sms);
-  w.g[kRoleGU] = make_gemv_plan(2 * c.inter, c.hidden, B, sms);
-  w.g[kRoleDown] = make_gemv_plan(c.hidden, c.inter, B, sms);
+  const int bud = 200 * 1024;  // shared-memory budget of one GEMV CTA (ring + reduction area)
+  w.g[kRoleQKV] = make_gemv_plan(nqkv, c.hidden, B, sms, false, bud);
+  w.g[kRoleO] = make_gemv_plan(c.hidden, c.n_q * c.head_dim, B, sms, false, bud);
+  w.g[kRoleGU] = make_gemv_plan(2 * c.inter, c.hidden, B, sms, true, bud);
+  w.g[kRoleDown] = make_gemv_plan(c.hidden, c.inter, B, sms, false, bud);
   w.nsplit = attn_splits(B, c.n_kv, max_ctx, sms);
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -71,32 +193,19 @@ static WsPlan make_plan(const ft_block_cfg& c, int B, int max_ctx) {
     return o;
   };
   w.x_h = take((size_t)B * c.hidden * 2);
+  w.s_x = take((size_t)(c.hidden / 128) * 32 * 4);
   w.rho1 = take((size_t)B * 4);
-  // counters cleared by the prep kernel every call: sumsq2, attention tickets, GEMV tickets
-  w.zero = off;
-  size_t z = 0;
-  w.sumsq2 = off + z;
-  z += (size_t)B * 4;
-  w.attn_tick = off + z;
-  z += (size_t)B * c.n_kv * 4;
-  for (int r = 0; r < 4; ++r) {
-    w.gtick[r] = off + z;
-    z += (size_t)w.g[r].NMB * 4;
-  }
-  w.nzero_words = z / 4;
-  take(z);
+  w.h1 = take((size_t)B * c.hidden * 4);
   w.qkv = take((size_t)B * nqkv * 4);
   w.o_h = take((size_t)B * c.n_q * c.head_dim * 2);
-  w.h1 = take((size_t)B * c.hidden * 4);
+  w.s_o = take((size_t)(c.n_q * c.head_dim / 128) * 32 * 4);
   w.h1_h = take((size_t)B * c.hidden * 2);
+  w.s_h1 = take((size_t)(c.hidden / 128) * 32 * 4);
+  w.rho2 = take((size_t)B * 4);
   w.a_h = take((size_t)B * c.inter * 2);
-  w.attn_part = take((size_t)B * c.n_kv * w.nsplit * (16 + 8 * c.head_dim) * 4);
-  size_t sl = 0;
-  for (int r = 0; r < 4; ++r) {
-    const size_t s = (size_t)w.g[r].NMB * w.g[r].maxp * w.g[r].slotf * 4;
-    if (s > sl) sl = s;
-  }
-  w.slots = take(sl);
+  w.s_a = take((size_t)(c.inter / 128) * 32 * 4);
+  w.out_acc = take((size_t)B * c.hidden * 4);
+  w.tick = take((size_t)w.g[kRoleDown].NSET * 4);
   w.total = off;
   return w;
 }
@@ -128,68 +237,69 @@ static int run_block(const ft_block_cfg* c, const ft_layer_weights* w, void* cac
   if (overlaps(x_out, act_bytes, ws, ws_bytes) || overlaps(x_in, act_bytes, ws, ws_bytes)) return FT_ERR_INVALID_ARG;
 
   uint8_t* W = static_cast<uint8_t*>(ws);
+  auto F = [&](size_t off) { return reinterpret_cast<float*>(W + off); };
+  auto Hh = [&](size_t off) { return reinterpret_cast<__half*>(W + off); };
   const bool pdl = ft_host::pdl_enabled();
   const KVLayout L = kv_layout(*c, max_batch, max_ctx);
-  cudaError_t err = cudaSuccess;
+  const bool f32_out = act_dtype == FT_F32;
+  float* down_acc = f32_out ? static_cast<float*>(x_out) : F(P.out_acc);
 
   if (mask & FT_STAGE_PREP) {
-    PrepParams pp;
+    PrepParams pp = {};
     pp.x_in = x_in;
     pp.act_dtype = act_dtype;
     pp.B = B;
     pp.H = c->hidden;
     pp.eps = c->rms_eps;
-    pp.x_h = reinterpret_cast<__half*>(W + P.x_h);
-    pp.rho1 = reinterpret_cast<float*>(W + P.rho1);
-    pp.zero = reinterpret_cast<uint32_t*>(W + P.zero);
-    pp.nzero = (int)P.nzero_words;
+    pp.x_h = Hh(P.x_h);
+    pp.s_x = F(P.s_x);
+    pp.rho1 = F(P.rho1);
+    pp.h1 = F(P.h1);
+    pp.qkv = F(P.qkv);
+    pp.nqkv = (c->n_q + 2 * c->n_kv) * c->head_dim;
+    pp.s_o = F(P.s_o);
+    pp.nkg_o = c->n_q * c->head_dim / 128;
+    pp.s_a = F(P.s_a);
+    pp.nkg_a = c->inter / 128;
+    pp.tick = reinterpret_cast<uint32_t*>(W + P.tick);
+    pp.ntick = P.g[kRoleDown].NSET;
     pp.status = status;
-    err = launch_ex(prep_kernel, dim3(B), dim3(256), 0, st, pdl, pp);
-    if (err != cudaSuccess) return FT_ERR_CUDA;
+    if (launch_ex(prep_kernel, dim3(B), dim3(256), 0, st, pdl, pp) != cudaSuccess) return FT_ERR_CUDA;
   }
 
-  auto gemv = [&](int role, const void* wptr, size_t xoff) {
+  auto gemv = [&](int role, const void* wptr, size_t xoff, size_t soff) {
     GemvParams g = {};
     g.plan = P.g[role];
     g.w = static_cast<const uint8_t*>(wptr);
-    g.x = reinterpret_cast<const __half*>(W + xoff);
+    g.x = Hh(xoff);
+    g.s_in = F(soff);
     g.B = B;
-    g.tick = reinterpret_cast<uint32_t*>(W + P.gtick[role]);
-    g.slots = reinterpret_cast<float*>(W + P.slots);
-    g.H = c->hidden;
-    g.eps = c->rms_eps;
     g.status = status;
-    g.sumsq = reinterpret_cast<float*>(W + P.sumsq2);
     switch (role) {
-      case kRoleQKV:
-        g.rho = reinterpret_cast<const float*>(W + P.rho1);
-        g.out_f32 = reinterpret_cast<float*>(W + P.qkv);
-        break;
-      case kRoleO:
-        g.out_f32 = reinterpret_cast<float*>(W + P.h1);
-        g.out_h = reinterpret_cast<__half*>(W + P.h1_h);
-        g.resid = x_in;
-        g.resid_dtype = act_dtype;
-        break;
+      case kRoleQKV: g.out_f32 = F(P.qkv); break;
+      case kRoleO: g.out_f32 = F(P.h1); break;
       case kRoleGU:
-        g.out_h = reinterpret_cast<__half*>(W + P.a_h);
+        g.out_h = Hh(P.a_h);
+        g.s_out = F(P.s_a);
+        g.rho2 = F(P.rho2);
         break;
       case kRoleDown:
-        g.resid = W + P.h1;
-        g.resid_dtype = FT_F32;
+        g.out_f32 = down_acc;
         g.out_final = x_out;
         g.out_dtype = act_dtype;
+        g.tick = reinterpret_cast<uint32_t*>(W + P.tick);
         break;
     }
     return launch_gemv(role, g, st, pdl);
   };
 
   if (mask & FT_STAGE_QKV) {
-    if ((err = gemv(kRoleQKV, w->qkv, P.x_h)) != cudaSuccess) return FT_ERR_CUDA;
+    if (gemv(kRoleQKV, w->qkv, P.x_h, P.s_x) != cudaSuccess) return FT_ERR_CUDA;
   }
   if (mask & FT_STAGE_ATTN) {
     AttnParams a;
-    a.qkv = reinterpret_cast<const float*>(W + P.qkv);
+    a.qkv = F(P.qkv);
+    a.rho1 = F(P.rho1);
     a.cache = static_cast<uint8_t*>(cache);
     a.L = L;
     a.pos = pos;
@@ -201,22 +311,34 @@ static int run_block(const ft_block_cfg* c, const ft_layer_weights* w, void* cac
     a.nsplit = P.nsplit;
     a.Nqkv = (c->n_q + 2 * c->n_kv) * c->head_dim;
     a.qscale = (float)(1.4426950408889634 / std::sqrt((double)c->head_dim));
-    a.part = reinterpret_cast<float*>(W + P.attn_part);
-    a.tick = reinterpret_cast<uint32_t*>(W + P.attn_tick);
-    a.o_h = reinterpret_cast<__half*>(W + P.o_h);
+    a.o_h = Hh(P.o_h);
+    a.s_o = F(P.s_o);
     a.status = status;
     for (int i = 0; i < 64; ++i)
       a.inv_freq[i] = (i < c->head_dim / 2) ? std::pow((double)c->rope_base, -2.0 * i / c->head_dim) : 0.0;
-    if ((err = launch_attn(a, c->head_dim, st, pdl)) != cudaSuccess) return FT_ERR_CUDA;
+    if (launch_attn(a, c->head_dim, st, pdl) != cudaSuccess) return FT_ERR_CUDA;
   }
   if (mask & FT_STAGE_O) {
-    if ((err = gemv(kRoleO, w->o, P.o_h)) != cudaSuccess) return FT_ERR_CUDA;
+    if (gemv(kRoleO, w->o, P.o_h, P.s_o) != cudaSuccess) return FT_ERR_CUDA;
+  }
+  if (mask & FT_STAGE_MID) {
+    MidParams mp = {};
+    mp.h1 = F(P.h1);
+    mp.B = B;
+    mp.H = c->hidden;
+    mp.eps = c->rms_eps;
+    mp.h1_h = Hh(P.h1_h);
+    mp.s_h1 = F(P.s_h1);
+    mp.rho2 = F(P.rho2);
+    mp.out_acc = down_acc;
+    mp.status = status;
+    if (launch_ex(mid_kernel, dim3(B), dim3(256), 0, st, pdl, mp) != cudaSuccess) return FT_ERR_CUDA;
   }
   if (mask & FT_STAGE_GU) {
-    if ((err = gemv(kRoleGU, w->gateup, P.h1_h)) != cudaSuccess) return FT_ERR_CUDA;
+    if (gemv(kRoleGU, w->gateup, P.h1_h, P.s_h1) != cudaSuccess) return FT_ERR_CUDA;
   }
   if (mask & FT_STAGE_DOWN) {
-    if ((err = gemv(kRoleDown, w->down, P.a_h)) != cudaSuccess) return FT_ERR_CUDA;
+    if (gemv(kRoleDown, w->down, P.a_h, P.s_a) != cudaSuccess) return FT_ERR_CUDA;
   }
   return FT_OK;
 }
@@ -236,6 +358,7 @@ int ft_decode_workspace_layout(const ft_block_cfg* c, int B, int max_ctx, ft_ws_
   if (!out || B < 1 || B > 32 || max_ctx < 1) return FT_ERR_INVALID_ARG;
   const ft::WsPlan P = ft::make_plan(*c, B, max_ctx);
   out->qkv = P.qkv;
+  out->rho1 = P.rho1;
   out->o = P.o_h;
   out->h1 = P.h1;
   out->a = P.a_h;
@@ -258,6 +381,6 @@ int ft_decode_block_stages(const ft_block_cfg* c, const ft_layer_weights* w, voi
                        (cudaStream_t)stream);
 }
 
-int ft_decode_block_launches(void) { return 6; }
+int ft_decode_block_launches(void) { return 7; }
 
 }  // extern "C"

@@ -9,22 +9,24 @@ namespace ft {
 enum GemvRole { kRoleQKV = 0, kRoleO = 1, kRoleGU = 2, kRoleDown = 3 };
 
 // Streaming GEMV work partition for one projection.
-// Units are (macro block mb, input group kg) pairs, mb-major, where a macro
-// block is RB consecutive 128-row blocks processed together (RB = NT, the
-// number of 8-token MMA column tiles, so B-fragments are reused RB times).
-// CTA c owns the contiguous unit range [u0(c), u1(c)); a macro block cut by a
-// range boundary is a split-K reduction: each piece writes its partial sums to
-// a slot and the last piece to finish (atomic ticket) sums the slots in piece
-// order and runs the epilogue.
+// Units are (row-tile set, input group) pairs, set-major; a set is RT
+// consecutive 16-row tiles processed together so each activation B fragment is
+// reused RT times.  CTA c owns the contiguous unit range [u0(c), u1(c)); with
+// `whole` the ranges are whole sets (no set is split across CTAs).
 struct GemvPlan {
-  int N, K, NRB, NKG, RB, NT, NMB;
-  int U, C, per, rem, maxp;
-  int slotf;  // floats per partial slot (8 warps x RB x NT x 128)
+  int N, K, NTILE, NKG;        // rows, inputs, 16-row tiles, 128-input groups
+  int NT, RT, NCW, NSET;       // 8-token column tiles, row tiles per set, consumer warps, sets
+  int whole, C, per, rem;      // partition of units over C CTAs
+  int ng;                      // groups per stage
+  int stages, slot, xoff, soff, xstride;  // ring geometry (bytes)
+  int redoff, slotoff, smem;   // shared-memory map
 };
 
 __host__ __device__ __forceinline__ int plan_u0(const GemvPlan& p, int c) {
-  return c * p.per + (c < p.rem ? c : p.rem);
+  const int u = c * p.per + (c < p.rem ? c : p.rem);
+  return p.whole ? u * p.NKG : u;
 }
+// CTA owning unit u (split partitions only).
 __host__ __device__ __forceinline__ int plan_owner(const GemvPlan& p, int u) {
   const int big = p.rem * (p.per + 1);
   return (u < big) ? u / (p.per + 1) : p.rem + (u - big) / p.per;
@@ -32,55 +34,72 @@ __host__ __device__ __forceinline__ int plan_owner(const GemvPlan& p, int u) {
 
 struct GemvParams {
   GemvPlan plan;
-  const uint8_t* w;  // packed weights of this role
-  const __half* x;   // FP16 activation operand [B][K]
+  const uint8_t* w;   // packed weights of this role
+  const __half* x;    // activation operand [B][K] (operand layout, see op_slot)
+  const float* s_in;  // its group offsets [K/128][32]
   int B;
-  uint32_t* tick;    // [NMB]
-  float* slots;      // [NMB][maxp][slotf]
-  // epilogue operands
-  const float* rho;     // QKV: rho1[B]
-  float* out_f32;       // QKV: qkv [B][N];  O: h1 [B][N]
-  __half* out_h;        // O: h1 as FP16;  GU: a [B][I]
-  const void* resid;    // O: block input (act dtype);  DOWN: h1 FP32
-  int resid_dtype;
-  float* sumsq;         // O: accumulates sum h1^2;  GU: reads it
-  void* out_final;      // DOWN: block output (act dtype)
+  uint32_t* tick;     // DOWN: per-set tickets [NSET]
+  float* out_f32;     // QKV: qkv acc;  O: h1 acc;  DOWN: out acc (or the FP32 output)
+  __half* out_h;      // GU: a operand [B][I]
+  float* s_out;       // GU: a's group offsets [I/128][32] (accumulated)
+  const float* rho2;  // GU: RMSNorm row factor of h1 [B]
+  void* out_final;    // DOWN: block output
   int out_dtype;
-  int H;
-  float eps;
   int32_t* status;
 };
 
 struct AttnParams {
-  const float* qkv;   // [B][Nqkv], rho1 applied, before RoPE
+  const float* qkv;   // [B][Nqkv] accumulated projections, before rho1 and RoPE
+  const float* rho1;  // [B] RMSNorm row factor of the block input
   uint8_t* cache;
   KVLayout L;
   const int32_t* pos;
   int B, nq, nkv, G, hb, nsplit, Nqkv;
   float qscale;       // log2(e) / sqrt(d), folded into the rotated query
-  float* part;        // [B][nkv][nsplit][16 + 8 d]
-  uint32_t* tick;     // [B * nkv]
-  __half* o_h;        // [B][nq d]
+  __half* o_h;        // [B][nq d] attention output (operand layout)
+  float* s_o;         // its group offsets [nq d / 128][32] (accumulated)
   int32_t* status;
   double inv_freq[64];
 };
 
+// Block input -> QKV operand, rho1, h1 accumulator initialised to x, and the
+// accumulators of this call cleared.  One CTA per request.
 struct PrepParams {
   const void* x_in;
   int act_dtype, B, H;
   float eps;
-  __half* x_h;
-  float* rho1;
-  uint32_t* zero;  // counters cleared every call
-  int nzero;
+  __half* x_h;       // [B][H] operand
+  float* s_x;        // [H/128][32]
+  float* rho1;       // [B]
+  float* h1;         // [B][H] <- x
+  float* qkv;        // [B][Nqkv] <- 0
+  int nqkv;
+  float* s_o;        // [NKG_o][32] <- 0 (column b)
+  int nkg_o;
+  float* s_a;        // [NKG_a][32] <- 0 (column b)
+  int nkg_a;
+  uint32_t* tick;    // down tickets <- 0
+  int ntick;
+  int32_t* status;
+};
+
+// Between O and gate/up: h1 -> its operand and offsets, rho2, and the down
+// accumulator initialised to h1.  One CTA per request.
+struct MidParams {
+  const float* h1;   // [B][H] complete after O
+  int B, H;
+  float eps;
+  __half* h1_h;      // [B][H] operand
+  float* s_h1;       // [H/128][32]
+  float* rho2;       // [B]
+  float* out_acc;    // [B][H] <- h1
   int32_t* status;
 };
 
 // host-side launchers (ft_gemv.cu / ft_attn.cu / ft_block.cu)
 cudaError_t launch_gemv(int role, const GemvParams& p, cudaStream_t st, bool pdl);
 cudaError_t launch_attn(const AttnParams& p, int head_dim, cudaStream_t st, bool pdl);
-GemvPlan make_gemv_plan(int N, int K, int B, int sms);
-size_t gemv_smem_bytes(int NT);
+GemvPlan make_gemv_plan(int N, int K, int B, int sms, bool whole_sets, int smem_budget);
 
 template <typename... Args>
 cudaError_t launch_ex(void (*kernel)(Args...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool pdl,

@@ -2,253 +2,294 @@
 //
 // y[t, o] = sum_g s[o, g] * sum_{i in g} (c[o, i] - 8) * x[t, i]
 // with the group scale applied after each 128-input partial sum (summary page,
-// "무엇과 다른가"), followed by a role-specific epilogue: the RMSNorm row
-// factor (QKV, "어떻게 동작하나": rho applied after accumulation), the residual
-// (O, down) or SwiGLU (gate/up).
+// "무엇과 다른가"), followed by a role epilogue.  The RMSNorm row factors are
+// not applied here: the consumer of each output applies them after the
+// accumulation (summary page, "어떻게 동작하나").
 //
 // GB300 design:
-//  * one CTA per SM, 9 warps: warp 8 is a producer that streams the CTA's
-//    contiguous run of packed weight slabs with 1-D bulk async copies
-//    (cp.async.bulk, mbarrier completion) into a ring of STAGES slots, and
-//    copies the matching 128-input chunks of the FP16 activation rows next to
-//    them.  Weights do not depend on earlier kernels, so the producer fills the
-//    whole ring BEFORE waiting on the previous kernel (programmatic dependent
-//    launch): the weight stream overlaps the previous kernel's tail.
-//  * warps 0-7 consume: each owns one 16-row tile of every 128-row block in the
-//    macro block, dequantises nibbles in registers into FP16 tensor-core A
-//    fragments (exact: (c-8) is representable) and runs mma.m16n8k16 with FP32
-//    accumulation; activation B fragments are read from shared memory once per
-//    k-step and reused across the RB row tiles.  Tensor cores here reduce the
-//    per-weight instruction count (one MMA replaces 256 FMAs); the kernel is
-//    bound by HBM bandwidth.
-//  * split-K across CTAs with deterministic reduction: partial sums go to
-//    per-piece slots and the last piece (atomic ticket, no waiting) adds them
-//    in piece order.
+//  * one CTA per SM: one producer warp streams the CTA's contiguous run of
+//    (row tile, group) slabs with 1-D bulk async copies (cp.async.bulk, mbarrier
+//    completion) into a ring of stages sized at launch, next to the matching
+//    chunk of the FP16 activation operand and its group offsets.  Weights do
+//    not depend on earlier kernels, so the ring fills BEFORE the producer waits
+//    on its predecessor (programmatic dependent launch).
+//  * NCW consumer warps split each stage's groups; each keeps RT row tiles x
+//    NT eight-token column tiles in registers.  Nibbles become FP16 A fragments
+//    with four logic ops and a shift per 8 weights (magic_word: the 1024-offset
+//    mantissa trick) and run through mma.m16n8k16 with FP32 accumulation; the
+//    offset is removed by starting each group's chain at -S (see ft_internal).
+//  * split-K: warps reduce through shared memory at the end of a row-tile set;
+//    across CTAs the partial sums are red.add-ed into an FP32 accumulator that
+//    the next kernel reads (QKV, O) or, for the BF16 down output, the last piece
+//    of a set (atomic ticket, never waits) converts it.  Gate/up CTAs own whole
+//    row-tile sets, so SwiGLU needs no cross-CTA step.
 #include "ft_block.cuh"
 
 namespace ft {
 
+// RT row tiles per set share every activation fragment (RT x NT independent
+// MMA chains per warp); NCW consumer warps split a stage's groups.
 template <int NT>
-struct GemvCfg {
-  static constexpr int RB = NT;
-  static constexpr int NGS = (RB == 1) ? 2 : 1;                // groups per stage
-  static constexpr int STAGES = (RB <= 2) ? 5 : 4;
-  static constexpr int WBYTES = RB * NGS * kBlockGroupBytes;     // weight bytes per slot
-  static constexpr int XROW = NGS * kWGroup + 8;                 // halfs per activation row
-  static constexpr int XBYTES = 8 * NT * XROW * 2;
-  static constexpr int SLOT = WBYTES + XBYTES;
-  static constexpr int SMEM = 128 + SLOT * STAGES;
-  static constexpr int THREADS = 288;
-};
+struct GemvShape;
+template <> struct GemvShape<1> { static constexpr int RT = 4, NCW = 8; };
+template <> struct GemvShape<2> { static constexpr int RT = 4, NCW = 8; };
+template <> struct GemvShape<3> { static constexpr int RT = 4, NCW = 4; };
+template <> struct GemvShape<4> { static constexpr int RT = 4, NCW = 4; };
 
-struct ConsumerSync {
-  uint32_t bar;
-  uint32_t phase;
-  // bounded barrier of the 8 consumer warps (an mbarrier with count 8)
-  __device__ __forceinline__ bool sync() {
-    __syncwarp();
-    if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
-    const bool ok = mbar_wait(bar, phase);
-    phase ^= 1;
-    __syncwarp();
-    return ok;
-  }
-};
+__device__ __forceinline__ void red_add(float* p, float v) { atomicAdd(p, v); }
 
-template <int NT, int ROLE>
-__device__ __forceinline__ void gemv_epilogue(const GemvParams& p, int mb, int nrb, float (&tot)[NT][NT][4]) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, tig = lane & 3;
+// Epilogue of one (row tile, column tile) of fully reduced values.
+// v[0] = (row g, token t0), v[1] = (row g, t0+1), v[2] = (row g+8, t0), v[3] = (row g+8, t0+1).
+template <int ROLE>
+__device__ __forceinline__ bool gemv_epi(const GemvParams& p, int T, int j, const float (&v)[4], bool direct) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, tig = lane & 3;
   const int N = p.plan.N;
-  bool range_bad = false;
+  const int r0 = T * kRowTile + g, r1 = r0 + 8;
+  bool bad = false;
+  if constexpr (ROLE == kRoleGU) {
+    const int inter = N / 2;
+    const int kcol = 8 * T + g;  // a column produced by packed rows g (gate) and g + 8 (up)
+    const int grp = kcol / kWGroup;
 #pragma unroll
-  for (int j = 0; j < NT; ++j) {
-    float sq[2] = {0.0f, 0.0f};
-#pragma unroll
-    for (int rb = 0; rb < NT; ++rb) {
-      if (rb >= nrb) continue;
-      const int rbg = mb * NT + rb;
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const int e = r & 1;
-        const int t = 8 * j + 2 * tig + e;
-        if (t >= p.B) continue;
-        const float val = tot[rb][j][r];
-        const int row = rbg * kRowBlock + warp * kRowTile + g + ((r & 2) ? 8 : 0);
-        if (ROLE == kRoleQKV) {
-          p.out_f32[(size_t)t * N + row] = p.rho[t] * val;
-        } else if (ROLE == kRoleO) {
-          const float xin = (p.resid_dtype == FT_F32)
-                                ? ld_cg_f32(static_cast<const float*>(p.resid) + (size_t)t * N + row)
-                                : bf16_bits_to_f32(static_cast<const uint16_t*>(p.resid)[(size_t)t * N + row]);
-          const float h1 = xin + val;
-          p.out_f32[(size_t)t * N + row] = h1;
-          p.out_h[(size_t)t * N + row] = __float2half_rn(h1);
-          range_bad |= !(fabsf(h1) <= 65504.0f);
-          sq[e] += h1 * h1;
-        } else if (ROLE == kRoleDown) {
-          const float y = ld_cg_f32(static_cast<const float*>(p.resid) + (size_t)t * N + row) + val;
-          if (p.out_dtype == FT_F32)
-            static_cast<float*>(p.out_final)[(size_t)t * N + row] = y;
-          else
-            static_cast<uint16_t*>(p.out_final)[(size_t)t * N + row] =
-                __bfloat16_as_ushort(__float2bfloat16_rn(y));
-        }
+    for (int e = 0; e < 2; ++e) {
+      const int t = 8 * j + 2 * tig + e;
+      float st = 0.0f;
+      if (t < p.B) {
+        const float rho2 = p.rho2[t];
+        const float gv = rho2 * v[e], uv = rho2 * v[2 + e];
+        const float a = gv / (1.0f + expf(-gv)) * uv;
+        bad |= !(fabsf(a) <= 65504.0f);
+        p.out_h[(size_t)t * inter + op_slot(kcol)] = op_encode(a, kcol, st);
       }
-      if (ROLE == kRoleGU) {
-        // rows g (gate) and g + 8 (up) of global tile T hold a-column 8 T + g
-        const int T = rbg * kTilesPerBlock + warp;
-        const int inter = N / 2;
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int t = 8 * j + 2 * tig + e;
-          if (t >= p.B) continue;
-          const float rho2 = rsqrtf(ld_cg_f32(p.sumsq + t) / (float)p.H + p.eps);
-          const float gv = rho2 * tot[rb][j][e];
-          const float uv = rho2 * tot[rb][j][2 + e];
-          const float a = gv / (1.0f + expf(-gv)) * uv;
-          range_bad |= !(fabsf(a) <= 65504.0f);
-          p.out_h[(size_t)t * inter + 8 * T + g] = __float2half_rn(a);
-        }
-      }
+      st += __shfl_xor_sync(0xffffffffu, st, 4);
+      st += __shfl_xor_sync(0xffffffffu, st, 8);
+      st += __shfl_xor_sync(0xffffffffu, st, 16);
+      if (g == 0 && t < p.B) atomicAdd(p.s_out + grp * 32 + t, st);
     }
-    if (ROLE == kRoleO) {
+    return bad;
+  } else {
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        float v = sq[e];
-        v += __shfl_xor_sync(0xffffffffu, v, 4);
-        v += __shfl_xor_sync(0xffffffffu, v, 8);
-        v += __shfl_xor_sync(0xffffffffu, v, 16);
-        const int t = 8 * j + 2 * tig + e;
-        if (g == 0 && t < p.B) atomicAdd(p.sumsq + t, v);
-      }
+  for (int r = 0; r < 4; ++r) {
+    const int t = 8 * j + 2 * tig + (r & 1);
+    if (t >= p.B) continue;
+    const int row = (r & 2) ? r1 : r0;
+    float* acc = p.out_f32 + (size_t)t * N + row;
+    if (ROLE == kRoleDown && direct) {
+      const float y = __ldcg(acc) + v[r];
+      if (p.out_dtype == FT_F32)
+        static_cast<float*>(p.out_final)[(size_t)t * N + row] = y;
+      else
+        static_cast<uint16_t*>(p.out_final)[(size_t)t * N + row] = __bfloat16_as_ushort(__float2bfloat16_rn(y));
+    } else {
+      red_add(acc, v[r]);
     }
   }
-  if (range_bad) set_status(p.status, FT_DEV_RANGE);
+  return bad;
+  }
 }
 
+// Walks a CTA's unit range stage by stage (set, first group, group count) with
+// no divisions in the loop; every warp role runs the same walk.
+struct StageWalk {
+  int u, u1, set, kg, ng, NKG, cap;
+  __device__ __forceinline__ StageWalk(const GemvPlan& pl, int u0, int u1_) {
+    u = u0;
+    u1 = u1_;
+    NKG = pl.NKG;
+    cap = pl.ng;
+    set = u0 / NKG;
+    kg = u0 - set * NKG;
+    ng = min(min(cap, NKG - kg), u1 - u);
+  }
+  __device__ __forceinline__ bool valid() const { return u < u1; }
+  // true if the stage just finished ends this CTA's piece of its set
+  __device__ __forceinline__ bool piece_end() const { return u + ng >= u1 || kg + ng == NKG; }
+  __device__ __forceinline__ void next() {
+    u += ng;
+    kg += ng;
+    if (kg == NKG) {
+      kg = 0;
+      ++set;
+    }
+    ng = min(min(cap, NKG - kg), u1 - u);
+  }
+};
+
 template <int NT, int ROLE>
-__global__ void __launch_bounds__(288, 1) gemv_kernel(const GemvParams p) {
-  using C = GemvCfg<NT>;
-  constexpr int RB = C::RB;
+__global__ void __launch_bounds__((GemvShape<NT>::NCW + 2) * 32, 1) gemv_kernel(const GemvParams p) {
+  constexpr int RT = GemvShape<NT>::RT, NCW = GemvShape<NT>::NCW;
+  constexpr int PRODUCER = NCW, EPILOGUE = NCW + 1;
   extern __shared__ __align__(128) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const GemvPlan& pl = p.plan;
   const int cta = blockIdx.x;
   const int u0 = plan_u0(pl, cta), u1 = plan_u0(pl, cta + 1);
-  const uint32_t full0 = smem_u32(smem), empty0 = full0 + 8 * C::STAGES, sync_bar = empty0 + 8 * C::STAGES;
-  uint8_t* slots = smem + 128;
-  volatile uint32_t* flag = reinterpret_cast<volatile uint32_t*>(smem + 8 * (2 * C::STAGES + 1));
+  const int S = pl.stages;
+  // barriers: full[S], empty[S], red_full, red_empty
+  const uint32_t full0 = smem_u32(smem), empty0 = full0 + 8 * S;
+  const uint32_t red_full = empty0 + 8 * S, red_empty = red_full + 8;
+  float* red = reinterpret_cast<float*>(smem + pl.redoff);
+  uint8_t* slots = smem + pl.slotoff;
 
   griddep_launch();
   if (tid == 0) {
-    for (int s = 0; s < C::STAGES; ++s) {
+    for (int s = 0; s < S; ++s) {
       mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, 8);
+      mbar_init(empty0 + 8 * s, NCW);
     }
-    mbar_init(sync_bar, 8);
+    mbar_init(red_full, NCW);
+    mbar_init(red_empty, 1);
     mbar_fence_init();
-  }
-  // activation rows of tokens >= B are never copied: keep them zero
-  {
-    const int padrows = 8 * NT - p.B;
-    const int words = padrows * (C::XROW / 2);
-    for (int i = tid; i < C::STAGES * words; i += C::THREADS) {
-      const int s = i / words, k = i % words;
-      uint32_t* xs = reinterpret_cast<uint32_t*>(slots + s * C::SLOT + C::WBYTES);
-      xs[p.B * (C::XROW / 2) + k] = 0u;
-    }
   }
   __syncthreads();
 
-  if (warp == 8) {
-    // ---------------- producer
+  if (warp == PRODUCER) {
+    // ------------------------------------------------------------ producer
     auto issue_x = [&](int slot, int kg, int ng) {
-      if (lane < p.B) {
-        const uint32_t dst = smem_u32(slots + slot * C::SLOT + C::WBYTES) + lane * C::XROW * 2;
-        bulk_g2s(dst, p.x + (size_t)lane * pl.K + (size_t)kg * kWGroup, ng * kWGroup * 2, full0 + 8 * slot);
-      }
+      uint8_t* sb = slots + slot * pl.slot;
+      if (lane < p.B)
+        bulk_g2s(smem_u32(sb + pl.xoff) + lane * pl.xstride, p.x + (size_t)lane * pl.K + (size_t)kg * kWGroup,
+                 ng * kWGroup * 2, full0 + 8 * slot);
+      if (lane == 31) bulk_g2s(smem_u32(sb + pl.soff), p.s_in + (size_t)kg * 32, ng * 128, full0 + 8 * slot);
     };
     bool waited = false;
-    int s = 0;
-    for (int u = u0; u < u1; ++s) {
-      const int mb = u / pl.NKG, kg = u - mb * pl.NKG;
-      const int ng = min(min(C::NGS, pl.NKG - kg), u1 - u);
-      const int slot = s % C::STAGES;
-      if (s >= C::STAGES && !mbar_wait(empty0 + 8 * slot, ((s / C::STAGES) - 1) & 1)) {
+    int s = 0, slot = 0, round = 0;
+    for (StageWalk st(pl, u0, u1); st.valid(); st.next(), ++s) {
+      if (round > 0 && !mbar_wait(empty0 + 8 * slot, (round - 1) & 1)) {
         set_status(p.status, FT_DEV_TIMEOUT);
         break;
       }
-      const int nrb = min(RB, pl.NRB - mb * RB);
-      const uint32_t sb = smem_u32(slots + slot * C::SLOT);
+      const int nrt = min(RT, pl.NTILE - st.set * RT);
       if (lane == 0) {
-        mbar_arrive_expect_tx(full0 + 8 * slot, (uint32_t)(nrb * ng * kBlockGroupBytes + p.B * ng * kWGroup * 2));
-        for (int rb = 0; rb < nrb; ++rb)
-          bulk_g2s(sb + rb * ng * kBlockGroupBytes,
-                   p.w + ((size_t)(mb * RB + rb) * pl.NKG + kg) * kBlockGroupBytes, ng * kBlockGroupBytes,
-                   full0 + 8 * slot);
+        mbar_arrive_expect_tx(full0 + 8 * slot,
+                              (uint32_t)(nrt * st.ng * kSlabBytes + p.B * st.ng * kWGroup * 2 + st.ng * 128));
+        const uint32_t sb = smem_u32(slots + slot * pl.slot);
+        for (int rt = 0; rt < nrt; ++rt)
+          bulk_g2s(sb + rt * pl.ng * kSlabBytes, p.w + ((size_t)(st.set * RT + rt) * pl.NKG + st.kg) * kSlabBytes,
+                   st.ng * kSlabBytes, full0 + 8 * slot);
       }
       __syncwarp();
-      if (waited) issue_x(slot, kg, ng);
-      u += ng;
-      if (!waited && (s == C::STAGES - 1 || u >= u1)) {
-        // the ring is full of weights: now wait for the activations' producer
-        griddep_wait();
+      if (waited) issue_x(slot, st.kg, st.ng);
+      if (!waited && (s == S - 1 || st.u + st.ng >= u1)) {
+        griddep_wait();  // the activation operand comes from the previous kernel
         waited = true;
-        int uu = u0;
-        for (int ss = 0; ss <= s; ++ss) {
-          const int mb2 = uu / pl.NKG, kg2 = uu - mb2 * pl.NKG;
-          const int ng2 = min(min(C::NGS, pl.NKG - kg2), u1 - uu);
-          issue_x(ss, kg2, ng2);
-          uu += ng2;
-        }
+        int ss = 0;
+        for (StageWalk s2(pl, u0, u1); ss <= s; s2.next(), ++ss) issue_x(ss, s2.kg, s2.ng);
+      }
+      if (++slot == S) {
+        slot = 0;
+        ++round;
       }
     }
     if (!waited) griddep_wait();
     return;
   }
 
-  // ---------------- consumers (warps 0..7)
-  griddep_wait();
-  ConsumerSync cs{sync_bar, 0};
-  const int g = lane >> 2, tig = lane & 3;
-  float tot[RB][NT][4];
+  if (warp == EPILOGUE) {
+    // ------------------------------------------------------------ epilogue
+    // Reduces each finished piece over the consumer warps and applies the role
+    // epilogue while the consumers already stream the next piece.
+    griddep_wait();
+    bool bad = false;
+    int k = 0, piece_kg0 = -1;
+    for (StageWalk st(pl, u0, u1); st.valid(); st.next()) {
+      if (piece_kg0 < 0) piece_kg0 = st.kg;
+      if (!st.piece_end()) continue;
+      const bool whole = (piece_kg0 == 0) && (st.kg + st.ng == pl.NKG);
+      piece_kg0 = -1;
+      const int nrt = min(RT, pl.NTILE - st.set * RT);
+      if (!mbar_wait(red_full, k & 1)) {
+        set_status(p.status, FT_DEV_TIMEOUT);
+        return;
+      }
+      for (int q = 0; q < RT * NT; ++q) {
+        const int rt = q / NT, j = q % NT;
+        if (rt >= nrt) continue;
+        float v[4];
 #pragma unroll
-  for (int a = 0; a < RB; ++a)
+        for (int r = 0; r < 4; ++r) {
+          float a = 0.0f;
+#pragma unroll
+          for (int w = 0; w < NCW; ++w) a += red[((w * RT * NT + q) * 4 + r) * 32 + lane];
+          v[r] = a;
+        }
+        bad |= gemv_epi<ROLE>(p, st.set * RT + rt, j, v, whole);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(red_empty);
+      if (ROLE == kRoleDown && !whole && p.out_dtype != FT_F32) {
+        // the last piece of this set converts the FP32 accumulator to BF16
+        __threadfence();
+        __syncwarp();
+        const int first = plan_owner(pl, st.set * pl.NKG);
+        const int np = plan_owner(pl, st.set * pl.NKG + pl.NKG - 1) - first + 1;
+        uint32_t last = 0;
+        if (lane == 0) last = (atomicAdd(p.tick + st.set, 1u) == (uint32_t)(np - 1)) ? 1u : 0u;
+        last = __shfl_sync(0xffffffffu, last, 0);
+        if (last) {
+          __threadfence();
+          const int rows = nrt * kRowTile;
+          for (int i = lane; i < rows * p.B; i += 32) {
+            const int t = i / rows, row = st.set * RT * kRowTile + i % rows;
+            const float y = __ldcg(p.out_f32 + (size_t)t * pl.N + row);
+            static_cast<uint16_t*>(p.out_final)[(size_t)t * pl.N + row] =
+                __bfloat16_as_ushort(__float2bfloat16_rn(y));
+          }
+          if (lane == 0) p.tick[st.set] = 0u;
+        }
+      }
+      ++k;
+    }
+    if (bad) set_status(p.status, FT_DEV_RANGE);
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  griddep_wait();
+  const int g = lane >> 2, tig = lane & 3;
+  float tot[RT][NT][4];
+#pragma unroll
+  for (int a = 0; a < RT; ++a)
 #pragma unroll
     for (int b = 0; b < NT; ++b)
 #pragma unroll
       for (int r = 0; r < 4; ++r) tot[a][b][r] = 0.0f;
 
-  int s = 0, piece_kg0 = -1;
-  for (int u = u0; u < u1; ++s) {
-    const int mb = u / pl.NKG, kg = u - mb * pl.NKG;
-    const int ng = min(min(C::NGS, pl.NKG - kg), u1 - u);
-    if (piece_kg0 < 0) piece_kg0 = kg;
-    const int slot = s % C::STAGES;
-    if (!mbar_wait(full0 + 8 * slot, (s / C::STAGES) & 1)) {
+  int slot = 0, fphase = 0, k = 0;
+  for (StageWalk st(pl, u0, u1); st.valid(); st.next()) {
+    if (!mbar_wait(full0 + 8 * slot, fphase)) {
       set_status(p.status, FT_DEV_TIMEOUT);
       return;
     }
-    const int nrb = min(RB, pl.NRB - mb * RB);
-    const uint8_t* sw = slots + slot * C::SLOT;
-    const uint8_t* sx = sw + C::WBYTES;
-    for (int kgl = 0; kgl < ng; ++kgl) {
-      float acc[RB][NT][4];
-      uint32_t sc[RB];
+    const int nrt = min(RT, pl.NTILE - st.set * RT);
+    const uint8_t* sw = slots + slot * pl.slot;
+    const uint8_t* sx = sw + pl.xoff;
+    const float* ss = reinterpret_cast<const float*>(sw + pl.soff);
+    for (int kgl = warp; kgl < st.ng; kgl += NCW) {
+      // group offsets -S of this group for the lane's two token columns
+      float c0[NT][2];
+#pragma unroll
+      for (int j = 0; j < NT; ++j) {
+        const int t = 8 * j + 2 * tig;
+        const float2 sv = *reinterpret_cast<const float2*>(ss + kgl * 32 + t);
+        c0[j][0] = (t < p.B) ? -sv.x : 0.0f;
+        c0[j][1] = (t + 1 < p.B) ? -sv.y : 0.0f;
+      }
+      uint32_t sc[RT];
+      float acc[RT][NT][4];
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
-        // nibble words of k-steps 4 half .. 4 half + 3 for each row tile
-        uint32_t wd[RB][4];
+        uint32_t wd[RT][4];
 #pragma unroll
-        for (int rb = 0; rb < RB; ++rb) {
-          if (rb < nrb) {
-            const uint8_t* slab = sw + ((rb * ng + kgl) * kTilesPerBlock + warp) * kSlabBytes;
+        for (int rt = 0; rt < RT; ++rt) {
+          if (rt < nrt) {
+            const uint8_t* slab = sw + (rt * pl.ng + kgl) * kSlabBytes;
             const uint4 q = *reinterpret_cast<const uint4*>(slab + half * 512 + lane * 16);
-            wd[rb][0] = q.x; wd[rb][1] = q.y; wd[rb][2] = q.z; wd[rb][3] = q.w;
-            if (half == 0) sc[rb] = *reinterpret_cast<const uint32_t*>(slab + kSlabCodes + 4 * g);
+            wd[rt][0] = q.x; wd[rt][1] = q.y; wd[rt][2] = q.z; wd[rt][3] = q.w;
+            if (half == 0) sc[rt] = *reinterpret_cast<const uint32_t*>(slab + kSlabCodes + 4 * g);
           } else {
-            wd[rb][0] = wd[rb][1] = wd[rb][2] = wd[rb][3] = 0x88888888u;
-            if (half == 0) sc[rb] = 0u;
+            wd[rt][0] = wd[rt][1] = wd[rt][2] = wd[rt][3] = 0u;
+            if (half == 0) sc[rt] = 0u;
           }
         }
 #pragma unroll
@@ -257,116 +298,85 @@ __global__ void __launch_bounds__(288, 1) gemv_kernel(const GemvParams p) {
           uint32_t b0[NT], b1[NT];
 #pragma unroll
           for (int j = 0; j < NT; ++j) {
-            const uint8_t* xr = sx + ((8 * j + g) * C::XROW + kgl * kWGroup + ks * 16 + 2 * tig) * 2;
-            b0[j] = *reinterpret_cast<const uint32_t*>(xr);
-            b1[j] = *reinterpret_cast<const uint32_t*>(xr + 16);
+            const int row = 8 * j + g;
+            const uint2 bv = *reinterpret_cast<const uint2*>(sx + min(row, p.B - 1) * pl.xstride +
+                                                            (kgl * kWGroup + ks * 16 + 4 * tig) * 2);
+            b0[j] = (row < p.B) ? bv.x : 0u;
+            b1[j] = (row < p.B) ? bv.y : 0u;
           }
 #pragma unroll
-          for (int rb = 0; rb < RB; ++rb) {
-            if (rb < nrb) {
-              uint32_t a[4];
-              dequant_word(wd[rb][kq], a);
+          for (int rt = 0; rt < RT; ++rt) {
+            if (rt < nrt) {
+              uint32_t r[4];
+              magic_word(wd[rt][kq], r);
+              const uint32_t a[4] = {r[0], r[2], r[1], r[3]};
 #pragma unroll
               for (int j = 0; j < NT; ++j) {
-                if (ks == 0)
-                  mma_f16_zc(acc[rb][j], a, b0[j], b1[j]);
-                else
-                  mma_f16(acc[rb][j], a, b0[j], b1[j]);
+                if (ks == 0) {
+                  float* d = acc[rt][j];
+                  d[0] = c0[j][0]; d[1] = c0[j][1]; d[2] = c0[j][0]; d[3] = c0[j][1];
+                }
+                mma_f16(acc[rt][j], a, b0[j], b1[j]);
               }
             }
           }
         }
       }
 #pragma unroll
-      for (int rb = 0; rb < RB; ++rb) {
-        if (rb < nrb) {
-          const float slo = bf16_bits_to_f32((uint16_t)(sc[rb] & 0xFFFFu));
-          const float shi = bf16_bits_to_f32((uint16_t)(sc[rb] >> 16));
+      for (int rt = 0; rt < RT; ++rt) {
+        if (rt < nrt) {
+          const float slo = bf16_bits_to_f32((uint16_t)(sc[rt] & 0xFFFFu));
+          const float shi = bf16_bits_to_f32((uint16_t)(sc[rt] >> 16));
 #pragma unroll
-          for (int j = 0; j < NT; ++j) {
-            tot[rb][j][0] = fmaf(slo, acc[rb][j][0], tot[rb][j][0]);
-            tot[rb][j][1] = fmaf(slo, acc[rb][j][1], tot[rb][j][1]);
-            tot[rb][j][2] = fmaf(shi, acc[rb][j][2], tot[rb][j][2]);
-            tot[rb][j][3] = fmaf(shi, acc[rb][j][3], tot[rb][j][3]);
-          }
+          for (int j = 0; j < NT; ++j)
+#pragma unroll
+            for (int r = 0; r < 4; ++r) tot[rt][j][r] = fmaf((r & 2) ? shi : slo, acc[rt][j][r], tot[rt][j][r]);
         }
       }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(empty0 + 8 * slot);
-    u += ng;
+    if (++slot == S) {
+      slot = 0;
+      fphase ^= 1;
+    }
 
-    if (u >= u1 || u % pl.NKG == 0) {
-      // ---- end of a piece of macro block mb
-      const bool full = (piece_kg0 == 0) && (u == (mb + 1) * pl.NKG);
-      piece_kg0 = -1;
-      if (!full) {
-        const int first = plan_owner(pl, mb * pl.NKG);
-        const int np = plan_owner(pl, mb * pl.NKG + pl.NKG - 1) - first + 1;
-        const int pidx = cta - first;
-        float* base = p.slots + ((size_t)mb * pl.maxp) * pl.slotf;
-        float* mine = base + (size_t)pidx * pl.slotf;
-#pragma unroll
-        for (int rb = 0; rb < RB; ++rb)
-#pragma unroll
-          for (int j = 0; j < NT; ++j)
-#pragma unroll
-            for (int r = 0; r < 4; ++r)
-              __stcg(mine + (((warp * RB + rb) * NT + j) * 4 + r) * 32 + lane, tot[rb][j][r]);
-        __threadfence();
-        if (!cs.sync()) { set_status(p.status, FT_DEV_TIMEOUT); return; }
-        if (tid == 0) *flag = (atomicAdd(p.tick + mb, 1u) == (uint32_t)(np - 1)) ? 1u : 0u;
-        if (!cs.sync()) { set_status(p.status, FT_DEV_TIMEOUT); return; }
-        const bool last = *flag != 0;
-        if (last) {
-          __threadfence();
-#pragma unroll
-          for (int rb = 0; rb < RB; ++rb)
-#pragma unroll
-            for (int j = 0; j < NT; ++j)
-#pragma unroll
-              for (int r = 0; r < 4; ++r) tot[rb][j][r] = 0.0f;
-          for (int q = 0; q < np; ++q) {
-            const float* src = base + (size_t)q * pl.slotf;
-#pragma unroll
-            for (int rb = 0; rb < RB; ++rb)
-#pragma unroll
-              for (int j = 0; j < NT; ++j)
-#pragma unroll
-                for (int r = 0; r < 4; ++r)
-                  tot[rb][j][r] += __ldcg(src + (((warp * RB + rb) * NT + j) * 4 + r) * 32 + lane);
-          }
-          if (tid == 0) p.tick[mb] = 0u;
-          gemv_epilogue<NT, ROLE>(p, mb, nrb, tot);
-        }
-        // a later piece may reuse the flag word
-        if (!cs.sync()) { set_status(p.status, FT_DEV_TIMEOUT); return; }
-      } else {
-        gemv_epilogue<NT, ROLE>(p, mb, nrb, tot);
+    if (st.piece_end()) {
+      // ---- end of this CTA's piece of a set: hand the partial sums to the epilogue warp
+      if (k > 0 && !mbar_wait(red_empty, (k - 1) & 1)) {
+        set_status(p.status, FT_DEV_TIMEOUT);
+        return;
       }
 #pragma unroll
-      for (int rb = 0; rb < RB; ++rb)
+      for (int rt = 0; rt < RT; ++rt)
 #pragma unroll
         for (int j = 0; j < NT; ++j)
 #pragma unroll
-          for (int r = 0; r < 4; ++r) tot[rb][j][r] = 0.0f;
+          for (int r = 0; r < 4; ++r) {
+            red[(((warp * RT + rt) * NT + j) * 4 + r) * 32 + lane] = tot[rt][j][r];
+            tot[rt][j][r] = 0.0f;
+          }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(red_full);
+      ++k;
     }
   }
 }
 
 template <int NT, int ROLE>
 static cudaError_t launch_one(const GemvParams& p, cudaStream_t st, bool pdl) {
-  using C = GemvCfg<NT>;
-  static bool attr_done[64] = {false};
+  constexpr int THREADS = (GemvShape<NT>::NCW + 2) * 32;
+  static int attr_smem[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!attr_done[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(gemv_kernel<NT, ROLE>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (attr_smem[dev] < p.plan.smem) {
+    cudaError_t e =
+        cudaFuncSetAttribute(gemv_kernel<NT, ROLE>, cudaFuncAttributeMaxDynamicSharedMemorySize, p.plan.smem);
     if (e != cudaSuccess) return e;
-    attr_done[dev] = true;
+    attr_smem[dev] = p.plan.smem;
   }
-  return launch_ex(gemv_kernel<NT, ROLE>, dim3(p.plan.C), dim3(C::THREADS), (size_t)C::SMEM, st, pdl, p);
+  return launch_ex(gemv_kernel<NT, ROLE>, dim3(p.plan.C), dim3(THREADS), (size_t)p.plan.smem, st, pdl, p);
 }
 
 template <int ROLE>
@@ -390,33 +400,46 @@ cudaError_t launch_gemv(int role, const GemvParams& p, cudaStream_t st, bool pdl
   }
 }
 
-GemvPlan make_gemv_plan(int N, int K, int B, int sms) {
-  GemvPlan p;
+static void shape_of(int NT, int& RT, int& NCW) {
+  switch (NT) {
+    case 1: RT = GemvShape<1>::RT; NCW = GemvShape<1>::NCW; break;
+    case 2: RT = GemvShape<2>::RT; NCW = GemvShape<2>::NCW; break;
+    case 3: RT = GemvShape<3>::RT; NCW = GemvShape<3>::NCW; break;
+    default: RT = GemvShape<4>::RT; NCW = GemvShape<4>::NCW; break;
+  }
+}
+
+GemvPlan make_gemv_plan(int N, int K, int B, int sms, bool whole_sets, int smem_budget) {
+  GemvPlan p = {};
   p.N = N;
   p.K = K;
   p.NT = (B + 7) / 8;
-  p.RB = p.NT;
-  p.NRB = N / kRowBlock;
+  shape_of(p.NT, p.RT, p.NCW);
+  p.NTILE = N / kRowTile;
   p.NKG = K / kWGroup;
-  p.NMB = (p.NRB + p.RB - 1) / p.RB;
-  p.U = p.NMB * p.NKG;
-  p.C = sms < p.U ? sms : p.U;
+  p.NSET = (p.NTILE + p.RT - 1) / p.RT;
+  p.whole = whole_sets ? 1 : 0;
+  const int units = whole_sets ? p.NSET : p.NSET * p.NKG;
+  p.C = sms < units ? sms : units;
   if (p.C < 1) p.C = 1;
-  p.per = p.U / p.C;
-  p.rem = p.U % p.C;
-  const int mp = (p.NKG + p.per - 1) / p.per + 1;
-  p.maxp = mp < p.NKG ? mp : p.NKG;
-  p.slotf = 8 * p.RB * p.NT * 128;
+  p.per = units / p.C;
+  p.rem = units % p.C;
+  p.ng = p.NCW;  // one group per consumer warp per stage
+  if (p.ng > p.NKG) p.ng = p.NKG;
+  p.xstride = p.ng * kWGroup * 2 + 16;
+  const int wbytes = p.RT * p.ng * kSlabBytes;
+  p.xoff = (int)align_up((size_t)wbytes, 16);
+  p.soff = (int)align_up((size_t)p.xoff + (size_t)B * p.xstride, 16);
+  p.slot = (int)align_up((size_t)p.soff + (size_t)p.ng * 128, 128);
+  p.redoff = 256;
+  const int redbytes = p.NCW * p.RT * p.NT * 128 * 4;
+  p.slotoff = (int)align_up((size_t)p.redoff + (size_t)redbytes, 128);
+  int stages = (smem_budget - p.slotoff) / p.slot;
+  if (stages > 8) stages = 8;
+  if (stages < 2) stages = 2;
+  p.stages = stages;
+  p.smem = p.slotoff + stages * p.slot;
   return p;
-}
-
-size_t gemv_smem_bytes(int NT) {
-  switch (NT) {
-    case 1: return GemvCfg<1>::SMEM;
-    case 2: return GemvCfg<2>::SMEM;
-    case 3: return GemvCfg<3>::SMEM;
-    default: return GemvCfg<4>::SMEM;
-  }
 }
 
 }  // namespace ft

@@ -122,6 +122,21 @@ __device__ __forceinline__ void mma_f16_zc(float (&d)[4], const uint32_t (&a)[4]
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.0f));
 }
 
+// Thread-block cluster barrier (all threads of every CTA of the cluster);
+// release/acquire make shared-memory writes visible across the cluster.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Load a float from the shared memory of CTA `rank` of this cluster at the
+// offset of the local shared address `local`.
+__device__ __forceinline__ float ld_dsmem_f32(uint32_t local, uint32_t rank) {
+  uint32_t remote;
+  float v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(rank));
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
   uint32_t y;
   asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
@@ -150,36 +165,77 @@ __device__ __forceinline__ uint32_t hfma2(uint32_t a, uint32_t b, uint32_t c) {
   return r;
 }
 
-// Nibble decode.  The 4-bit code c sits in the mantissa of FP16 1024.0
-// (0x6400), whose mantissa step is 1, giving 1024 + c; subtracting 1032 yields
-// c - 8 exactly.  A nibble at bits 4..7 of a 16-bit half lands as 1024 + 16c,
-// which (v / 16) - 72 maps to c - 8 exactly.  From one 32-bit word with
-// nibbles n0..n7 (bits 4i..4i+3) this yields four f16x2 registers:
-//   r0 = (n0, n4) - 8,  r1 = (n1, n5) - 8,  r2 = (n2, n6) - 8,  r3 = (n3, n7) - 8
-// (low half first).
+// Nibble decode.  A 4-bit code c placed in the low mantissa bits of FP16
+// 1024.0 (0x6400, mantissa step 1) reads as 1024 + c; placed at bits 4..7 of
+// the half it reads as 1024 + 16 c.  Both are exact.  The offset (1024 + 8 for
+// the first kind, 1024 + 128 after dividing the activation by 16 for the
+// second) is not subtracted per weight: every k-step of 16 uses the first kind
+// for k = 0..7 and the second for k = 8..15, the activation operand holds
+// x (k < 8) and x / 16 (k >= 8), and each group's accumulation starts at -S
+// with S = 1032 * sum_{k<8} x + 1152 * sum_{k>=8} (x / 16) (kOffLo / kOffHi).
+// From one 32-bit word with nibbles n0..n7 (bits 4i..4i+3) four integer ops
+// and one shift give the four f16x2 registers
+//   r0 = (n0, n4),  r1 = 16 (n1, n5),  r2 = (n2, n6),  r3 = 16 (n3, n7)
+// (low half first, before the offsets).
 constexpr uint32_t kH1024 = 0x64006400u;   // (1024, 1024)
-constexpr uint32_t kH1032 = 0x64086408u;   // (1032, 1032)
-constexpr uint32_t kH1_16 = 0x2C002C00u;   // (1/16, 1/16)
-constexpr uint32_t kHm72 = 0xD480D480u;    // (-72, -72)
+constexpr float kOffLo = 1032.0f;          // 1024 + 8
+constexpr float kOffHi = 1152.0f;          // (1024 + 16 * 8) with x / 16: 1024 + 128
+constexpr uint32_t kHOffLo = 0x64086408u;  // (1032, 1032) in FP16
+constexpr uint32_t kHOffHi = 0x64806480u;  // (1152, 1152) in FP16
 
-__device__ __forceinline__ void dequant_word(uint32_t w, uint32_t (&r)[4]) {
+__device__ __forceinline__ void magic_word(uint32_t w, uint32_t (&r)[4]) {
   const uint32_t w8 = w >> 8;
-  r[0] = hsub2(lop3_or_and(w, 0x000F000Fu, kH1024), kH1032);
-  r[1] = hfma2(lop3_or_and(w, 0x00F000F0u, kH1024), kH1_16, kHm72);
-  r[2] = hsub2(lop3_or_and(w8, 0x000F000Fu, kH1024), kH1032);
-  r[3] = hfma2(lop3_or_and(w8, 0x00F000F0u, kH1024), kH1_16, kHm72);
+  r[0] = lop3_or_and(w, 0x000F000Fu, kH1024);
+  r[1] = lop3_or_and(w, 0x00F000F0u, kH1024);
+  r[2] = lop3_or_and(w8, 0x000F000Fu, kH1024);
+  r[3] = lop3_or_and(w8, 0x00F000F0u, kH1024);
+}
+
+// Four f16x2 registers (n_i of the low half, n_i of the high half) from a
+// register holding nibbles n0..n3 in each 16-bit half: at the unscaled
+// position (1024 + c) or at bits 4..7 (1024 + 16 c).
+__device__ __forceinline__ void magic_low4(uint32_t r, uint32_t (&o)[4]) {
+  o[0] = lop3_or_and(r, 0x000F000Fu, kH1024);
+  o[1] = lop3_or_and(r >> 4, 0x000F000Fu, kH1024);
+  o[2] = lop3_or_and(r >> 8, 0x000F000Fu, kH1024);
+  o[3] = lop3_or_and(r >> 12, 0x000F000Fu, kH1024);
+}
+__device__ __forceinline__ void magic_high4(uint32_t r, uint32_t (&o)[4]) {
+  o[0] = lop3_or_and(r << 4, 0x00F000F0u, kH1024);
+  o[1] = lop3_or_and(r, 0x00F000F0u, kH1024);
+  o[2] = lop3_or_and(r >> 4, 0x00F000F0u, kH1024);
+  o[3] = lop3_or_and(r >> 8, 0x00F000F0u, kH1024);
+}
+
+// Activation operand layout.  Within each chunk of 16 consecutive inputs the
+// FP16 values are stored in the order 0,1,8,9, 2,3,10,11, 4,5,12,13, 6,7,14,15
+// (so lane tig's four B-fragment values are one 8-byte load), and inputs
+// 8..15 of the chunk hold x / 16.  op_slot(k) is the storage index of input k.
+__host__ __device__ __forceinline__ int op_slot(int k) {
+  const int c = k & 15, base = k & ~15;
+  return base + ((c < 8) ? (4 * (c >> 1) + (c & 1)) : (4 * ((c - 8) >> 1) + 2 + (c & 1)));
+}
+__host__ __device__ __forceinline__ bool op_high(int k) { return (k & 15) >= 8; }
+// FP16 operand value of input k and its contribution to the group offset S.
+__device__ __forceinline__ __half op_encode(float x, int k, float& s_term) {
+  const __half h = __float2half_rn(op_high(k) ? x * 0.0625f : x);
+  s_term = (op_high(k) ? kOffHi : kOffLo) * __half2float(h);
+  return h;
 }
 
 // ------------------------------------------------------------------ packed weights
-// Nibble i of the word for (lane = 4g + tig, k-step ks) of a row tile holds
-// row  g + (i & 1 ? 8 : 0)  and column  16 ks + 2 tig + (i & 2 ? 8 : 0) + (i & 4 ? 1 : 0),
-// which dequant_word() turns into the m16n8k16 A-fragment {a0, a1, a2, a3}.
+// Row-tile-major: [row tile T][group kg] -> one 1056-byte slab: 1024 bytes of
+// nibbles (two 512-byte halves for k-steps 0-3 and 4-7, 16 bytes per lane)
+// followed by 8 x (bf16 s[g], bf16 s[g+8]).  Nibble i of the word for
+// (lane = 4g + tig, k-step ks) holds
+//   row  g + (i & 2 ? 8 : 0),  column  16 ks + 2 tig + (i & 1 ? 8 : 0) + (i & 4 ? 1 : 0)
+// so that magic_word() yields the m16n8k16 A fragment {r0, r2, r1, r3}.
 __host__ __device__ __forceinline__ int wslab_word_offset(int lane, int ks) {
   return (ks >> 2) * 512 + lane * 16 + (ks & 3) * 4;
 }
-__host__ __device__ __forceinline__ int wnib_row(int g, int i) { return g + ((i & 1) ? 8 : 0); }
+__host__ __device__ __forceinline__ int wnib_row(int g, int i) { return g + ((i & 2) ? 8 : 0); }
 __host__ __device__ __forceinline__ int wnib_col(int ks, int tig, int i) {
-  return 16 * ks + 2 * tig + ((i & 2) ? 8 : 0) + ((i & 4) ? 1 : 0);
+  return 16 * ks + 2 * tig + ((i & 1) ? 8 : 0) + ((i & 4) ? 1 : 0);
 }
 
 // Logical row of packed row r (0..15) of global row tile T for a role.

@@ -3,12 +3,12 @@
 // W' = gamma W before quantisation; "무엇과 다른가": INT4 values with group
 // scales, stored in the order the decode kernels consume them).
 //
-// Layout of a packed role with N_out rows and K_in inputs:
-//   [row block rb < N/128][group kg < K/128][row tile rt < 8] -> one 1056-byte slab
+// Layout of a packed role with N_out rows and K_in inputs (row-tile-major):
+//   [row tile T < N/16][group kg < K/128] -> one 1056-byte slab
 //   slab = 1024 bytes of nibbles (two 512-byte halves: k-steps 0-3 and 4-7,
 //          lane-major 16 bytes each) + 8 x (bf16 s[g], bf16 s[g+8]).
-// The GEMV streams a CTA's contiguous range of (row block, group) units with
-// bulk copies, so each copy is one contiguous run of slabs.
+// A row tile's whole input range is contiguous, so the GEMV streams any run
+// of (row tile, group) units with one bulk copy per row tile.
 #include "ft_internal.cuh"
 
 namespace ft {
@@ -41,8 +41,7 @@ __global__ void __launch_bounds__(256) pack_kernel(const float* __restrict__ W, 
     }
   }
   __syncthreads();
-  const int rb = T / kTilesPerBlock, rt = T % kTilesPerBlock;
-  uint8_t* slab = out + ((size_t)(rb * NKG + kg) * kTilesPerBlock + rt) * kSlabBytes;
+  uint8_t* slab = out + ((size_t)T * NKG + kg) * kSlabBytes;
   // pass 2: one 32-bit word of 8 nibbles per thread, in A-fragment order
   {
     const int ks = t >> 5, lane = t & 31, g = lane >> 2, tig = lane & 3;
@@ -64,8 +63,7 @@ __global__ void __launch_bounds__(256) unpack_kernel(const uint8_t* __restrict__
                                                      uint16_t* __restrict__ scales, int role, int inter, int K,
                                                      int NKG) {
   const int T = blockIdx.x, kg = blockIdx.y, t = threadIdx.x;
-  const int rb = T / kTilesPerBlock, rt = T % kTilesPerBlock;
-  const uint8_t* slab = in + ((size_t)(rb * NKG + kg) * kTilesPerBlock + rt) * kSlabBytes;
+  const uint8_t* slab = in + ((size_t)T * NKG + kg) * kSlabBytes;
   const int ks = t >> 5, lane = t & 31, g = lane >> 2, tig = lane & 3;
   const uint32_t w = *reinterpret_cast<const uint32_t*>(slab + wslab_word_offset(lane, ks));
 #pragma unroll

@@ -104,15 +104,28 @@ def run_gpu(pb: Problem, act_dtype=ft.FT_F32, cache: Optional[torch.Tensor] = No
     def view(off, n, dt):
         nbytes = n * torch.tensor([], dtype=dt).element_size()
         return ws[off:off + nbytes].view(dt).cpu().numpy()
-    qkv = view(lay.qkv, B * s.n_qkv, torch.float32).reshape(B, s.n_qkv)
-    o = view(lay.o, B * s.n_q * s.head_dim, torch.float16).astype(np.float32).reshape(B, -1)
+    rho1 = view(lay.rho1, B, torch.float32)
+    qkv = view(lay.qkv, B * s.n_qkv, torch.float32).reshape(B, s.n_qkv) * rho1[:, None]
+    o = operand_decode(view(lay.o, B * s.n_q * s.head_dim, torch.float16).reshape(B, -1))
     h1 = view(lay.h1, B * H, torch.float32).reshape(B, H)
-    a = view(lay.a, B * s.inter, torch.float16).astype(np.float32).reshape(B, -1)
+    a = operand_decode(view(lay.a, B * s.inter, torch.float16).reshape(B, -1))
     if act_dtype == ft.FT_F32:
         out = y.cpu().numpy()
     else:
         out = synth.bf16_bits_to_f32(y.cpu().numpy().view(np.uint16))
     return GpuResult(out, qkv, o, h1, a, int(st.item()), cache)
+
+
+def operand_decode(x16: np.ndarray) -> np.ndarray:
+    """Logical FP32 values of a vector stored in the projections' operand layout
+    (include/ft.h: within each 16 inputs the storage order is
+    0,1,8,9,2,3,10,11,4,5,12,13,6,7,14,15 and inputs 8..15 hold value / 16)."""
+    order = np.array([0, 1, 8, 9, 2, 3, 10, 11, 4, 5, 12, 13, 6, 7, 14, 15])
+    x = np.asarray(x16, np.float32).reshape(x16.shape[:-1] + (-1, 16))
+    out = np.empty_like(x)
+    out[..., order] = x
+    out[..., 8:] *= 16.0
+    return out.reshape(x16.shape)
 
 
 def oracle_cache(pb: Problem) -> KVCacheOracle:

@@ -152,7 +152,7 @@ def test_block_split_invariance(tiny):
     nb = ft.ft_decode_workspace_layout(tiny.cfg, 2, 3000).n_split
     assert na != nb
     assert H.rel_rms(ga.o, gb.o) < 2e-3
-    assert H.rel_rms(ga.out, gb.out) < 1e-5
+    assert H.rel_rms(ga.out, gb.out) < 1e-4
 
 
 def test_block_capacity_flag(tiny):
