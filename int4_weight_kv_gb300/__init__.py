@@ -67,6 +67,8 @@ _SIGS = {
                                        c_void_p, c_int, c_void_p, c_int, c_void_p, c_size_t, c_void_p, c_uint,
                                        c_void_p]),
     "ft_decode_workspace_layout": (c_int, [POINTER(BlockCfg), c_int, c_int, POINTER(WsLayout)]),
+    "ft_decode_block_static_ws": (c_int, [POINTER(BlockCfg), POINTER(LayerWeights), c_void_p, c_int, c_int,
+                                          c_void_p, c_void_p, c_int, c_void_p, c_int, c_void_p, c_void_p]),
     "ft_decode_block_launches": (c_int, []),
     "ft_set_pdl": (c_int, [c_int]),
 }
@@ -202,6 +204,15 @@ def ft_decode_block_stages(cfg, weights, cache, max_batch, max_ctx, x_in, x_out,
                                         _ptr(x_in), _ptr(x_out), act_dtype, _ptr(pos), B, _ptr(workspace),
                                         workspace.numel() * workspace.element_size(), _ptr(dev_status),
                                         stage_mask, _stream(stream))
+
+
+def ft_decode_block_static_ws(cfg, weights, cache, max_batch, max_ctx, x_in, x_out, act_dtype, pos, B,
+                              dev_status=None, stream=None) -> int:
+    """ft_decode_block with the library's fixed device scratch instead of a workspace."""
+    lw = _layer(weights)
+    return lib().ft_decode_block_static_ws(ctypes.byref(cfg), ctypes.byref(lw), _ptr(cache), max_batch, max_ctx,
+                                           _ptr(x_in), _ptr(x_out), act_dtype, _ptr(pos), B, _ptr(dev_status),
+                                           _stream(stream))
 
 
 def ft_decode_block_launches() -> int:
