@@ -232,7 +232,7 @@ def run_ours(args):
         dist.barrier(device_ids=[local])
     ms = e0.elapsed_time(e1)
     # keep the GPU under the same load long enough for the clock sampler
-    t_end = time.time() + max(0.0, 1.0 - ms / 1000.0)
+    t_end = time.time() + (0.0 if args.profile else max(0.0, 1.0 - ms / 1000.0))
     while time.time() < t_end:
         run_steps(R * 50)
         torch.cuda.synchronize()
@@ -249,7 +249,7 @@ def run_ours(args):
     dom_role = max(ab["per_role"], key=lambda r: ab["per_role"][r])
     stage = {ft.FT_W_QKV: ft.FT_STAGE_QKV, ft.FT_W_O: ft.FT_STAGE_O, ft.FT_W_GATEUP: ft.FT_STAGE_GU,
              ft.FT_W_DOWN: ft.FT_STAGE_DOWN}[dom_role]
-    n_dom = max(R * 20, min(args.steps, 2000))
+    n_dom = R if args.profile else max(R * 20, min(args.steps, 2000))
     for i in range(R):
         p = reps[i]
         ft.check(ft.ft_decode_block_stages(cfg, p["w"], p["cache"], B, max_ctx, p["x"], p["y"], ft.FT_BF16, pos, B,
@@ -273,7 +273,7 @@ def run_ours(args):
             traffic = json.load(f).get(args.workload)
 
     # end to end through the C ABI with host buffers (pinned), copies inside the timed region
-    n_e2e = min(args.steps, 500)
+    n_e2e = R if args.profile else min(args.steps, 500)
     x_host = torch.from_numpy(np.ascontiguousarray(xb).view(np.int16)).pin_memory()
     pos_host = torch.full((B,), ctx, dtype=torch.int32).pin_memory()
     y_host = torch.empty((B, s.hidden), dtype=torch.int16).pin_memory()
@@ -315,7 +315,9 @@ def run_ours(args):
         "clocks": clk,
     }
     if rank == 0:
-        line["cpu_baseline"] = cpu_baseline(wl)
+        line["cpu_baseline"] = None if args.profile else cpu_baseline(wl)
+        if args.profile:
+            line["note"] = "profiler run: timings are not bench values"
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier(device_ids=[local])
@@ -402,6 +404,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--profile", action="store_true",
+                    help="short run for a profiler: no clock hold, no oracle baseline; numbers are not bench values")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
