@@ -196,6 +196,25 @@ typedef struct {
 
 int ft_decode_workspace_layout(const ft_block_cfg *cfg, int B, int max_ctx, ft_ws_layout *out);
 
+/* ---- full decode step helpers (BF16, not INT4) ----------------------------
+ * A complete Llama-style decode step is: embedding gather, the decode block
+ * per layer (FT_F32 residual between layers), final RMSNorm, LM head (summary
+ * page, "전제와 한계": the full Llama-3.1-8B step at batch 1). */
+
+/* x_out[b, :] = table[tokens[b], :] widened to FP32.  table: BF16 bits [V, H];
+ * tokens: device int32 [B]; x_out: FP32 [B, H].  A token outside [0, V) gives a
+ * zero row and sets FT_DEV_RANGE. */
+int ft_embed_bf16(const uint16_t *table, const int32_t *tokens, float *x_out, int B, int V, int H,
+                  int32_t *dev_status, ft_stream stream);
+
+/* logits[b, v] = sum_k W[v, k] * z[b, k] with z = gamma * rho(x_b) * x_b,
+ * rho = (mean x^2 + eps)^-1/2.  x: FP32 [B, H]; gamma: FP32 [H]; W: BF16 bits
+ * [V, H] (16-byte aligned); logits: FP32 [B, V] (overwritten).  B <= 8,
+ * H a multiple of 128, B * H * 4 <= 160 KiB, else FT_ERR_UNSUPPORTED.
+ * z enters the tensor cores as a BF16 (hi, lo) pair. */
+int ft_lm_head_bf16(const float *x, const float *gamma, const uint16_t *W, float *logits, int B, int V, int H,
+                    float eps, ft_stream stream);
+
 /* ft_decode_block without a caller-provided workspace.  The FuTransformer paper
  * has no counterpart to this call; it exists for callers that cannot allocate
  * device memory when

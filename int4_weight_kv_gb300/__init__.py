@@ -69,6 +69,8 @@ _SIGS = {
     "ft_decode_workspace_layout": (c_int, [POINTER(BlockCfg), c_int, c_int, POINTER(WsLayout)]),
     "ft_decode_block_static_ws": (c_int, [POINTER(BlockCfg), POINTER(LayerWeights), c_void_p, c_int, c_int,
                                           c_void_p, c_void_p, c_int, c_void_p, c_int, c_void_p, c_void_p]),
+    "ft_embed_bf16": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_void_p, c_void_p]),
+    "ft_lm_head_bf16": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_float, c_void_p]),
     "ft_decode_block_launches": (c_int, []),
     "ft_set_pdl": (c_int, [c_int]),
 }
@@ -213,6 +215,14 @@ def ft_decode_block_static_ws(cfg, weights, cache, max_batch, max_ctx, x_in, x_o
     return lib().ft_decode_block_static_ws(ctypes.byref(cfg), ctypes.byref(lw), _ptr(cache), max_batch, max_ctx,
                                            _ptr(x_in), _ptr(x_out), act_dtype, _ptr(pos), B, _ptr(dev_status),
                                            _stream(stream))
+
+
+def ft_embed_bf16(table, tokens, x_out, B, V, H, dev_status=None, stream=None) -> int:
+    return lib().ft_embed_bf16(_ptr(table), _ptr(tokens), _ptr(x_out), B, V, H, _ptr(dev_status), _stream(stream))
+
+
+def ft_lm_head_bf16(x, gamma, W, logits, B, V, H, eps, stream=None) -> int:
+    return lib().ft_lm_head_bf16(_ptr(x), _ptr(gamma), _ptr(W), _ptr(logits), B, V, H, eps, _stream(stream))
 
 
 def ft_decode_block_launches() -> int:

@@ -6,8 +6,9 @@ from __future__ import annotations
 import numpy as np
 import torch
 
-from . import (FT_W_QKV, FT_W_O, FT_W_GATEUP, FT_W_DOWN, check, ft_decode_workspace_bytes, ft_kv_append_int4,
-               ft_kv_cache_bytes, ft_pack_weights_int4, ft_packed_weight_bytes)
+from . import (FT_F32, FT_W_QKV, FT_W_O, FT_W_GATEUP, FT_W_DOWN, check, ft_decode_block, ft_decode_workspace_bytes,
+               ft_embed_bf16, ft_kv_append_int4, ft_kv_cache_bytes, ft_lm_head_bf16, ft_pack_weights_int4,
+               ft_packed_weight_bytes)
 
 ROLE_KEYS = {FT_W_QKV: ("wqkv", "gamma_attn"), FT_W_O: ("wo", None), FT_W_GATEUP: ("wgu", "gamma_ffn"),
              FT_W_DOWN: ("wdown", None)}
@@ -58,3 +59,23 @@ def fill_history(cfg, cache, max_batch, max_ctx, k_bits: np.ndarray, v_bits: np.
         pos = torch.full((B,), t0, dtype=torch.int32, device=k.device)
         check(ft_kv_append_int4(cfg, cache, max_batch, max_ctx, k, v, pos, B, t1 - t0, status, stream),
               "ft_kv_append_int4")
+
+
+def model_step(cfg, layers, caches, max_batch, max_ctx, emb, lm, gamma_final, tokens, pos, bufs, workspaces,
+               status=None, stream=None, save_layer_inputs=None):
+    """One full decode step through the C ABI: embedding, every layer's decode
+    block with an FP32 residual, final RMSNorm + LM head.  ``bufs`` holds two
+    FP32 [B, H] device buffers and the FP32 [B, V] logits; ``save_layer_inputs``
+    (optional list) receives a copy of each layer's input."""
+    B = tokens.numel()
+    V, H = emb.shape
+    x, y = bufs["x"], bufs["y"]
+    check(ft_embed_bf16(emb, tokens, x, B, V, H, status, stream), "ft_embed_bf16")
+    for li, (w, c) in enumerate(zip(layers, caches)):
+        if save_layer_inputs is not None:
+            save_layer_inputs.append(x.clone())
+        check(ft_decode_block(cfg, w, c, max_batch, max_ctx, x, y, FT_F32, pos, B, workspaces[li % len(workspaces)],
+                              status, stream), "ft_decode_block")
+        x, y = y, x
+    check(ft_lm_head_bf16(x, gamma_final, lm, bufs["logits"], B, V, H, cfg.rms_eps, stream), "ft_lm_head_bf16")
+    return x

@@ -186,3 +186,28 @@ def test_block_8b_batch_sweep(l8b, B):
     rows = sorted({0, B // 2, B - 1})
     o = H.run_oracle(pb, rows=rows)
     H.assert_block_close(g, o, rows)
+
+
+# ---------------------------------------------------------------- full-size configurations
+def test_block_8b_b32_ctx4096(l8b):
+    """Llama-3-8B layer, batch 32, context 4096 (attention-dominated, split-KV);
+    the oracle runs on sampled requests (requests are independent)."""
+    pb = H.make_problem(l8b, 3, B=32, ctx=4096)
+    g = H.run_gpu(pb)
+    rows = [0, 13, 31]
+    o = H.run_oracle(pb, rows=rows)
+    H.assert_block_close(g, o, rows)
+
+
+@pytest.fixture(scope="module")
+def l70b():
+    return H.make_layer(synth.L70B, 4)
+
+
+@pytest.mark.parametrize("B,ctx,rows", [(1, 2048, [0]), (32, 2048, [0, 17, 31]), (1, 32768, [0])])
+def test_block_70b(l70b, B, ctx, rows):
+    """Llama-3-70B layer shape at batch 1 and 32 (context 2048) and batch 1 at context 32768."""
+    pb = H.make_problem(l70b, 4, B=B, ctx=ctx)
+    g = H.run_gpu(pb)
+    o = H.run_oracle(pb, rows=rows)
+    H.assert_block_close(g, o, rows)
