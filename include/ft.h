@@ -155,15 +155,32 @@ typedef struct {
   const void *qkv, *o, *gateup, *down; /* each from ft_pack_weights_int4 */
 } ft_layer_weights;
 
-/* Bytes of scratch one call needs (depends on the current device's SM count).
- * The workspace must be zero-filled once before its first use (cudaMemset);
- * every call that returns leaves its first 256 bytes (the grid-barrier
- * counters) zero again, so it can be reused by later calls of any shape. */
 size_t ft_decode_workspace_bytes(const ft_block_cfg *cfg, int B, int max_ctx);
 
 int ft_decode_block(const ft_block_cfg *cfg, const ft_layer_weights *w, void *cache, int max_batch,
                     int max_ctx, const void *x_in, void *x_out, int act_dtype, const int32_t *pos,
                     int B, void *workspace, size_t ws_bytes, int32_t *dev_status, ft_stream stream);
+
+/* Stage selection for ft_decode_block_stages (bit mask). */
+enum {
+  FT_STAGE_PREP = 1,  /* input -> FP16 operand, rho1, zero the counters      */
+  FT_STAGE_QKV = 2,   /* QKV projection (x rho1)                             */
+  FT_STAGE_ATTN = 4,  /* RoPE, rotation, cache write, split-KV attention     */
+  FT_STAGE_O = 8,     /* O projection + residual                              */
+  FT_STAGE_MID = 16,  /* h1 -> gate/up operand, rho2, down accumulator        */
+  FT_STAGE_GU = 32,   /* gate/up projection + SwiGLU                          */
+  FT_STAGE_DOWN = 64, /* down projection + residual -> x_out                  */
+  FT_STAGE_ALL = 127
+};
+
+/* Runs a subset of the block's stages on a workspace left by a previous full
+ * call with the same arguments (each stage reads what the earlier stages
+ * wrote there).  Used to time one stage alone; FT_STAGE_ALL equals
+ * ft_decode_block. */
+int ft_decode_block_stages(const ft_block_cfg *cfg, const ft_layer_weights *w, void *cache,
+                           int max_batch, int max_ctx, const void *x_in, void *x_out, int act_dtype,
+                           const int32_t *pos, int B, void *workspace, size_t ws_bytes,
+                           int32_t *dev_status, unsigned stage_mask, ft_stream stream);
 
 /* Byte offsets of intermediate tensors inside the workspace (host struct out),
  * for tests:  qkv FP32 [B, (n_q+2n_kv) d] (the projection before rho1 and
@@ -174,7 +191,7 @@ int ft_decode_block(const ft_block_cfg *cfg, const ft_layer_weights *w, void *ca
  * inputs 8..15 hold value / 16. */
 typedef struct {
   size_t qkv, rho1, o, h1, a;
-  int32_t n_split; /* CTAs sharing the attention tiles (split-KV pieces are per CTA) */
+  int32_t n_split; /* split-KV chunks per (request, KV head) */
 } ft_ws_layout;
 
 int ft_decode_workspace_layout(const ft_block_cfg *cfg, int B, int max_ctx, ft_ws_layout *out);
@@ -204,13 +221,12 @@ int ft_lm_head_bf16(const float *x, const float *gamma, const uint16_t *W, float
  * they run a step (a pool or allocation policy that forbids new device
  * allocations after start-up, a host that hands over only input and output
  * buffers, or a loop that must not pay for an allocation).  The scratch space
- * is a fixed 16 MiB device array inside this library, held by every GPU that
+ * is a fixed 8 MiB device array inside this library, held by every GPU that
  * loads it until the process exits; problems needing more (see
  * ft_decode_workspace_bytes) return FT_ERR_WORKSPACE and enqueue nothing.  No
  * memory is allocated by this call.  The array is shared by all calls on a
- * device and keeps the previous call's contents (it starts zero-filled, and
- * the block clears what it needs itself); calls that overlap on the GPU race
- * on it.  The first call on
+ * device and keeps the previous call's contents (the block clears what it
+ * needs itself); calls that overlap on the GPU race on it.  The first call on
  * each device looks up the array's address (cudaGetSymbolAddress) with that
  * device current; make that first call before any stream capture.  Arguments
  * and results are otherwise those of ft_decode_block. */
@@ -218,9 +234,12 @@ int ft_decode_block_static_ws(const ft_block_cfg *cfg, const ft_layer_weights *w
                               int max_ctx, const void *x_in, void *x_out, int act_dtype, const int32_t *pos, int B,
                               int32_t *dev_status, ft_stream stream);
 
-/* Number of kernels one ft_decode_block call launches (one persistent,
- * cooperatively launched kernel with one CTA per SM). */
+/* Number of kernels one ft_decode_block call launches. */
 int ft_decode_block_launches(void);
+
+/* Programmatic dependent launch between the block's kernels (default on).
+ * Returns the previous setting. */
+int ft_set_pdl(int enabled);
 
 #ifdef __cplusplus
 }

@@ -10,7 +10,7 @@ from __future__ import annotations
 
 import ctypes
 import os
-from ctypes import c_int, c_int32, c_size_t, c_void_p, c_float, c_char_p, POINTER
+from ctypes import c_int, c_int32, c_size_t, c_uint, c_void_p, c_float, c_char_p, POINTER
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libft.so")
@@ -19,6 +19,8 @@ FT_OK, FT_ERR_INVALID_ARG, FT_ERR_UNSUPPORTED, FT_ERR_WORKSPACE, FT_ERR_CAPACITY
 FT_DEV_CAPACITY, FT_DEV_TIMEOUT, FT_DEV_RANGE = 1, 2, 4
 FT_BF16, FT_F32 = 0, 1
 FT_W_QKV, FT_W_O, FT_W_GATEUP, FT_W_DOWN = 0, 1, 2, 3
+FT_STAGE_PREP, FT_STAGE_QKV, FT_STAGE_ATTN, FT_STAGE_O = 1, 2, 4, 8
+FT_STAGE_MID, FT_STAGE_GU, FT_STAGE_DOWN, FT_STAGE_ALL = 16, 32, 64, 127
 ROLES = (FT_W_QKV, FT_W_O, FT_W_GATEUP, FT_W_DOWN)
 
 
@@ -61,12 +63,16 @@ _SIGS = {
     "ft_decode_workspace_bytes": (c_size_t, [POINTER(BlockCfg), c_int, c_int]),
     "ft_decode_block": (c_int, [POINTER(BlockCfg), POINTER(LayerWeights), c_void_p, c_int, c_int, c_void_p,
                                 c_void_p, c_int, c_void_p, c_int, c_void_p, c_size_t, c_void_p, c_void_p]),
+    "ft_decode_block_stages": (c_int, [POINTER(BlockCfg), POINTER(LayerWeights), c_void_p, c_int, c_int, c_void_p,
+                                       c_void_p, c_int, c_void_p, c_int, c_void_p, c_size_t, c_void_p, c_uint,
+                                       c_void_p]),
     "ft_decode_workspace_layout": (c_int, [POINTER(BlockCfg), c_int, c_int, POINTER(WsLayout)]),
     "ft_decode_block_static_ws": (c_int, [POINTER(BlockCfg), POINTER(LayerWeights), c_void_p, c_int, c_int,
                                           c_void_p, c_void_p, c_int, c_void_p, c_int, c_void_p, c_void_p]),
     "ft_embed_bf16": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_void_p, c_void_p]),
     "ft_lm_head_bf16": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_float, c_void_p]),
     "ft_decode_block_launches": (c_int, []),
+    "ft_set_pdl": (c_int, [c_int]),
 }
 
 
@@ -193,6 +199,15 @@ def ft_decode_block(cfg, weights, cache, max_batch, max_ctx, x_in, x_out, act_dt
                                  workspace.numel() * workspace.element_size(), _ptr(dev_status), _stream(stream))
 
 
+def ft_decode_block_stages(cfg, weights, cache, max_batch, max_ctx, x_in, x_out, act_dtype, pos, B, workspace,
+                           stage_mask, dev_status=None, stream=None) -> int:
+    lw = _layer(weights)
+    return lib().ft_decode_block_stages(ctypes.byref(cfg), ctypes.byref(lw), _ptr(cache), max_batch, max_ctx,
+                                        _ptr(x_in), _ptr(x_out), act_dtype, _ptr(pos), B, _ptr(workspace),
+                                        workspace.numel() * workspace.element_size(), _ptr(dev_status),
+                                        stage_mask, _stream(stream))
+
+
 def ft_decode_block_static_ws(cfg, weights, cache, max_batch, max_ctx, x_in, x_out, act_dtype, pos, B,
                               dev_status=None, stream=None) -> int:
     """ft_decode_block with the library's fixed device scratch instead of a workspace."""
@@ -213,3 +228,6 @@ def ft_lm_head_bf16(x, gamma, W, logits, B, V, H, eps, stream=None) -> int:
 def ft_decode_block_launches() -> int:
     return lib().ft_decode_block_launches()
 
+
+def ft_set_pdl(enabled: bool) -> bool:
+    return bool(lib().ft_set_pdl(1 if enabled else 0))

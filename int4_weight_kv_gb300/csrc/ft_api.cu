@@ -1,11 +1,13 @@
 // Host-side common entry points: status strings, configuration checks,
-// weight shapes and device properties.
+// weight shapes, device properties and the programmatic-dependent-launch switch.
+#include <atomic>
 #include <mutex>
 
 #include "ft_internal.cuh"
 
 namespace ft_host {
 
+static std::atomic<int> g_pdl{1};
 static std::mutex g_sm_mu;
 static int g_sm_count[64] = {0};
 
@@ -24,6 +26,8 @@ int num_sms() {
   }
   return n;
 }
+
+bool pdl_enabled() { return g_pdl.load() != 0; }
 
 static bool pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
 
@@ -81,5 +85,7 @@ size_t ft_packed_weight_bytes(const ft_block_cfg* c, int role) {
   if (ft_weight_shape(c, role, &n, &k) != FT_OK) return 0;
   return (size_t)(n / ft::kRowTile) * (size_t)(k / ft::kWGroup) * ft::kSlabBytes;
 }
+
+int ft_set_pdl(int enabled) { return ft_host::g_pdl.exchange(enabled ? 1 : 0); }
 
 }  // extern "C"

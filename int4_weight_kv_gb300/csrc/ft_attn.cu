@@ -1,0 +1,390 @@
+// Decode attention over the Hadamard-rotated INT4 KV cache, with RoPE, the
+// rotation of q, the new token's cache write, split-KV and the inverse rotation
+// of the output (summary page, "무엇과 다른가": rotation of K/V, q and the
+// output, split-KV reduction for long contexts; "전제와 한계": the 8-head INT4
+// cache is read directly by the query heads, no head expansion).
+//
+// One CTA (4 warps) per (request b, KV head h, split): the G = n_q / n_kv query
+// heads of the group share every K/V byte the CTA reads.  Per 16-position tile
+// a warp computes
+//   S[pos][head]  = K^(16 x d) . q~ (d x 8 heads)       (A = K codes, FP16 exact)
+//   online softmax in FP32 (exp2 domain, log2(e)/sqrt(d) folded into q~)
+//   O[ch][head] += V^T(d x 16) . (P * s_v)(16 x 8)      (A = V codes, B = P via
+//                                                        movmatrix transpose)
+// The K entry's nibbles are stored so that a 16-byte load per thread is the
+// A fragment of two k-steps; the V entry's nibbles so that two positions' bytes
+// combine (prmt) into A fragments of V^T.  Per-position scales multiply the
+// scores (K) and the probabilities (V).  The n_split CTAs of one (b, h) form a
+// thread-block cluster: each keeps its (max, sum, acc) partial in shared
+// memory, a cluster barrier publishes them, and CTA r merges heads r, r+n_split,
+// ... by reading its peers' partials through distributed shared memory, adds
+// the new token (quantised and written to the cache at L_b by CTA 0, decoded
+// identically by every CTA), undoes the rotation and writes o.
+#include "ft_block.cuh"
+
+namespace ft {
+
+template <int D>
+struct TileRegs {
+  uint32_t k[2][D / 32];  // K words of positions g and g+8 (chunk tig)
+  uint32_t v[4][D / 64];  // V words of positions 2tig, 2tig+1, 2tig+8, 2tig+9 (chunk g)
+  uint16_t ks[2], vs[2];  // K / V scales of positions g and g+8
+};
+
+template <int D>
+__device__ __forceinline__ void load_tile(TileRegs<D>& r, const uint8_t* cache, const KVLayout& L, int b, int h, int p,
+                                          int g, int tig) {
+  const int last = L.max_ctx - 1;
+  const int pk0 = min(p + g, last), pk1 = min(p + g + 8, last);
+  const uint8_t* kb = cache + L.kc;
+  const uint8_t* vb = cache + L.vc;
+  const uint16_t* ksb = reinterpret_cast<const uint16_t*>(cache + L.ks);
+  const uint16_t* vsb = reinterpret_cast<const uint16_t*>(cache + L.vs);
+  const size_t r0 = L.row(b, h, pk0), r1 = L.row(b, h, pk1);
+  if constexpr (D == 128) {
+    const uint4 a = ld_stream_v4(kb + r0 * L.entry + tig * 16);
+    const uint4 c = ld_stream_v4(kb + r1 * L.entry + tig * 16);
+    r.k[0][0] = a.x; r.k[0][1] = a.y; r.k[0][2] = a.z; r.k[0][3] = a.w;
+    r.k[1][0] = c.x; r.k[1][1] = c.y; r.k[1][2] = c.z; r.k[1][3] = c.w;
+  } else {
+    const uint2 a = ld_stream_v2(kb + r0 * L.entry + tig * 8);
+    const uint2 c = ld_stream_v2(kb + r1 * L.entry + tig * 8);
+    r.k[0][0] = a.x; r.k[0][1] = a.y;
+    r.k[1][0] = c.x; r.k[1][1] = c.y;
+  }
+  const int pv[4] = {p + 2 * tig, p + 2 * tig + 1, p + 2 * tig + 8, p + 2 * tig + 9};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const size_t rv = L.row(b, h, min(pv[q], last));
+    if constexpr (D == 128) {
+      const uint2 a = ld_stream_v2(vb + rv * L.entry + g * 8);
+      r.v[q][0] = a.x;
+      r.v[q][1] = a.y;
+    } else {
+      r.v[q][0] = ld_stream_u32(vb + rv * L.entry + g * 4);
+    }
+  }
+  r.ks[0] = ld_stream_u16(ksb + r0);
+  r.ks[1] = ld_stream_u16(ksb + r1);
+  r.vs[0] = ld_stream_u16(vsb + r0);
+  r.vs[1] = ld_stream_u16(vsb + r1);
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// RoPE at position pos on a d-vector held stride-32 (lane owns l + 32 m);
+// angles pos * inv_freq[i] are formed and reduced modulo 2 pi in FP64.
+template <int NPL>
+__device__ __forceinline__ void warp_rope(float (&v)[NPL], int pos, const double* inv_freq) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int m = 0; m < NPL / 2; ++m) {
+    const int i = lane + 32 * m;
+    const double ang = (double)pos * inv_freq[i];
+    const double r = fma(-6.283185307179586476925, rint(ang * 0.15915494309189533577), ang);
+    float sn, cs;
+    sincosf((float)r, &sn, &cs);
+    const float x1 = v[m], x2 = v[m + NPL / 2];
+    v[m] = x1 * cs - x2 * sn;
+    v[m + NPL / 2] = x2 * cs + x1 * sn;
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(128) attn_kernel(const AttnParams p) {
+  constexpr int NPL = D / 32;
+  constexpr int KT = D / 16;  // k-tiles of q.K == m-tiles of P.V
+  constexpr int PARTF = 16 + 8 * D;
+  __shared__ float qt[8][D];            // rotated, scaled query (FP16 values)
+  __shared__ float qoff[8];             // its operand offsets (magic-number decode)
+  __shared__ float mrg[4][PARTF];       // per-warp partials for the CTA merge
+  __shared__ float knew[D], vnew[D];
+  __shared__ float cpart[16 + 8 * D];    // this CTA's merged partial, read by the cluster
+  __shared__ uint8_t stage[2][D];
+  __shared__ __align__(16) uint8_t stage_out[2][D / 2];
+  __shared__ uint16_t stage_sc[2];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, tig = lane & 3;
+  const int split = blockIdx.x % p.nsplit;
+  const int bh = blockIdx.x / p.nsplit;
+  const int h = bh % p.nkv, b = bh / p.nkv;
+  const int G = p.G;
+  const int Lb = p.pos[b];
+  if (Lb < 0 || Lb >= p.L.max_ctx) {
+    // every CTA of this cluster serves the same request, so all leave here together
+    if (tid == 0 && split == 0 && h == 0) set_status(p.status, FT_DEV_CAPACITY);
+    griddep_launch();
+    return;
+  }
+  const int ntiles = (Lb + 15) / 16;
+  const int tps = (ntiles + p.nsplit - 1) / p.nsplit;
+  const int t0 = split * tps, t1 = min(t0 + tps, ntiles);
+  const int p1 = min(16 * t1, Lb);
+
+  // history K/V do not depend on earlier kernels: start streaming now
+  TileRegs<D> cur;
+  int ti = t0 + warp;
+  if (ti < t1) load_tile<D>(cur, p.cache, p.L, b, h, 16 * ti, g, tig);
+
+  griddep_wait();
+
+  // ---- rotated query of the G heads: rho1, RoPE, Hadamard, softmax scale
+  const float rho1 = p.rho1[b];
+  for (int hh = warp; hh < G; hh += 4) {
+    float v[NPL];
+    const float* src = p.qkv + (size_t)b * p.Nqkv + (size_t)(h * G + hh) * D;
+#pragma unroll
+    for (int m = 0; m < NPL; ++m) v[m] = __ldcg(src + lane + 32 * m) * rho1;
+    warp_rope<NPL>(v, Lb, p.inv_freq);
+    warp_fwht<NPL>(v, p.hb);
+    // q~ as the FP16 B operand (channels c % 16 >= 8 hold q / 16) and its offset
+    float sq = 0.0f;
+#pragma unroll
+    for (int m = 0; m < NPL; ++m) {
+      const int c = lane + 32 * m;
+      const float q = __half2float(__float2half_rn(v[m] * p.qscale));
+      qt[hh][c] = q;
+      float st;
+      (void)op_encode(q, c, st);
+      sq += st;
+    }
+    sq = warp_sum(sq);
+    if (lane == 0) qoff[hh] = sq;
+  }
+  __syncthreads();
+  uint32_t bq[KT][2];
+#pragma unroll
+  for (int kt = 0; kt < KT; ++kt) {
+    if (g < G) {
+      const int c = 16 * kt + 2 * tig;
+      bq[kt][0] = pack_half2(qt[g][c], qt[g][c + 1]);
+      bq[kt][1] = pack_half2(qt[g][c + 8] * 0.0625f, qt[g][c + 9] * 0.0625f);
+    } else {
+      bq[kt][0] = bq[kt][1] = 0u;
+    }
+  }
+  const float qo0 = (2 * tig < G) ? qoff[2 * tig] : 0.0f;
+  const float qo1 = (2 * tig + 1 < G) ? qoff[2 * tig + 1] : 0.0f;
+
+  float acc[KT][4];
+#pragma unroll
+  for (int mt = 0; mt < KT; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.0f;
+  // offset accumulator: the same P.V product with every V code replaced by its
+  // decode offset (rows of constant 1032 / 1152), rescaled like acc
+  float kacc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  const uint32_t kappa[4] = {kHOffLo, kHOffLo, kHOffHi, kHOffHi};
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
+
+  for (; ti < t1; ti += 4) {
+    TileRegs<D> nxt;
+    const bool more = ti + 4 < t1;
+    if (more) load_tile<D>(nxt, p.cache, p.L, b, h, 16 * (ti + 4), g, tig);
+    const int p0 = 16 * ti;
+    // S = K . q~   (rows: positions g, g+8; columns: heads 2tig, 2tig+1)
+    float sacc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+    for (int j = 0; j < D / 32; ++j) {
+      uint32_t dg[4], dg8[4];
+      magic_word(cur.k[0][j], dg);
+      magic_word(cur.k[1][j], dg8);
+      const uint32_t a0[4] = {dg[0], dg8[0], dg[1], dg8[1]};
+      const uint32_t a1[4] = {dg[2], dg8[2], dg[3], dg8[3]};
+      mma_f16(sacc, a0, bq[2 * j][0], bq[2 * j][1]);
+      mma_f16(sacc, a1, bq[2 * j + 1][0], bq[2 * j + 1][1]);
+    }
+    const bool va = (p0 + g) < p1, vb = (p0 + g + 8) < p1;
+    const float ks0 = bf16_bits_to_f32(cur.ks[0]), ks1 = bf16_bits_to_f32(cur.ks[1]);
+    const float s0 = va ? (sacc[0] - qo0) * ks0 : -INFINITY;
+    const float s1 = va ? (sacc[1] - qo1) * ks0 : -INFINITY;
+    const float s2 = vb ? (sacc[2] - qo0) * ks1 : -INFINITY;
+    const float s3 = vb ? (sacc[3] - qo1) * ks1 : -INFINITY;
+    float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+    }
+    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+    const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
+    m0 = mn0;
+    m1 = mn1;
+    const float e0 = exp2f(s0 - mn0), e1 = exp2f(s1 - mn1), e2 = exp2f(s2 - mn0), e3 = exp2f(s3 - mn1);
+    l0 = l0 * al0 + e0 + e2;
+    l1 = l1 * al1 + e1 + e3;
+#pragma unroll
+    for (int mt = 0; mt < KT; ++mt) {
+      acc[mt][0] *= al0;
+      acc[mt][1] *= al1;
+      acc[mt][2] *= al0;
+      acc[mt][3] *= al1;
+    }
+    kacc[0] *= al0;
+    kacc[1] *= al1;
+    kacc[2] *= al0;
+    kacc[3] *= al1;
+    const float vs0 = va ? bf16_bits_to_f32(cur.vs[0]) : 0.0f;
+    const float vs1 = vb ? bf16_bits_to_f32(cur.vs[1]) * 0.0625f : 0.0f;  // positions 8..15: operand / 16
+    const uint32_t P0 = pack_half2(e0 * vs0, e1 * vs0);  // position g,   heads 2tig, 2tig+1
+    const uint32_t P1 = pack_half2(e2 * vs1, e3 * vs1);  // position g+8
+    const uint32_t pb0 = movmatrix_trans(P0);            // positions 2tig, 2tig+1 of head g
+    const uint32_t pb1 = movmatrix_trans(P1);            // positions 2tig+8, 2tig+9
+    // O += V^T . P  (positions 2tig, 2tig+1 decode at 1024 + c, positions +8 at 1024 + 16 c)
+#pragma unroll
+    for (int j = 0; j < D / 64; ++j) {
+      uint32_t lo01[4], hi01[4], lo23[4], hi23[4];
+      magic_low4(prmt(cur.v[0][j], cur.v[1][j], 0x5410u), lo01);
+      magic_low4(prmt(cur.v[0][j], cur.v[1][j], 0x7632u), hi01);
+      magic_high4(prmt(cur.v[2][j], cur.v[3][j], 0x5410u), lo23);
+      magic_high4(prmt(cur.v[2][j], cur.v[3][j], 0x7632u), hi23);
+      const uint32_t A0[4] = {lo01[0], lo01[1], lo23[0], lo23[1]};
+      const uint32_t A1[4] = {lo01[2], lo01[3], lo23[2], lo23[3]};
+      const uint32_t A2[4] = {hi01[0], hi01[1], hi23[0], hi23[1]};
+      const uint32_t A3[4] = {hi01[2], hi01[3], hi23[2], hi23[3]};
+      mma_f16(acc[4 * j + 0], A0, pb0, pb1);
+      mma_f16(acc[4 * j + 1], A1, pb0, pb1);
+      mma_f16(acc[4 * j + 2], A2, pb0, pb1);
+      mma_f16(acc[4 * j + 3], A3, pb0, pb1);
+    }
+    mma_f16(kacc, kappa, pb0, pb1);
+    if (more) cur = nxt;
+  }
+  griddep_launch();
+
+  // remove the decode offsets (every row of kacc carries the same value)
+#pragma unroll
+  for (int mt = 0; mt < KT; ++mt) {
+    acc[mt][0] -= kacc[0];
+    acc[mt][1] -= kacc[1];
+    acc[mt][2] -= kacc[0];
+    acc[mt][3] -= kacc[1];
+  }
+
+  // ---- merge the 4 warps of the CTA into this CTA's partial (kept in smem)
+#pragma unroll
+  for (int o = 4; o < 32; o <<= 1) {
+    l0 += __shfl_xor_sync(0xffffffffu, l0, o);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+  }
+  float* mw = mrg[warp];
+  if (g == 0) {
+    mw[2 * tig] = m0;
+    mw[2 * tig + 1] = m1;
+    mw[8 + 2 * tig] = l0;
+    mw[8 + 2 * tig + 1] = l1;
+  }
+#pragma unroll
+  for (int mt = 0; mt < KT; ++mt) {
+    const int c0 = 16 * mt + g, c1 = c0 + 8;
+    mw[16 + (2 * tig) * D + c0] = acc[mt][0];
+    mw[16 + (2 * tig + 1) * D + c0] = acc[mt][1];
+    mw[16 + (2 * tig) * D + c1] = acc[mt][2];
+    mw[16 + (2 * tig + 1) * D + c1] = acc[mt][3];
+  }
+  __syncthreads();
+  for (int i = tid; i < 8 * D + 16; i += 128) {
+    const int hh = (i < 16) ? (i & 7) : (i - 16) / D;
+    float M = -INFINITY;
+    for (int w = 0; w < 4; ++w) M = fmaxf(M, mrg[w][hh]);
+    float v;
+    if (i < 8) {
+      v = M;
+    } else {
+      v = 0.0f;
+      if (M != -INFINITY)
+        for (int w = 0; w < 4; ++w) {
+          const float mw2 = mrg[w][hh];
+          if (mw2 != -INFINITY) v += mrg[w][i] * exp2f(mw2 - M);
+        }
+    }
+    cpart[i] = v;
+  }
+
+  // ---- the new token: RoPE on k, rotation, INT4 (cache write by split 0), decode
+  if (warp < 2) {
+    float v[NPL];
+    const int off = (warp == 0) ? (p.nq + h) * D : (p.nq + p.nkv + h) * D;
+    const float* src = p.qkv + (size_t)b * p.Nqkv + off;
+#pragma unroll
+    for (int m = 0; m < NPL; ++m) v[m] = __ldcg(src + lane + 32 * m) * rho1;
+    if (warp == 0) warp_rope<NPL>(v, Lb, p.inv_freq);
+    warp_fwht<NPL>(v, p.hb);
+    const size_t row = p.L.row(b, h, Lb);
+    uint8_t* entry = (split == 0) ? p.cache + (warp == 0 ? p.L.kc : p.L.vc) + row * p.L.entry : stage_out[warp];
+    uint16_t* sc = (split == 0) ? reinterpret_cast<uint16_t*>(p.cache + (warp == 0 ? p.L.ks : p.L.vs)) + row
+                                : &stage_sc[warp];
+    warp_quant_store<NPL>(v, warp == 0, stage[warp], entry, sc);
+    float* dst = (warp == 0) ? knew : vnew;
+#pragma unroll
+    for (int m = 0; m < NPL; ++m) dst[lane + 32 * m] = v[m];
+  }
+  __syncthreads();
+  cluster_sync();  // every CTA's partial is now visible to the cluster
+
+  // ---- CTA r merges heads r, r + n_split, ...: peers' partials via DSMEM
+  const uint32_t cp_local = smem_u32(cpart);
+  for (int hh = split + p.nsplit * warp; hh < G; hh += p.nsplit * 4) {
+    float sn = 0.0f;
+#pragma unroll
+    for (int m = 0; m < NPL; ++m) sn += qt[hh][lane + 32 * m] * knew[lane + 32 * m];
+    sn = warp_sum(sn);
+    float M = sn;
+    for (int r = 0; r < p.nsplit; ++r) M = fmaxf(M, ld_dsmem_f32(cp_local + 4 * hh, r));
+    const float wn = exp2f(sn - M);
+    float lsum = wn;
+    float o[NPL];
+#pragma unroll
+    for (int m = 0; m < NPL; ++m) o[m] = wn * vnew[lane + 32 * m];
+    for (int r = 0; r < p.nsplit; ++r) {
+      const float ms = ld_dsmem_f32(cp_local + 4 * hh, r);
+      if (ms == -INFINITY) continue;
+      const float w = exp2f(ms - M);
+      lsum += w * ld_dsmem_f32(cp_local + 4 * (8 + hh), r);
+#pragma unroll
+      for (int m = 0; m < NPL; ++m) o[m] += w * ld_dsmem_f32(cp_local + 4 * (16 + hh * D + lane + 32 * m), r);
+    }
+    const float inv = 1.0f / lsum;
+#pragma unroll
+    for (int m = 0; m < NPL; ++m) o[m] *= inv;
+    warp_fwht<NPL>(o, p.hb);
+    const int kbase = (h * G + hh) * D;  // input index of channel 0 of this head in the O projection
+    __half* dst = p.o_h + (size_t)b * p.nq * D;
+    bool bad = false;
+    float so = 0.0f;
+#pragma unroll
+    for (int m = 0; m < NPL; ++m) {
+      const int k = kbase + lane + 32 * m;
+      bad |= !(fabsf(o[m]) <= 65504.0f);
+      float st;
+      dst[op_slot(k)] = op_encode(o[m], k, st);
+      so += st;
+    }
+    so = warp_sum(so);  // a head (d <= 128 channels) lies inside one 128-input group
+    if (lane == 0) atomicAdd(p.s_o + (kbase / kWGroup) * 32 + b, so);
+    if (bad) set_status(p.status, FT_DEV_RANGE);
+  }
+  cluster_sync();  // keep this CTA's shared memory alive until every peer has read it
+}
+
+cudaError_t launch_attn(const AttnParams& p, int head_dim, cudaStream_t st, bool pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(p.B * p.nkv * p.nsplit));
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)p.nsplit;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 2 : 1;
+  if (head_dim == 128) return cudaLaunchKernelEx(&cfg, attn_kernel<128>, p);
+  return cudaLaunchKernelEx(&cfg, attn_kernel<64>, p);
+}
+
+}  // namespace ft

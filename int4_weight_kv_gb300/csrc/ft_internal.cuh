@@ -9,8 +9,6 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
-#include <cmath>
-
 #include "ft.h"
 
 namespace ft {
@@ -70,38 +68,6 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 255u) == 0 && globaltimer() - t0 > kWaitLimitNs) return false;
   }
-}
-
-// Non-blocking test of an mbarrier phase.
-__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
-  uint32_t done;
-  asm volatile(
-      "{ .reg .pred p; mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
-      : "=r"(done)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return done != 0;
-}
-
-// Barrier over a subset of the CTA's warps (id 1..15, count a multiple of 32).
-__device__ __forceinline__ void named_bar(int id, int count) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ uint32_t ld_volatile_u32(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.volatile.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-// Orders this thread's earlier (acquired) view of global memory before its
-// later bulk async copies, which read through the async proxy.
-__device__ __forceinline__ void fence_proxy_async_global() {
-  asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 // 1-D bulk copy global -> shared, completion signalled on an mbarrier.
@@ -290,15 +256,12 @@ __host__ __device__ __forceinline__ int kv_v_channel(int g, int j, int i) {
   return 16 * (4 * j + (i >> 1)) + g + ((i & 1) ? 8 : 0);
 }
 
-// Rows of one (request, head) are `pitch` = max_ctx rounded up to 16
-// positions apart, so that any run of whole 16-position tiles below max_ctx
-// is one contiguous, 16-byte aligned block in each of the four regions.
 struct KVLayout {
-  int d, nkv, max_batch, max_ctx, pitch;
+  int d, nkv, max_batch, max_ctx;
   size_t entry;        // d/2 bytes of one K (or V) entry
   size_t kc, vc, ks, vs, total;
   __host__ __device__ size_t row(int b, int h, int p) const {
-    return ((size_t)(b * nkv + h) * (size_t)pitch + (size_t)p);
+    return ((size_t)(b * nkv + h) * (size_t)max_ctx + (size_t)p);
   }
 };
 
@@ -310,9 +273,8 @@ inline KVLayout kv_layout(const ft_block_cfg& c, int max_batch, int max_ctx) {
   L.nkv = c.n_kv;
   L.max_batch = max_batch;
   L.max_ctx = max_ctx;
-  L.pitch = (int)align_up((size_t)max_ctx, 16);
   L.entry = (size_t)c.head_dim / 2;
-  const size_t n = (size_t)max_batch * c.n_kv * (size_t)L.pitch;
+  const size_t n = (size_t)max_batch * c.n_kv * (size_t)max_ctx;
   L.kc = 0;
   L.vc = align_up(n * L.entry, 256);
   L.ks = L.vc + align_up(n * L.entry, 256);
@@ -330,31 +292,23 @@ __device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) { return __uint_as
 
 // Symmetric INT4 quantiser decision (FP32): s = bf16_rne(amax / 7); code =
 // clamp(rne(x / s), -8, 7) + 8; s = 0 gives code 8.
-// IEEE round-to-nearest FP32 division, kept out of line: the quantiser calls
-// it per element and one copy of its code is enough.
-static __device__ __noinline__ float div_rn(float a, float b) { return __fdiv_rn(a, b); }
-
 __device__ __forceinline__ uint16_t quant_scale_bits(float amax) {
-  const float q = div_rn(amax, 7.0f);
+  const float q = __fdiv_rn(amax, 7.0f);
   return __bfloat16_as_ushort(__float2bfloat16_rn(q));
 }
 __device__ __forceinline__ uint32_t quant_code(float x, float s) {
   if (s == 0.0f) return 8u;
-  float t = rintf(div_rn(x, s));
+  float t = rintf(__fdiv_rn(x, s));
   t = fminf(fmaxf(t, -8.0f), 7.0f);
   return (uint32_t)((int)t + 8);
 }
 
-// 1 / sqrt(hb) rounded to FP32 (the normalisation of the order-hb Sylvester
-// matrix); hb is a power of two.
-inline float hadamard_scale(int hb) { return (float)(1.0 / std::sqrt((double)hb)); }
-
 // Fast Walsh-Hadamard transform of a d-vector held stride-32 across a warp:
 // lane l owns channels l + 32 m (m < NPL = d / 32).  Butterflies for strides
 // < hb give the natural-order Sylvester transform on each hb block; the
-// result is scaled by sc = hadamard_scale(hb).
+// result is scaled by 1 / sqrt(hb).
 template <int NPL>
-__device__ __forceinline__ void warp_fwht(float (&v)[NPL], int hb, float sc) {
+__device__ __forceinline__ void warp_fwht(float (&v)[NPL], int hb) {
   const int lane = threadIdx.x & 31;
   for (int s = 1; s < hb && s < 32; s <<= 1) {
 #pragma unroll
@@ -374,6 +328,7 @@ __device__ __forceinline__ void warp_fwht(float (&v)[NPL], int hb, float sc) {
       v[m + sm] = a - b;
     }
   }
+  const float sc = __frsqrt_rn((float)hb);
 #pragma unroll
   for (int m = 0; m < NPL; ++m) v[m] *= sc;
 }
@@ -435,6 +390,7 @@ __device__ __forceinline__ void warp_quant_store(float (&v)[NPL], bool is_k, uin
 namespace ft_host {
 
 int num_sms();
+bool pdl_enabled();
 int check_cfg(const ft_block_cfg* c);
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 

@@ -3,9 +3,8 @@
 // "어떻게 동작하나": direct placement at offset(request, head, position, channel)).
 //
 // Cache layout for one layer (KVLayout): four regions
-//   K nibbles [max_batch][n_kv][pitch][d/2], V nibbles (same),
-//   K scales  [max_batch][n_kv][pitch] BF16, V scales (same); pitch = max_ctx
-//   rounded up to 16 positions.
+//   K nibbles [max_batch][n_kv][max_ctx][d/2], V nibbles (same),
+//   K scales  [max_batch][n_kv][max_ctx] BF16, V scales (same).
 // Within an entry the nibbles are permuted (kv_k_channel / kv_v_channel) so that
 // the attention kernel's 16-byte / 8-byte loads land directly in tensor-core
 // fragment order: K as the A operand of q.K (rows = positions), V as the A
@@ -17,7 +16,7 @@ namespace ft {
 template <int NPL>
 __global__ void __launch_bounds__(128) kv_append_kernel(const uint16_t* __restrict__ k, const uint16_t* __restrict__ v,
                                                         const int32_t* __restrict__ pos, uint8_t* __restrict__ cache,
-                                                        KVLayout L, int B, int T, int hb, float hsc, int32_t* status) {
+                                                        KVLayout L, int B, int T, int hb, int32_t* status) {
   constexpr int D = NPL * 32;
   __shared__ uint8_t stage[4][D];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -35,12 +34,12 @@ __global__ void __launch_bounds__(128) kv_append_kernel(const uint16_t* __restri
   float x[NPL];
 #pragma unroll
   for (int m = 0; m < NPL; ++m) x[m] = bf16_bits_to_f32(k[src + lane + 32 * m]);
-  warp_fwht<NPL>(x, hb, hsc);
+  warp_fwht<NPL>(x, hb);
   warp_quant_store<NPL>(x, true, stage[warp], cache + L.kc + row * L.entry,
                         reinterpret_cast<uint16_t*>(cache + L.ks) + row);
 #pragma unroll
   for (int m = 0; m < NPL; ++m) x[m] = bf16_bits_to_f32(v[src + lane + 32 * m]);
-  warp_fwht<NPL>(x, hb, hsc);
+  warp_fwht<NPL>(x, hb);
   warp_quant_store<NPL>(x, false, stage[warp], cache + L.vc + row * L.entry,
                         reinterpret_cast<uint16_t*>(cache + L.vs) + row);
 }
@@ -96,10 +95,10 @@ int ft_kv_append_int4(const ft_block_cfg* c, void* cache, int max_batch, int max
   auto* cp = static_cast<uint8_t*>(cache);
   if (c->head_dim == 128)
     ft::kv_append_kernel<4><<<blocks, 128, 0, (cudaStream_t)stream>>>(k_bf16, v_bf16, pos, cp, L, B, T, c->had_block,
-                                                                      ft::hadamard_scale(c->had_block), dev_status);
+                                                                      dev_status);
   else
     ft::kv_append_kernel<2><<<blocks, 128, 0, (cudaStream_t)stream>>>(k_bf16, v_bf16, pos, cp, L, B, T, c->had_block,
-                                                                      ft::hadamard_scale(c->had_block), dev_status);
+                                                                      dev_status);
   return cudaGetLastError() == cudaSuccess ? FT_OK : FT_ERR_CUDA;
 }
 

@@ -11,7 +11,7 @@
 // the scratch space comes from here.
 //
 // Properties a caller must know:
-//  * the array is kStaticWorkspaceBytes (16 MiB) of device memory that every GPU
+//  * the array is kStaticWorkspaceBytes (8 MiB) of device memory that every GPU
 //    loading this library keeps until the process exits;
 //  * problems whose workspace would exceed it are rejected with
 //    FT_ERR_WORKSPACE before anything is enqueued;
@@ -29,7 +29,7 @@
 
 namespace {
 
-constexpr size_t kStaticWorkspaceBytes = 16u << 20;
+constexpr size_t kStaticWorkspaceBytes = 8u << 20;
 
 // Device-side scratch.  In host code this name is only a handle for
 // cudaGetSymbolAddress, never a device address.

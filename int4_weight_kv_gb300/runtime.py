@@ -40,8 +40,7 @@ def alloc_cache(cfg, max_batch: int, max_ctx: int, device="cuda") -> torch.Tenso
 
 
 def alloc_workspace(cfg, B: int, max_ctx: int, device="cuda") -> torch.Tensor:
-    """Zero-filled, as the decode block requires before the workspace's first use."""
-    return torch.zeros(ft_decode_workspace_bytes(cfg, B, max_ctx), dtype=torch.uint8, device=device)
+    return torch.empty(ft_decode_workspace_bytes(cfg, B, max_ctx), dtype=torch.uint8, device=device)
 
 
 def bits_tensor(bits: np.ndarray, device="cuda") -> torch.Tensor:

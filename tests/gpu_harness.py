@@ -71,21 +71,6 @@ def make_problem(layer: Layer, config_id: int, B: int, ctx: int, pos: Optional[n
     return Problem(layer, B, max_ctx, pos, x_bits, x_f32, kb[:, :hist], vb[:, :hist], cache, status)
 
 
-def sub_problem(pb: Problem, rows) -> Problem:
-    """The requests `rows` of a batch problem as a batch of their own (same
-    inputs, history and positions, a cache of their own)."""
-    rows = list(rows)
-    L = pb.layer
-    B = len(rows)
-    cache = rt.alloc_cache(L.cfg, B, pb.max_ctx)
-    status = torch.zeros(1, dtype=torch.int32, device="cuda")
-    kb, vb = pb.k_bits[rows], pb.v_bits[rows]
-    if kb.shape[1] > 0:
-        rt.fill_history(L.cfg, cache, B, pb.max_ctx, kb, vb, status)
-    torch.cuda.synchronize()
-    return Problem(L, B, pb.max_ctx, pb.pos[rows], pb.x_bits[rows], pb.x_f32[rows], kb, vb, cache, status)
-
-
 @dataclasses.dataclass
 class GpuResult:
     out: np.ndarray          # FP32 [B, H] (or BF16 values widened)

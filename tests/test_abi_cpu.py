@@ -73,9 +73,8 @@ def test_weight_shapes_and_packed_bytes(ft):
 def test_kv_and_workspace_sizes(ft):
     c = _cfg8b(ft)
     nb = ft.ft_kv_cache_bytes(c, 1, 1025)
-    pitch = 1040                                       # positions per (request, head), a multiple of 16
-    assert nb >= pitch * 8 * (64 + 64 + 2 + 2)         # 1056 B per token per layer
-    assert nb < pitch * 8 * (64 + 64 + 2 + 2) + 4 * 256
+    assert nb >= 1025 * 8 * (64 + 64 + 2 + 2)        # 1056 B per token per layer
+    assert nb < 1025 * 8 * (64 + 64 + 2 + 2) + 4 * 256
     assert ft.ft_decode_workspace_bytes(c, 1, 1025) > 0
     assert ft.ft_decode_workspace_bytes(c, 33, 1025) == 0
     assert ft.ft_decode_workspace_bytes(c, 32, 4097) > ft.ft_decode_workspace_bytes(c, 1, 4097)
@@ -102,6 +101,8 @@ def test_argument_errors_return_before_launch(ft):
     assert call(x_out=8192 + 64) == ft.FT_ERR_INVALID_ARG     # overlaps x_in
     assert call(dt=7) == ft.FT_ERR_INVALID_ARG
     assert call(wsb=16) == ft.FT_ERR_WORKSPACE
+    assert lib.ft_decode_block_stages(ctypes.byref(c), ctypes.byref(lw), 4096, 4, 64, 8192, 1 << 20, 0, 256, 1,
+                                      1 << 24, 1 << 30, None, 0, None) == ft.FT_ERR_INVALID_ARG
     # pack / append / unpack argument checks
     assert lib.ft_pack_weights_int4(ctypes.byref(c), 0, None, None, 4096, 1 << 30, None) == ft.FT_ERR_INVALID_ARG
     assert lib.ft_pack_weights_int4(ctypes.byref(c), 0, 4096, None, 8192, 16, None) == ft.FT_ERR_WORKSPACE
@@ -110,4 +111,6 @@ def test_argument_errors_return_before_launch(ft):
     assert lib.ft_kv_append_int4(ctypes.byref(c), 4096, 2, 64, 16, 16, 16, 1, 65, None, None) == ft.FT_ERR_CAPACITY
     assert lib.ft_kv_append_int4(ctypes.byref(c), 4097, 2, 64, 16, 16, 16, 1, 1, None, None) == ft.FT_ERR_INVALID_ARG
     assert lib.ft_kv_unpack_int4(ctypes.byref(c), 4096, 2, 64, 3, 8, 16, 16, 16, 16, None) == ft.FT_ERR_INVALID_ARG
-    assert ft.ft_decode_block_launches() == 1
+    assert ft.ft_decode_block_launches() == 7
+    prev = ft.ft_set_pdl(False)
+    assert ft.ft_set_pdl(prev) is False

@@ -55,15 +55,13 @@ def test_static_workspace_matches_workspace_entry_point(shape, cid, B, ctx):
         # the block's parity tolerances ...
         assert H.rel_rms(out, ref.out) <= 5e-3
         assert H.max_abs_over_rms(out, ref.out) <= 2e-2
-        # ... and, since both run the same kernel, agreement up to rounding: the order of
-        # the atomic FP32 accumulations differs between runs, which can flip the FP16
-        # rounding of single elements of the o and a operands (5e-4, a tenth of the gate)
-        assert H.rel_rms(out, ref.out) < 5e-4
+        # ... and, since both run the same kernels, agreement up to FP32 summation order
+        assert H.rel_rms(out, ref.out) < 1e-4
 
 
 def test_static_workspace_refuses_oversized_problem():
-    cfg = ft.make_cfg(32768, 128, 16, 128, 131072)
-    assert ft.ft_decode_workspace_bytes(cfg, 32, 4097) > 16 << 20
+    cfg = ft.make_cfg(16384, 128, 16, 128, 65536)
+    assert ft.ft_decode_workspace_bytes(cfg, 32, 4097) > 8 << 20
     lw = ft.LayerWeights(16, 16, 16, 16)
     rc = ft.lib().ft_decode_block_static_ws(ctypes.byref(cfg), ctypes.byref(lw), 4096, 32, 4097, 8192, 1 << 24,
                                             ft.FT_BF16, 256, 32, None, None)
