@@ -123,6 +123,24 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# ---------------------------------------------------------------------------- multi-rank helpers
+def dist_env() -> tuple[int, int, int]:
+    """(world size, rank, local rank) from the torchrun environment (1, 0, 0 when run directly)."""
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def max_over_ranks(value: float, device, world: int) -> float:
+    """The largest of every rank's value (the job's time is set by its slowest rank); identity at N=1."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 # ---------------------------------------------------------------------------- our arm
 def setup_replicas(wl, R: int, device):
     import torch
@@ -162,9 +180,7 @@ def run_ours(args):
     import synth
     import int4_weight_kv_gb300 as ft
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    world, rank, local = dist_env()
     if world > 1:
         dist.init_process_group("nccl")
     torch.cuda.set_device(local)
@@ -239,10 +255,7 @@ def run_ours(args):
     clk = clocks.stop()
     if int(status.item()) != 0:
         raise RuntimeError(f"device status {status.item()}")
-    t = torch.tensor([ms], dtype=torch.float64, device=device)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms = float(t.item())
+    ms = max_over_ranks(ms, device, world)
     us_step = ms * 1000.0 / args.steps
 
     # dominant kernel (gate/up projection) timed alone with CUDA events on its stream
