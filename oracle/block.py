@@ -16,7 +16,7 @@ Steps, in the order the pages give them (summary page, sections "어떻게
 6. [g; u] = rho_2 * W'_gu h1;  a = g * sigmoid(g) * u  (SwiGLU).
 7. out = h1 + W_down a.
 
-Readings taken where the pages are silent (all listed in the design doc): eps, the
+Readings taken where the pages are silent: eps, the
 RoPE convention, the Hadamard choice, scale divisor 7, contiguous GQA groups,
 the new token attending to its own quantised K/V.
 """
