@@ -163,11 +163,11 @@ int ft_decode_block(const ft_block_cfg *cfg, const ft_layer_weights *w, void *ca
 
 /* Stage selection for ft_decode_block_stages (bit mask). */
 enum {
-  FT_STAGE_PREP = 1,  /* input -> FP16 operand, rho1, zero the counters      */
+  FT_STAGE_PREP = 1,  /* input -> FP16 operand, sums of squares, zero counters */
   FT_STAGE_QKV = 2,   /* QKV projection (x rho1)                             */
   FT_STAGE_ATTN = 4,  /* RoPE, rotation, cache write, split-KV attention     */
   FT_STAGE_O = 8,     /* O projection + residual                              */
-  FT_STAGE_MID = 16,  /* h1 -> gate/up operand, rho2, down accumulator        */
+  FT_STAGE_MID = 16,  /* h1 -> gate/up operand, sums of squares, down acc.   */
   FT_STAGE_GU = 32,   /* gate/up projection + SwiGLU                          */
   FT_STAGE_DOWN = 64, /* down projection + residual -> x_out                  */
   FT_STAGE_ALL = 127

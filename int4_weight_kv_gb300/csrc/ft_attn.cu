@@ -132,7 +132,13 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnParams p) {
   griddep_wait();
 
   // ---- rotated query of the G heads: rho1, RoPE, Hadamard, softmax scale
-  const float rho1 = p.rho1[b];
+  float rho1;  // RMSNorm row factor of the block input, from the prep kernel's partial sums
+  {
+    float t = 0.0f;
+    for (int k = lane; k < p.nssq; k += 32) t += __ldcg(p.ssq1 + b * p.nssq + k);
+    rho1 = rsqrtf(warp_sum(t) * p.inv_h + p.eps);
+    if (tid == 0 && h == 0 && split == 0) p.rho1[b] = rho1;
+  }
   for (int hh = warp; hh < G; hh += 4) {
     float v[NPL];
     const float* src = p.qkv + (size_t)b * p.Nqkv + (size_t)(h * G + hh) * D;

@@ -34,134 +34,105 @@ __device__ __forceinline__ float group16_sum(float v) {
   return v;
 }
 
-// Block input -> QKV operand + offsets, rho1 (applied after the QKV
-// accumulation, summary page "어떻게 동작하나"), h1 accumulator <- x, and this
-// call's accumulators cleared.  One CTA (256 threads) per request.
-__global__ void __launch_bounds__(256) prep_kernel(const PrepParams p) {
-  griddep_wait();  // the previous kernel may have produced x_in or still read the workspace
-  griddep_launch();
-  __shared__ float red[8];
-  const int b = blockIdx.x, tid = threadIdx.x;
-  for (int i = tid; i < p.nqkv; i += 256) p.qkv[(size_t)b * p.nqkv + i] = 0.0f;
-  for (int i = tid; i < p.nkg_o; i += 256) p.s_o[i * 32 + b] = 0.0f;
-  for (int i = tid; i < p.nkg_a; i += 256) p.s_a[i * 32 + b] = 0.0f;
-  if (b == 0)
-    for (int i = tid; i < p.ntick; i += 256) p.tick[i] = 0u;
-  constexpr int MAXC = 4;
-  const int nchunk = p.H / 8;  // a multiple of 16
-  float ss = 0.0f;
+// Loads chunk ch (inputs 8 ch .. 8 ch + 7) of a BF16 or FP32 row.
+__device__ __forceinline__ void load_chunk8(const void* row, int dtype, int ch, float (&v)[8]) {
+  if (dtype == FT_F32) {
+    const float4* src = reinterpret_cast<const float4*>(row) + 2 * ch;
+    const float4 a = __ldcg(src), d = __ldcg(src + 1);
+    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    v[4] = d.x; v[5] = d.y; v[6] = d.z; v[7] = d.w;
+  } else {
+    const uint4 a = __ldcg(reinterpret_cast<const uint4*>(row) + ch);
+    const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      v[2 * k] = __uint_as_float(w[k] << 16);
+      v[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+    }
+  }
+}
+
+// One row part: chunk ch of the row -> FP32 copy, FP16 operand + group offsets,
+// and the part's sum of squares (written by thread 0).  kPrepThreads threads,
+// one chunk each; a part is a whole number of 128-input groups.
+__device__ __forceinline__ bool row_part(const float (&v)[8], bool valid, int ch, int b, float* copy, __half* op,
+                                         float* s_grp, float* ssq_out) {
+  __shared__ float red[kPrepThreads / 32];
+  float ss = 0.0f, sterm = 0.0f;
   bool bad = false;
-  for (int base = 0; base < nchunk; base += 256 * MAXC) {
-    float v[MAXC][8];
+  if (valid) {
 #pragma unroll
-    for (int c = 0; c < MAXC; ++c) {
-      const int ch = base + tid + 256 * c;
-      if (ch < nchunk) {
-        if (p.act_dtype == FT_F32) {
-          const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(p.x_in) + (size_t)b * p.H) + 2 * ch;
-          const float4 a = __ldcg(src), d = __ldcg(src + 1);
-          v[c][0] = a.x; v[c][1] = a.y; v[c][2] = a.z; v[c][3] = a.w;
-          v[c][4] = d.x; v[c][5] = d.y; v[c][6] = d.z; v[c][7] = d.w;
-        } else {
-          const uint4 a =
-              __ldcg(reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.x_in) + (size_t)b * p.H) + ch);
-          const uint32_t w[4] = {a.x, a.y, a.z, a.w};
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            v[c][2 * k] = __uint_as_float(w[k] << 16);
-            v[c][2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
-          }
-        }
-      }
+    for (int k = 0; k < 8; ++k) {
+      ss = fmaf(v[k], v[k], ss);
+      bad |= !(fabsf(v[k]) <= 65504.0f);
     }
-#pragma unroll
-    for (int c = 0; c < MAXC; ++c) {
-      const int ch = base + tid + 256 * c;
-      float sterm = 0.0f;
-      if (ch < nchunk) {
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          ss = fmaf(v[c][k], v[c][k], ss);
-          bad |= !(fabsf(v[c][k]) <= 65504.0f);
-        }
-        float4* h1 = reinterpret_cast<float4*>(p.h1 + (size_t)b * p.H) + 2 * ch;
-        h1[0] = make_float4(v[c][0], v[c][1], v[c][2], v[c][3]);
-        h1[1] = make_float4(v[c][4], v[c][5], v[c][6], v[c][7]);
-        sterm = encode_chunk8(v[c], ch, p.x_h + (size_t)b * p.H);
-      }
-      // whole warps stay converged here: nchunk and 256 * MAXC are multiples of 16
-      const float gs = group16_sum(sterm);
-      if (ch < nchunk && (ch & 15) == 0) p.s_x[(ch >> 4) * 32 + b] = gs;
+    if (copy) {
+      float4* dst = reinterpret_cast<float4*>(copy) + 2 * ch;
+      dst[0] = make_float4(v[0], v[1], v[2], v[3]);
+      dst[1] = make_float4(v[4], v[5], v[6], v[7]);
     }
+    sterm = encode_chunk8(v, ch, op);
   }
+  // warps stay converged: a group is 16 chunks and parts start on group boundaries
+  const float gs = group16_sum(sterm);
+  if (valid && (ch & 15) == 0) s_grp[(ch >> 4) * 32 + b] = gs;
   ss = warp_sum(ss);
-  if ((tid & 31) == 0) red[tid >> 5] = ss;
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
   __syncthreads();
-  if (tid == 0) {
+  if (threadIdx.x == 0) {
     float t = 0.0f;
-    for (int w = 0; w < 8; ++w) t += red[w];
-    p.rho1[b] = rsqrtf(t / (float)p.H + p.eps);
+#pragma unroll
+    for (int w = 0; w < kPrepThreads / 32; ++w) t += red[w];
+    *ssq_out = t;
   }
+  return bad;
+}
+
+// Block input -> QKV operand + offsets, partial sums of x^2 (the consumers form
+// rho1 from them and apply it after the QKV accumulation, summary page
+// "어떻게 동작하나"), h1 accumulator <- x, and this call's accumulators cleared.
+// Grid (parts, B).
+__global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepParams p) {
+  griddep_launch();  // the QKV kernel may start streaming its weights
+  griddep_wait();    // the previous kernel may have produced x_in or still read the workspace
+  const int part = blockIdx.x, parts = gridDim.x, b = blockIdx.y, tid = threadIdx.x;
+  const int first = part * kPrepThreads + tid, step = parts * kPrepThreads;
+  for (int i = first; i < p.nqkv; i += step) p.qkv[(size_t)b * p.nqkv + i] = 0.0f;
+  for (int i = first; i < p.nkg_o; i += step) p.s_o[i * 32 + b] = 0.0f;
+  for (int i = first; i < p.nkg_a; i += step) p.s_a[i * 32 + b] = 0.0f;
+  if (b == 0)
+    for (int i = first; i < p.ntick; i += step) p.tick[i] = 0u;
+  const int ch = first;
+  const bool valid = ch < p.H / 8;
+  float v[8];
+  const size_t esz = p.act_dtype == FT_F32 ? 4 : 2;
+  if (valid) load_chunk8(static_cast<const uint8_t*>(p.x_in) + (size_t)b * p.H * esz, p.act_dtype, ch, v);
+  const bool bad = row_part(v, valid, ch, b, p.h1 + (size_t)b * p.H, p.x_h + (size_t)b * p.H, p.s_x,
+                            p.ssq + b * parts + part);
   if (bad) set_status(p.status, FT_DEV_RANGE);
 }
 
-// h1 (complete after the O projection) -> gate/up operand + offsets, rho2
-// (applied after the gate/up accumulation), and the down accumulator <- h1.
-__global__ void __launch_bounds__(256) mid_kernel(const MidParams p) {
+// h1 (complete after the O projection) -> gate/up operand + offsets, partial
+// sums of h1^2 (rho2 is formed and applied after the gate/up accumulation), and
+// the down accumulator <- h1.  Grid (parts, B).
+__global__ void __launch_bounds__(kPrepThreads) mid_kernel(const MidParams p) {
+  griddep_launch();  // the gate/up kernel may start streaming its weights
   griddep_wait();
-  griddep_launch();
-  __shared__ float red[8];
-  const int b = blockIdx.x, tid = threadIdx.x;
-  constexpr int MAXC = 4;
-  const int nchunk = p.H / 8;
-  float ss = 0.0f;
-  bool bad = false;
-  for (int base = 0; base < nchunk; base += 256 * MAXC) {
-    float v[MAXC][8];
-#pragma unroll
-    for (int c = 0; c < MAXC; ++c) {
-      const int ch = base + tid + 256 * c;
-      if (ch < nchunk) {
-        const float4* src = reinterpret_cast<const float4*>(p.h1 + (size_t)b * p.H) + 2 * ch;
-        const float4 a = __ldcg(src), d = __ldcg(src + 1);
-        v[c][0] = a.x; v[c][1] = a.y; v[c][2] = a.z; v[c][3] = a.w;
-        v[c][4] = d.x; v[c][5] = d.y; v[c][6] = d.z; v[c][7] = d.w;
-      }
-    }
-#pragma unroll
-    for (int c = 0; c < MAXC; ++c) {
-      const int ch = base + tid + 256 * c;
-      float sterm = 0.0f;
-      if (ch < nchunk) {
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          ss = fmaf(v[c][k], v[c][k], ss);
-          bad |= !(fabsf(v[c][k]) <= 65504.0f);
-        }
-        float4* dst = reinterpret_cast<float4*>(p.out_acc + (size_t)b * p.H) + 2 * ch;
-        dst[0] = make_float4(v[c][0], v[c][1], v[c][2], v[c][3]);
-        dst[1] = make_float4(v[c][4], v[c][5], v[c][6], v[c][7]);
-        sterm = encode_chunk8(v[c], ch, p.h1_h + (size_t)b * p.H);
-      }
-      const float gs = group16_sum(sterm);
-      if (ch < nchunk && (ch & 15) == 0) p.s_h1[(ch >> 4) * 32 + b] = gs;
-    }
-  }
-  ss = warp_sum(ss);
-  if ((tid & 31) == 0) red[tid >> 5] = ss;
-  __syncthreads();
-  if (tid == 0) {
-    float t = 0.0f;
-    for (int w = 0; w < 8; ++w) t += red[w];
-    p.rho2[b] = rsqrtf(t / (float)p.H + p.eps);
-  }
+  const int part = blockIdx.x, parts = gridDim.x, b = blockIdx.y;
+  const int ch = part * kPrepThreads + threadIdx.x;
+  const bool valid = ch < p.H / 8;
+  float v[8];
+  if (valid) load_chunk8(p.h1 + (size_t)b * p.H, FT_F32, ch, v);
+  const bool bad = row_part(v, valid, ch, b, p.out_acc == p.h1 ? nullptr : p.out_acc + (size_t)b * p.H,
+                            p.h1_h + (size_t)b * p.H, p.s_h1, p.ssq + b * parts + part);
   if (bad) set_status(p.status, FT_DEV_RANGE);
 }
 
 struct WsPlan {
   GemvPlan g[4];
   int nsplit;
-  size_t x_h, s_x, rho1, h1, qkv, o_h, s_o, h1_h, s_h1, rho2, a_h, s_a, out_acc, tick, total;
+  int parts;  // prep / mid CTAs per request
+  size_t x_h, s_x, rho1, ssq1, h1, qkv, o_h, s_o, h1_h, s_h1, ssq2, a_h, s_a, out_acc, tick, total;
 };
 
 static int attn_splits(int B, int nkv, int max_ctx, int sms) {
@@ -194,14 +165,16 @@ static WsPlan make_plan(const ft_block_cfg& c, int B, int max_ctx) {
   };
   w.x_h = take((size_t)B * c.hidden * 2);
   w.s_x = take((size_t)(c.hidden / 128) * 32 * 4);
+  w.parts = rms_parts(c.hidden);
   w.rho1 = take((size_t)B * 4);
+  w.ssq1 = take((size_t)B * w.parts * 4);
   w.h1 = take((size_t)B * c.hidden * 4);
   w.qkv = take((size_t)B * nqkv * 4);
   w.o_h = take((size_t)B * c.n_q * c.head_dim * 2);
   w.s_o = take((size_t)(c.n_q * c.head_dim / 128) * 32 * 4);
   w.h1_h = take((size_t)B * c.hidden * 2);
   w.s_h1 = take((size_t)(c.hidden / 128) * 32 * 4);
-  w.rho2 = take((size_t)B * 4);
+  w.ssq2 = take((size_t)B * w.parts * 4);
   w.a_h = take((size_t)B * c.inter * 2);
   w.s_a = take((size_t)(c.inter / 128) * 32 * 4);
   w.out_acc = take((size_t)B * c.hidden * 4);
@@ -250,10 +223,9 @@ static int run_block(const ft_block_cfg* c, const ft_layer_weights* w, void* cac
     pp.act_dtype = act_dtype;
     pp.B = B;
     pp.H = c->hidden;
-    pp.eps = c->rms_eps;
     pp.x_h = Hh(P.x_h);
     pp.s_x = F(P.s_x);
-    pp.rho1 = F(P.rho1);
+    pp.ssq = F(P.ssq1);
     pp.h1 = F(P.h1);
     pp.qkv = F(P.qkv);
     pp.nqkv = (c->n_q + 2 * c->n_kv) * c->head_dim;
@@ -264,7 +236,8 @@ static int run_block(const ft_block_cfg* c, const ft_layer_weights* w, void* cac
     pp.tick = reinterpret_cast<uint32_t*>(W + P.tick);
     pp.ntick = P.g[kRoleDown].NSET;
     pp.status = status;
-    if (launch_ex(prep_kernel, dim3(B), dim3(256), 0, st, pdl, pp) != cudaSuccess) return FT_ERR_CUDA;
+    if (launch_ex(prep_kernel, dim3(P.parts, B), dim3(kPrepThreads), 0, st, pdl, pp) != cudaSuccess)
+      return FT_ERR_CUDA;
   }
 
   auto gemv = [&](int role, const void* wptr, size_t xoff, size_t soff) {
@@ -281,7 +254,10 @@ static int run_block(const ft_block_cfg* c, const ft_layer_weights* w, void* cac
       case kRoleGU:
         g.out_h = Hh(P.a_h);
         g.s_out = F(P.s_a);
-        g.rho2 = F(P.rho2);
+        g.ssq2 = F(P.ssq2);
+        g.nssq = P.parts;
+        g.inv_h = 1.0f / (float)c->hidden;
+        g.eps = c->rms_eps;
         break;
       case kRoleDown:
         g.out_f32 = down_acc;
@@ -299,6 +275,10 @@ static int run_block(const ft_block_cfg* c, const ft_layer_weights* w, void* cac
   if (mask & FT_STAGE_ATTN) {
     AttnParams a;
     a.qkv = F(P.qkv);
+    a.ssq1 = F(P.ssq1);
+    a.nssq = P.parts;
+    a.inv_h = 1.0f / (float)c->hidden;
+    a.eps = c->rms_eps;
     a.rho1 = F(P.rho1);
     a.cache = static_cast<uint8_t*>(cache);
     a.L = L;
@@ -326,13 +306,13 @@ static int run_block(const ft_block_cfg* c, const ft_layer_weights* w, void* cac
     mp.h1 = F(P.h1);
     mp.B = B;
     mp.H = c->hidden;
-    mp.eps = c->rms_eps;
     mp.h1_h = Hh(P.h1_h);
     mp.s_h1 = F(P.s_h1);
-    mp.rho2 = F(P.rho2);
+    mp.ssq = F(P.ssq2);
     mp.out_acc = down_acc;
     mp.status = status;
-    if (launch_ex(mid_kernel, dim3(B), dim3(256), 0, st, pdl, mp) != cudaSuccess) return FT_ERR_CUDA;
+    if (launch_ex(mid_kernel, dim3(P.parts, B), dim3(kPrepThreads), 0, st, pdl, mp) != cudaSuccess)
+      return FT_ERR_CUDA;
   }
   if (mask & FT_STAGE_GU) {
     if (gemv(kRoleGU, w->gateup, P.h1_h, P.s_h1) != cudaSuccess) return FT_ERR_CUDA;

@@ -42,7 +42,9 @@ struct GemvParams {
   float* out_f32;     // QKV: qkv acc;  O: h1 acc;  DOWN: out acc (or the FP32 output)
   __half* out_h;      // GU: a operand [B][I]
   float* s_out;       // GU: a's group offsets [I/128][32] (accumulated)
-  const float* rho2;  // GU: RMSNorm row factor of h1 [B]
+  const float* ssq2;  // GU: partial sums of h1^2 [B][nssq], giving the RMSNorm row factor rho2
+  int nssq;
+  float inv_h, eps;   // GU: 1 / hidden, RMSNorm epsilon
   void* out_final;    // DOWN: block output
   int out_dtype;
   int32_t* status;
@@ -50,7 +52,10 @@ struct GemvParams {
 
 struct AttnParams {
   const float* qkv;   // [B][Nqkv] accumulated projections, before rho1 and RoPE
-  const float* rho1;  // [B] RMSNorm row factor of the block input
+  const float* ssq1;  // [B][nssq] partial sums of x^2, giving the RMSNorm row factor rho1
+  int nssq;
+  float inv_h, eps;
+  float* rho1;        // [B] rho1, recorded for inspection
   uint8_t* cache;
   KVLayout L;
   const int32_t* pos;
@@ -62,15 +67,15 @@ struct AttnParams {
   double inv_freq[64];
 };
 
-// Block input -> QKV operand, rho1, h1 accumulator initialised to x, and the
-// accumulators of this call cleared.  One CTA per request.
+// Block input -> QKV operand, partial sums of x^2, h1 accumulator initialised
+// to x, and the accumulators of this call cleared.  CTA (part, request) covers
+// 512 inputs (kPrepChunk chunks of 8).
 struct PrepParams {
   const void* x_in;
   int act_dtype, B, H;
-  float eps;
   __half* x_h;       // [B][H] operand
   float* s_x;        // [H/128][32]
-  float* rho1;       // [B]
+  float* ssq;        // [B][parts] partial sums of x^2
   float* h1;         // [B][H] <- x
   float* qkv;        // [B][Nqkv] <- 0
   int nqkv;
@@ -83,18 +88,21 @@ struct PrepParams {
   int32_t* status;
 };
 
-// Between O and gate/up: h1 -> its operand and offsets, rho2, and the down
-// accumulator initialised to h1.  One CTA per request.
+// Between O and gate/up: h1 -> its operand and offsets, partial sums of h1^2,
+// and the down accumulator initialised to h1.  CTA (part, request) covers 512
+// inputs.
 struct MidParams {
   const float* h1;   // [B][H] complete after O
   int B, H;
-  float eps;
   __half* h1_h;      // [B][H] operand
   float* s_h1;       // [H/128][32]
-  float* rho2;       // [B]
+  float* ssq;        // [B][parts] partial sums of h1^2
   float* out_acc;    // [B][H] <- h1
   int32_t* status;
 };
+
+constexpr int kPrepThreads = 64;  // threads (chunks of 8 inputs) per prep / mid CTA
+__host__ __device__ __forceinline__ int rms_parts(int H) { return (H / 8 + kPrepThreads - 1) / kPrepThreads; }
 
 // host-side launchers (ft_gemv.cu / ft_attn.cu / ft_block.cu)
 cudaError_t launch_gemv(int role, const GemvParams& p, cudaStream_t st, bool pdl);

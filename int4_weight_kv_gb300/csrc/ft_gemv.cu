@@ -40,8 +40,10 @@ __device__ __forceinline__ void red_add(float* p, float v) { atomicAdd(p, v); }
 
 // Epilogue of one (row tile, column tile) of fully reduced values.
 // v[0] = (row g, token t0), v[1] = (row g, t0+1), v[2] = (row g+8, t0), v[3] = (row g+8, t0+1).
+// rho2_lane: lane t holds the RMSNorm row factor of token t (gate/up only).
 template <int ROLE>
-__device__ __forceinline__ bool gemv_epi(const GemvParams& p, int T, int j, const float (&v)[4], bool direct) {
+__device__ __forceinline__ bool gemv_epi(const GemvParams& p, int T, int j, const float (&v)[4], bool direct,
+                                         float rho2_lane) {
   const int lane = threadIdx.x & 31, g = lane >> 2, tig = lane & 3;
   const int N = p.plan.N;
   const int r0 = T * kRowTile + g, r1 = r0 + 8;
@@ -54,8 +56,8 @@ __device__ __forceinline__ bool gemv_epi(const GemvParams& p, int T, int j, cons
     for (int e = 0; e < 2; ++e) {
       const int t = 8 * j + 2 * tig + e;
       float st = 0.0f;
+      const float rho2 = __shfl_sync(0xffffffffu, rho2_lane, t & 31);
       if (t < p.B) {
-        const float rho2 = p.rho2[t];
         const float gv = rho2 * v[e], uv = rho2 * v[2 + e];
         const float a = gv / (1.0f + expf(-gv)) * uv;
         bad |= !(fabsf(a) <= 65504.0f);
@@ -193,6 +195,14 @@ __global__ void __launch_bounds__((GemvShape<NT>::NCW + 2) * 32, 1) gemv_kernel(
     // Reduces each finished piece over the consumer warps and applies the role
     // epilogue while the consumers already stream the next piece.
     griddep_wait();
+    // loaded once: a dependent global load per epilogue call would sit on the
+    // critical path of every piece
+    float rho2_lane = 0.0f;
+    if (ROLE == kRoleGU && lane < p.B) {
+      float t = 0.0f;
+      for (int k = 0; k < p.nssq; ++k) t += __ldcg(p.ssq2 + lane * p.nssq + k);
+      rho2_lane = rsqrtf(t * p.inv_h + p.eps);
+    }
     bool bad = false;
     int k = 0, piece_kg0 = -1;
     for (StageWalk st(pl, u0, u1); st.valid(); st.next()) {
@@ -216,7 +226,7 @@ __global__ void __launch_bounds__((GemvShape<NT>::NCW + 2) * 32, 1) gemv_kernel(
           for (int w = 0; w < NCW; ++w) a += red[((w * RT * NT + q) * 4 + r) * 32 + lane];
           v[r] = a;
         }
-        bad |= gemv_epi<ROLE>(p, st.set * RT + rt, j, v, whole);
+        bad |= gemv_epi<ROLE>(p, st.set * RT + rt, j, v, whole, rho2_lane);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(red_empty);
