@@ -29,6 +29,13 @@ int num_sms() {
 
 bool pdl_enabled() { return g_pdl.load() != 0; }
 
+int smem_per_sm() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess) return 0;
+  return n;
+}
+
 static bool pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
 
 int check_cfg(const ft_block_cfg* c) {

@@ -15,11 +15,13 @@
 // A fragment of two k-steps; the V entry's nibbles so that two positions' bytes
 // combine (prmt) into A fragments of V^T.  Per-position scales multiply the
 // scores (K) and the probabilities (V).  The n_split CTAs of one (b, h) form a
-// thread-block cluster: each keeps its (max, sum, acc) partial in shared
-// memory, a cluster barrier publishes them, and CTA r merges heads r, r+n_split,
-// ... by reading its peers' partials through distributed shared memory, adds
-// the new token (quantised and written to the cache at L_b by CTA 0, decoded
-// identically by every CTA), undoes the rotation and writes o.
+// thread-block cluster.  CTA r merges heads r, r + n_split, ...: every CTA
+// pushes its (max, sum, acc) partial of each head into the merging CTA's shared
+// memory with distributed-shared-memory stores, one cluster barrier publishes
+// them, and the merger combines them from its own shared memory with the new
+// token, undoes the rotation and writes o.  The new token is quantised (and
+// written to the cache at L_b by CTA 0) and decoded by every merging CTA before
+// the main loop, while the first K/V tiles are in flight.
 #include "ft_block.cuh"
 
 namespace ft {
@@ -75,18 +77,20 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-// RoPE at position pos on a d-vector held stride-32 (lane owns l + 32 m);
-// angles pos * inv_freq[i] are formed and reduced modulo 2 pi in FP64.
+// RoPE at position pos on a d-vector held stride-32 (lane owns l + 32 m).
+// turn[i] is inv_freq[i] / (2 pi) as a 64-bit binary fraction, so pos * turn[i]
+// modulo 2^64 is the angle in turns reduced exactly modulo one turn; its top 32
+// bits, read as a signed fraction in [-1/2, 1/2), feed sincospif.
 template <int NPL>
-__device__ __forceinline__ void warp_rope(float (&v)[NPL], int pos, const double* inv_freq) {
+__device__ __forceinline__ void warp_rope(float (&v)[NPL], int pos, const uint64_t* turn) {
   const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int m = 0; m < NPL / 2; ++m) {
     const int i = lane + 32 * m;
-    const double ang = (double)pos * inv_freq[i];
-    const double r = fma(-6.283185307179586476925, rint(ang * 0.15915494309189533577), ang);
+    const uint64_t t = (uint64_t)(uint32_t)pos * turn[i];
+    const float half_turns = (float)(int32_t)(uint32_t)(t >> 32) * 4.656612873077393e-10f;  // x 2^-31
     float sn, cs;
-    sincosf((float)r, &sn, &cs);
+    sincospif(half_turns, &sn, &cs);
     const float x1 = v[m], x2 = v[m + NPL / 2];
     v[m] = x1 * cs - x2 * sn;
     v[m + NPL / 2] = x2 * cs + x1 * sn;
@@ -97,12 +101,15 @@ template <int D>
 __global__ void __launch_bounds__(128) attn_kernel(const AttnParams p) {
   constexpr int NPL = D / 32;
   constexpr int KT = D / 16;  // k-tiles of q.K == m-tiles of P.V
-  constexpr int PARTF = 16 + 8 * D;
+  constexpr int PW = D + 2;             // one partial: running max, sum, acc[D]
   __shared__ float qt[8][D];            // rotated, scaled query (FP16 values)
   __shared__ float qoff[8];             // its operand offsets (magic-number decode)
-  __shared__ float mrg[4][PARTF];       // per-warp partials for the CTA merge
   __shared__ float knew[D], vnew[D];
-  __shared__ float cpart[16 + 8 * D];    // this CTA's merged partial, read by the cluster
+  // dynamic: mrg[4][G * PW], each warp's partial of every head, then
+  // inbox[n_split * ceil(G / n_split)][PW], the partials of the heads this CTA
+  // merges, pushed by every CTA of the cluster (slot j * n_split + r holds CTA
+  // r's partial of head split + j * n_split)
+  extern __shared__ __align__(16) float dyn[];
   __shared__ uint8_t stage[2][D];
   __shared__ __align__(16) uint8_t stage_out[2][D / 2];
   __shared__ uint16_t stage_sc[2];
@@ -124,6 +131,8 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnParams p) {
   const int t0 = split * tps, t1 = min(t0 + tps, ntiles);
   const int p1 = min(16 * t1, Lb);
 
+  cluster_arrive_relaxed();  // paired with cluster_wait() before the first DSMEM store
+
   // history K/V do not depend on earlier kernels: start streaming now
   TileRegs<D> cur;
   int ti = t0 + warp;
@@ -131,7 +140,6 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnParams p) {
 
   griddep_wait();
 
-  // ---- rotated query of the G heads: rho1, RoPE, Hadamard, softmax scale
   float rho1;  // RMSNorm row factor of the block input, from the prep kernel's partial sums
   {
     float t = 0.0f;
@@ -139,12 +147,13 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnParams p) {
     rho1 = rsqrtf(warp_sum(t) * p.inv_h + p.eps);
     if (tid == 0 && h == 0 && split == 0) p.rho1[b] = rho1;
   }
-  for (int hh = warp; hh < G; hh += 4) {
+  // ---- rotated, scaled query of each head (rho1, RoPE, Hadamard, softmax scale)
+  for (int u = warp; u < G; u += 4) {
     float v[NPL];
-    const float* src = p.qkv + (size_t)b * p.Nqkv + (size_t)(h * G + hh) * D;
+    const float* src = p.qkv + (size_t)b * p.Nqkv + (size_t)(h * G + u) * D;
 #pragma unroll
     for (int m = 0; m < NPL; ++m) v[m] = __ldcg(src + lane + 32 * m) * rho1;
-    warp_rope<NPL>(v, Lb, p.inv_freq);
+    warp_rope<NPL>(v, Lb, p.rope_turn);
     warp_fwht<NPL>(v, p.hb);
     // q~ as the FP16 B operand (channels c % 16 >= 8 hold q / 16) and its offset
     float sq = 0.0f;
@@ -152,13 +161,22 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnParams p) {
     for (int m = 0; m < NPL; ++m) {
       const int c = lane + 32 * m;
       const float q = __half2float(__float2half_rn(v[m] * p.qscale));
-      qt[hh][c] = q;
+      qt[u][c] = q;
       float st;
       (void)op_encode(q, c, st);
       sq += st;
     }
     sq = warp_sum(sq);
-    if (lane == 0) qoff[hh] = sq;
+    if (lane == 0) qoff[u] = sq;
+  }
+  // the new token's k (warp 0) and v (warp 1), needed by the merging CTAs only:
+  // loaded now, processed after the main loop
+  const bool merger = split < G;
+  float kvraw[NPL];
+  if (merger && warp < 2) {
+    const float* src = p.qkv + (size_t)b * p.Nqkv + (size_t)(p.nq + warp * p.nkv + h) * D;
+#pragma unroll
+    for (int m = 0; m < NPL; ++m) kvraw[m] = __ldcg(src + lane + 32 * m);
   }
   __syncthreads();
   uint32_t bq[KT][2];
@@ -274,48 +292,53 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnParams p) {
     l0 += __shfl_xor_sync(0xffffffffu, l0, o);
     l1 += __shfl_xor_sync(0xffffffffu, l1, o);
   }
-  float* mw = mrg[warp];
+  float* mrg = dyn;                       // [4][G * PW]
+  float* inbox = dyn + 4 * G * PW;        // [n_split * ceil(G / n_split)][PW]
+  float* mw = mrg + warp * G * PW;
+  const bool c0ok = 2 * tig < G, c1ok = 2 * tig + 1 < G;  // this lane's two head columns exist
+  float* h0 = mw + (2 * tig) * PW;
+  float* h1 = mw + (2 * tig + 1) * PW;
   if (g == 0) {
-    mw[2 * tig] = m0;
-    mw[2 * tig + 1] = m1;
-    mw[8 + 2 * tig] = l0;
-    mw[8 + 2 * tig + 1] = l1;
+    if (c0ok) h0[0] = m0, h0[1] = l0;
+    if (c1ok) h1[0] = m1, h1[1] = l1;
   }
 #pragma unroll
   for (int mt = 0; mt < KT; ++mt) {
     const int c0 = 16 * mt + g, c1 = c0 + 8;
-    mw[16 + (2 * tig) * D + c0] = acc[mt][0];
-    mw[16 + (2 * tig + 1) * D + c0] = acc[mt][1];
-    mw[16 + (2 * tig) * D + c1] = acc[mt][2];
-    mw[16 + (2 * tig + 1) * D + c1] = acc[mt][3];
+    if (c0ok) h0[2 + c0] = acc[mt][0], h0[2 + c1] = acc[mt][2];
+    if (c1ok) h1[2 + c0] = acc[mt][1], h1[2 + c1] = acc[mt][3];
   }
   __syncthreads();
-  for (int i = tid; i < 8 * D + 16; i += 128) {
-    const int hh = (i < 16) ? (i & 7) : (i - 16) / D;
+  // ---- this CTA's partial of every head, pushed into the inbox of the CTA that
+  // merges the head (DSMEM stores; the cluster barrier below publishes them)
+  cluster_wait();  // every CTA of the cluster has started (arrived at entry)
+  const uint32_t inbox0 = smem_u32(inbox);
+  for (int i = tid; i < G * PW; i += 128) {
+    const int hh = i / PW, e = i - hh * PW;
     float M = -INFINITY;
-    for (int w = 0; w < 4; ++w) M = fmaxf(M, mrg[w][hh]);
+    for (int w = 0; w < 4; ++w) M = fmaxf(M, mrg[w * G * PW + hh * PW]);
     float v;
-    if (i < 8) {
+    if (e == 0) {
       v = M;
     } else {
       v = 0.0f;
       if (M != -INFINITY)
         for (int w = 0; w < 4; ++w) {
-          const float mw2 = mrg[w][hh];
-          if (mw2 != -INFINITY) v += mrg[w][i] * exp2f(mw2 - M);
+          const float mw2 = mrg[w * G * PW + hh * PW];
+          if (mw2 != -INFINITY) v += mrg[w * G * PW + i] * exp2f(mw2 - M);
         }
     }
-    cpart[i] = v;
+    const int slot = (hh / p.nsplit) * p.nsplit + split;
+    st_dsmem_f32(inbox0 + 4 * (slot * PW + e), (uint32_t)(hh % p.nsplit), v);
   }
 
-  // ---- the new token: RoPE on k, rotation, INT4 (cache write by split 0), decode
-  if (warp < 2) {
+  // ---- the new token (merging CTAs): RoPE on k, rotation, INT4 (cache write at
+  // L_b by split 0), decode; overlaps the peers' pushes
+  if (merger && warp < 2) {
     float v[NPL];
-    const int off = (warp == 0) ? (p.nq + h) * D : (p.nq + p.nkv + h) * D;
-    const float* src = p.qkv + (size_t)b * p.Nqkv + off;
 #pragma unroll
-    for (int m = 0; m < NPL; ++m) v[m] = __ldcg(src + lane + 32 * m) * rho1;
-    if (warp == 0) warp_rope<NPL>(v, Lb, p.inv_freq);
+    for (int m = 0; m < NPL; ++m) v[m] = kvraw[m] * rho1;
+    if (warp == 0) warp_rope<NPL>(v, Lb, p.rope_turn);
     warp_fwht<NPL>(v, p.hb);
     const size_t row = p.L.row(b, h, Lb);
     uint8_t* entry = (split == 0) ? p.cache + (warp == 0 ? p.L.kc : p.L.vc) + row * p.L.entry : stage_out[warp];
@@ -326,30 +349,30 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnParams p) {
 #pragma unroll
     for (int m = 0; m < NPL; ++m) dst[lane + 32 * m] = v[m];
   }
-  __syncthreads();
-  cluster_sync();  // every CTA's partial is now visible to the cluster
+  cluster_sync();  // every pushed partial is now in its merger's shared memory
 
-  // ---- CTA r merges heads r, r + n_split, ...: peers' partials via DSMEM
-  const uint32_t cp_local = smem_u32(cpart);
-  for (int hh = split + p.nsplit * warp; hh < G; hh += p.nsplit * 4) {
+  // ---- CTA r merges heads r, r + n_split, ...: the new token and the n_split partials
+  for (int j = warp; split + p.nsplit * j < G; j += 4) {
+    const int hh = split + p.nsplit * j;
     float sn = 0.0f;
 #pragma unroll
     for (int m = 0; m < NPL; ++m) sn += qt[hh][lane + 32 * m] * knew[lane + 32 * m];
     sn = warp_sum(sn);
     float M = sn;
-    for (int r = 0; r < p.nsplit; ++r) M = fmaxf(M, ld_dsmem_f32(cp_local + 4 * hh, r));
+    for (int r = 0; r < p.nsplit; ++r) M = fmaxf(M, inbox[(j * p.nsplit + r) * PW]);
     const float wn = exp2f(sn - M);
     float lsum = wn;
     float o[NPL];
 #pragma unroll
     for (int m = 0; m < NPL; ++m) o[m] = wn * vnew[lane + 32 * m];
     for (int r = 0; r < p.nsplit; ++r) {
-      const float ms = ld_dsmem_f32(cp_local + 4 * hh, r);
+      const float* part = inbox + (j * p.nsplit + r) * PW;
+      const float ms = part[0];
       if (ms == -INFINITY) continue;
       const float w = exp2f(ms - M);
-      lsum += w * ld_dsmem_f32(cp_local + 4 * (8 + hh), r);
+      lsum += w * part[1];
 #pragma unroll
-      for (int m = 0; m < NPL; ++m) o[m] += w * ld_dsmem_f32(cp_local + 4 * (16 + hh * D + lane + 32 * m), r);
+      for (int m = 0; m < NPL; ++m) o[m] += w * part[2 + lane + 32 * m];
     }
     const float inv = 1.0f / lsum;
 #pragma unroll
@@ -371,14 +394,21 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnParams p) {
     if (lane == 0) atomicAdd(p.s_o + (kbase / kWGroup) * 32 + b, so);
     if (bad) set_status(p.status, FT_DEV_RANGE);
   }
-  cluster_sync();  // keep this CTA's shared memory alive until every peer has read it
+  // no DSMEM access follows the last cluster barrier, so no CTA waits for its peers here
+}
+
+int attn_smem_bytes(int G, int nsplit, int d) {
+  cudaFuncAttributes fa = {};
+  const cudaError_t e = (d == 128) ? cudaFuncGetAttributes(&fa, attn_kernel<128>) : cudaFuncGetAttributes(&fa, attn_kernel<64>);
+  const int stat = (e == cudaSuccess) ? (int)fa.sharedSizeBytes : 8 * 1024;
+  return stat + attn_dyn_smem(G, nsplit, d);
 }
 
 cudaError_t launch_attn(const AttnParams& p, int head_dim, cudaStream_t st, bool pdl) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(p.B * p.nkv * p.nsplit));
   cfg.blockDim = dim3(128);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = attn_dyn_smem(p.G, p.nsplit, head_dim);
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;

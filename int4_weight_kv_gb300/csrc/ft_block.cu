@@ -3,6 +3,7 @@
 // attention, O, mid, gate/up, down) on the caller's stream, chained with
 // programmatic dependent launch so each projection's weight stream starts while
 // its predecessor finishes.
+#include <algorithm>
 #include <cmath>
 
 #include "ft_block.cuh"
@@ -113,8 +114,8 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepParams p) 
 }
 
 // h1 (complete after the O projection) -> gate/up operand + offsets, partial
-// sums of h1^2 (rho2 is formed and applied after the gate/up accumulation), and
-// the down accumulator <- h1.  Grid (parts, B).
+// sums of h1^2 (rho2 is formed and applied after the gate/up accumulation) and,
+// when the down projection splits sets, its accumulator <- h1.  Grid (parts, B).
 __global__ void __launch_bounds__(kPrepThreads) mid_kernel(const MidParams p) {
   griddep_launch();  // the gate/up kernel may start streaming its weights
   griddep_wait();
@@ -123,7 +124,7 @@ __global__ void __launch_bounds__(kPrepThreads) mid_kernel(const MidParams p) {
   const bool valid = ch < p.H / 8;
   float v[8];
   if (valid) load_chunk8(p.h1 + (size_t)b * p.H, FT_F32, ch, v);
-  const bool bad = row_part(v, valid, ch, b, p.out_acc == p.h1 ? nullptr : p.out_acc + (size_t)b * p.H,
+  const bool bad = row_part(v, valid, ch, b, p.out_acc ? p.out_acc + (size_t)b * p.H : nullptr,
                             p.h1_h + (size_t)b * p.H, p.s_h1, p.ssq + b * parts + part);
   if (bad) set_status(p.status, FT_DEV_RANGE);
 }
@@ -151,12 +152,19 @@ static WsPlan make_plan(const ft_block_cfg& c, int B, int max_ctx) {
   int sms = ft_host::num_sms();
   if (sms <= 0) sms = 148;
   const int nqkv = (c.n_q + 2 * c.n_kv) * c.head_dim;
-  const int bud = 200 * 1024;  // shared-memory budget of one GEMV CTA (ring + reduction area)
-  w.g[kRoleQKV] = make_gemv_plan(nqkv, c.hidden, B, sms, false, bud);
-  w.g[kRoleO] = make_gemv_plan(c.hidden, c.n_q * c.head_dim, B, sms, false, bud);
-  w.g[kRoleGU] = make_gemv_plan(2 * c.inter, c.hidden, B, sms, true, bud);
-  w.g[kRoleDown] = make_gemv_plan(c.hidden, c.inter, B, sms, false, bud);
   w.nsplit = attn_splits(B, c.n_kv, max_ctx, sms);
+  // shared-memory budget of one GEMV CTA (ring + reduction area); the QKV and O
+  // CTAs leave room for one attention CTA on their SM, so that attention CTAs
+  // start (and load their first K/V tiles) while QKV still runs, and O CTAs
+  // start (and fill their rings) while attention runs
+  const int bud = 200 * 1024;
+  const int per_sm = ft_host::smem_per_sm();
+  const int attn = attn_smem_bytes(c.n_q / c.n_kv, w.nsplit, c.head_dim);
+  const int bud_att = per_sm > 0 ? std::min(bud, per_sm - attn - 3 * 1024) : bud;
+  w.g[kRoleQKV] = make_gemv_plan(kRoleQKV, nqkv, c.hidden, B, sms, bud_att);
+  w.g[kRoleO] = make_gemv_plan(kRoleO, c.hidden, c.n_q * c.head_dim, B, sms, bud_att);
+  w.g[kRoleGU] = make_gemv_plan(kRoleGU, 2 * c.inter, c.hidden, B, sms, bud);
+  w.g[kRoleDown] = make_gemv_plan(kRoleDown, c.hidden, c.inter, B, sms, bud);
   size_t off = 0;
   auto take = [&](size_t bytes) {
     const size_t o = off;
@@ -177,10 +185,28 @@ static WsPlan make_plan(const ft_block_cfg& c, int B, int max_ctx) {
   w.ssq2 = take((size_t)B * w.parts * 4);
   w.a_h = take((size_t)B * c.inter * 2);
   w.s_a = take((size_t)(c.inter / 128) * 32 * 4);
-  w.out_acc = take((size_t)B * c.hidden * 4);
+  w.out_acc = w.g[kRoleDown].whole ? 0 : take((size_t)B * c.hidden * 4);
   w.tick = take((size_t)w.g[kRoleDown].NSET * 4);
   w.total = off;
   return w;
+}
+
+// inv_freq[i] = base^(-2i/d) (FP64) divided by 2 pi and scaled by 2^64: the
+// RoPE angle of position p is p * turn[i] turns, reduced modulo one turn by
+// unsigned 64-bit wrap-around.  Cached for the last (base, d) of this thread.
+static void rope_turns(float base, int d, uint64_t (&turn)[64]) {
+  thread_local float cb = -1.0f;
+  thread_local int cd = -1;
+  thread_local uint64_t ct[64];
+  if (cb != base || cd != d) {
+    for (int i = 0; i < 64; ++i) {
+      const double inv_freq = (i < d / 2) ? std::pow((double)base, -2.0 * i / d) : 0.0;
+      ct[i] = (uint64_t)std::ldexp(inv_freq / 6.283185307179586476925, 64);
+    }
+    cb = base;
+    cd = d;
+  }
+  for (int i = 0; i < 64; ++i) turn[i] = ct[i];
 }
 
 static bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
@@ -214,8 +240,6 @@ static int run_block(const ft_block_cfg* c, const ft_layer_weights* w, void* cac
   auto Hh = [&](size_t off) { return reinterpret_cast<__half*>(W + off); };
   const bool pdl = ft_host::pdl_enabled();
   const KVLayout L = kv_layout(*c, max_batch, max_ctx);
-  const bool f32_out = act_dtype == FT_F32;
-  float* down_acc = f32_out ? static_cast<float*>(x_out) : F(P.out_acc);
 
   if (mask & FT_STAGE_PREP) {
     PrepParams pp = {};
@@ -234,7 +258,7 @@ static int run_block(const ft_block_cfg* c, const ft_layer_weights* w, void* cac
     pp.s_a = F(P.s_a);
     pp.nkg_a = c->inter / 128;
     pp.tick = reinterpret_cast<uint32_t*>(W + P.tick);
-    pp.ntick = P.g[kRoleDown].NSET;
+    pp.ntick = P.g[kRoleDown].whole ? 0 : P.g[kRoleDown].NSET;
     pp.status = status;
     if (launch_ex(prep_kernel, dim3(P.parts, B), dim3(kPrepThreads), 0, st, pdl, pp) != cudaSuccess)
       return FT_ERR_CUDA;
@@ -260,10 +284,11 @@ static int run_block(const ft_block_cfg* c, const ft_layer_weights* w, void* cac
         g.eps = c->rms_eps;
         break;
       case kRoleDown:
-        g.out_f32 = down_acc;
+        // whole sets read the residual h1; split sets accumulate into a copy of it
+        g.out_f32 = P.g[kRoleDown].whole ? F(P.h1) : F(P.out_acc);
+        g.tick = reinterpret_cast<uint32_t*>(W + P.tick);
         g.out_final = x_out;
         g.out_dtype = act_dtype;
-        g.tick = reinterpret_cast<uint32_t*>(W + P.tick);
         break;
     }
     return launch_gemv(role, g, st, pdl);
@@ -294,8 +319,7 @@ static int run_block(const ft_block_cfg* c, const ft_layer_weights* w, void* cac
     a.o_h = Hh(P.o_h);
     a.s_o = F(P.s_o);
     a.status = status;
-    for (int i = 0; i < 64; ++i)
-      a.inv_freq[i] = (i < c->head_dim / 2) ? std::pow((double)c->rope_base, -2.0 * i / c->head_dim) : 0.0;
+    rope_turns(c->rope_base, c->head_dim, a.rope_turn);
     if (launch_attn(a, c->head_dim, st, pdl) != cudaSuccess) return FT_ERR_CUDA;
   }
   if (mask & FT_STAGE_O) {
@@ -309,7 +333,7 @@ static int run_block(const ft_block_cfg* c, const ft_layer_weights* w, void* cac
     mp.h1_h = Hh(P.h1_h);
     mp.s_h1 = F(P.s_h1);
     mp.ssq = F(P.ssq2);
-    mp.out_acc = down_acc;
+    mp.out_acc = P.g[kRoleDown].whole ? nullptr : F(P.out_acc);
     mp.status = status;
     if (launch_ex(mid_kernel, dim3(P.parts, B), dim3(kPrepThreads), 0, st, pdl, mp) != cudaSuccess)
       return FT_ERR_CUDA;

@@ -38,14 +38,14 @@ struct GemvParams {
   const __half* x;    // activation operand [B][K] (operand layout, see op_slot)
   const float* s_in;  // its group offsets [K/128][32]
   int B;
-  uint32_t* tick;     // DOWN: per-set tickets [NSET]
-  float* out_f32;     // QKV: qkv acc;  O: h1 acc;  DOWN: out acc (or the FP32 output)
+  uint32_t* tick;     // DOWN (split sets): per-set completion tickets [NSET]
+  float* out_f32;     // QKV: qkv acc;  O: h1 acc;  DOWN: h1 (whole sets) or its copy accumulating split sets
   __half* out_h;      // GU: a operand [B][I]
   float* s_out;       // GU: a's group offsets [I/128][32] (accumulated)
   const float* ssq2;  // GU: partial sums of h1^2 [B][nssq], giving the RMSNorm row factor rho2
   int nssq;
   float inv_h, eps;   // GU: 1 / hidden, RMSNorm epsilon
-  void* out_final;    // DOWN: block output
+  void* out_final;    // DOWN: block output (h1 + W_down a, BF16 or FP32)
   int out_dtype;
   int32_t* status;
 };
@@ -64,7 +64,7 @@ struct AttnParams {
   __half* o_h;        // [B][nq d] attention output (operand layout)
   float* s_o;         // its group offsets [nq d / 128][32] (accumulated)
   int32_t* status;
-  double inv_freq[64];
+  uint64_t rope_turn[64];  // inv_freq[i] / (2 pi) as 64-bit binary fractions (RoPE angles in turns)
 };
 
 // Block input -> QKV operand, partial sums of x^2, h1 accumulator initialised
@@ -83,13 +83,13 @@ struct PrepParams {
   int nkg_o;
   float* s_a;        // [NKG_a][32] <- 0 (column b)
   int nkg_a;
-  uint32_t* tick;    // down tickets <- 0
+  uint32_t* tick;    // down completion tickets <- 0 (split sets only)
   int ntick;
   int32_t* status;
 };
 
-// Between O and gate/up: h1 -> its operand and offsets, partial sums of h1^2,
-// and the down accumulator initialised to h1.  CTA (part, request) covers 512
+// Between O and gate/up: h1 -> its operand and offsets, partial sums of h1^2
+// and (split down sets) the down accumulator.  CTA (part, request) covers 512
 // inputs.
 struct MidParams {
   const float* h1;   // [B][H] complete after O
@@ -97,7 +97,7 @@ struct MidParams {
   __half* h1_h;      // [B][H] operand
   float* s_h1;       // [H/128][32]
   float* ssq;        // [B][parts] partial sums of h1^2
-  float* out_acc;    // [B][H] <- h1
+  float* out_acc;    // [B][H] <- h1 (down accumulator of split sets) or null
   int32_t* status;
 };
 
@@ -107,7 +107,16 @@ __host__ __device__ __forceinline__ int rms_parts(int H) { return (H / 8 + kPrep
 // host-side launchers (ft_gemv.cu / ft_attn.cu / ft_block.cu)
 cudaError_t launch_gemv(int role, const GemvParams& p, cudaStream_t st, bool pdl);
 cudaError_t launch_attn(const AttnParams& p, int head_dim, cudaStream_t st, bool pdl);
-GemvPlan make_gemv_plan(int N, int K, int B, int sms, bool whole_sets, int smem_budget);
+// Dynamic shared memory of one attention CTA: 4 warp partials of G heads and
+// the inbox of n_split * ceil(G / n_split) pushed partials, (d + 2) floats each.
+__host__ __device__ __forceinline__ int attn_dyn_smem(int G, int nsplit, int d) {
+  return (4 * G + nsplit * ((G + nsplit - 1) / nsplit)) * (d + 2) * 4;
+}
+// Static + dynamic shared memory of one attention CTA (host).
+int attn_smem_bytes(int G, int nsplit, int d);
+// Gate/up and down CTAs own whole row-tile sets; QKV and O split sets over
+// CTAs along K (partial sums red.add-ed into an FP32 accumulator).
+GemvPlan make_gemv_plan(int role, int N, int K, int B, int sms, int smem_budget);
 
 template <typename... Args>
 cudaError_t launch_ex(void (*kernel)(Args...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool pdl,

@@ -18,11 +18,13 @@
 //    with four logic ops and a shift per 8 weights (magic_word: the 1024-offset
 //    mantissa trick) and run through mma.m16n8k16 with FP32 accumulation; the
 //    offset is removed by starting each group's chain at -S (see ft_internal).
-//  * split-K: warps reduce through shared memory at the end of a row-tile set;
-//    across CTAs the partial sums are red.add-ed into an FP32 accumulator that
-//    the next kernel reads (QKV, O) or, for the BF16 down output, the last piece
-//    of a set (atomic ticket, never waits) converts it.  Gate/up CTAs own whole
-//    row-tile sets, so SwiGLU needs no cross-CTA step.
+//  * warps reduce through shared memory at the end of a row-tile set.  QKV and
+//    O split sets along K across CTAs and red.add the partial sums into an FP32
+//    accumulator that the next kernel reads.  Gate/up and down CTAs own whole
+//    row-tile sets, so SwiGLU and the block output (residual + BF16 rounding)
+//    are written directly, with no cross-CTA step.
+#include <algorithm>
+
 #include "ft_block.cuh"
 
 namespace ft {
@@ -35,6 +37,13 @@ template <> struct GemvShape<1> { static constexpr int RT = 4, NCW = 8; };
 template <> struct GemvShape<2> { static constexpr int RT = 4, NCW = 8; };
 template <> struct GemvShape<3> { static constexpr int RT = 4, NCW = 4; };
 template <> struct GemvShape<4> { static constexpr int RT = 4, NCW = 4; };
+// The down projection uses sets of two row tiles: fine enough that whole sets
+// (no split-K, output written directly with the residual added) balance over
+// the SMs for the 8B-class shapes; where whole sets would leave CTAs too
+// unequal (long K, many sets), it splits sets along K like QKV and O.
+constexpr int kDownRT = 2;
+template <int NT, int ROLE>
+constexpr int gemv_rt() { return ROLE == kRoleDown ? kDownRT : GemvShape<NT>::RT; }
 
 __device__ __forceinline__ void red_add(float* p, float v) { atomicAdd(p, v); }
 
@@ -119,7 +128,7 @@ struct StageWalk {
 
 template <int NT, int ROLE>
 __global__ void __launch_bounds__((GemvShape<NT>::NCW + 2) * 32, 1) gemv_kernel(const GemvParams p) {
-  constexpr int RT = GemvShape<NT>::RT, NCW = GemvShape<NT>::NCW;
+  constexpr int RT = gemv_rt<NT, ROLE>(), NCW = GemvShape<NT>::NCW;
   constexpr int PRODUCER = NCW, EPILOGUE = NCW + 1;
   extern __shared__ __align__(128) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -230,8 +239,9 @@ __global__ void __launch_bounds__((GemvShape<NT>::NCW + 2) * 32, 1) gemv_kernel(
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(red_empty);
-      if (ROLE == kRoleDown && !whole && p.out_dtype != FT_F32) {
-        // the last piece of this set converts the FP32 accumulator to BF16
+      if (ROLE == kRoleDown && !whole) {
+        // split set: the last of its pieces writes the block output from the
+        // h1 rows the pieces accumulated into (completion ticket, never waits)
         __threadfence();
         __syncwarp();
         const int first = plan_owner(pl, st.set * pl.NKG);
@@ -245,8 +255,10 @@ __global__ void __launch_bounds__((GemvShape<NT>::NCW + 2) * 32, 1) gemv_kernel(
           for (int i = lane; i < rows * p.B; i += 32) {
             const int t = i / rows, row = st.set * RT * kRowTile + i % rows;
             const float y = __ldcg(p.out_f32 + (size_t)t * pl.N + row);
-            static_cast<uint16_t*>(p.out_final)[(size_t)t * pl.N + row] =
-                __bfloat16_as_ushort(__float2bfloat16_rn(y));
+            if (p.out_dtype == FT_F32)
+              static_cast<float*>(p.out_final)[(size_t)t * pl.N + row] = y;
+            else
+              static_cast<uint16_t*>(p.out_final)[(size_t)t * pl.N + row] = __bfloat16_as_ushort(__float2bfloat16_rn(y));
           }
           if (lane == 0) p.tick[st.set] = 0u;
         }
@@ -431,22 +443,34 @@ static void shape_of(int NT, int& RT, int& NCW) {
   }
 }
 
-GemvPlan make_gemv_plan(int N, int K, int B, int sms, bool whole_sets, int smem_budget) {
+GemvPlan make_gemv_plan(int role, int N, int K, int B, int sms, int smem_budget) {
   GemvPlan p = {};
   p.N = N;
   p.K = K;
   p.NT = (B + 7) / 8;
   shape_of(p.NT, p.RT, p.NCW);
+  if (role == kRoleDown) p.RT = kDownRT;
   p.NTILE = N / kRowTile;
   p.NKG = K / kWGroup;
   p.NSET = (p.NTILE + p.RT - 1) / p.RT;
+  bool whole_sets = role == kRoleGU;
+  if (role == kRoleDown) {
+    // whole sets unless the busiest CTA would stream > 64 KB more weights than
+    // the average CTA of the split partition (the split costs a completion
+    // ticket round trip at the end of each split set)
+    const long units = (long)p.NSET * p.NKG;
+    const long c_split = std::min<long>(sms, units), c_whole = std::min<long>(sms, p.NSET);
+    const double avg = (double)units / (double)c_split;
+    const long max_whole = (p.NSET + c_whole - 1) / c_whole * (long)p.NKG;
+    whole_sets = ((double)max_whole - avg) * p.RT * kSlabBytes <= 64.0 * 1024.0;
+  }
   p.whole = whole_sets ? 1 : 0;
   const int units = whole_sets ? p.NSET : p.NSET * p.NKG;
   p.C = sms < units ? sms : units;
   if (p.C < 1) p.C = 1;
   p.per = units / p.C;
   p.rem = units % p.C;
-  p.ng = p.NCW;  // one group per consumer warp per stage
+  p.ng = p.NCW * 4 / p.RT;  // stages of 4 row tiles x NCW groups (a group per warp for RT = 4)
   if (p.ng > p.NKG) p.ng = p.NKG;
   p.xstride = p.ng * kWGroup * 2 + 16;
   const int wbytes = p.RT * p.ng * kSlabBytes;

@@ -127,14 +127,19 @@ __device__ __forceinline__ void mma_f16_zc(float (&d)[4], const uint32_t (&a)[4]
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-// Load a float from the shared memory of CTA `rank` of this cluster at the
-// offset of the local shared address `local`.
-__device__ __forceinline__ float ld_dsmem_f32(uint32_t local, uint32_t rank) {
+// Split cluster barrier: arrive early (no ordering), wait before the first
+// access to a peer's shared memory, which must have started executing.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
+// Store a float into the shared memory of CTA `rank` of this cluster at the
+// offset of the local shared address `local` (published by a later
+// cluster_sync()).
+__device__ __forceinline__ void st_dsmem_f32(uint32_t local, uint32_t rank, float v) {
   uint32_t remote;
-  float v;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(rank));
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
-  return v;
+  asm("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(rank));
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
 }
 
 __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
@@ -390,6 +395,7 @@ __device__ __forceinline__ void warp_quant_store(float (&v)[NPL], bool is_k, uin
 namespace ft_host {
 
 int num_sms();
+int smem_per_sm();  // shared memory per SM in bytes (0 if unknown)
 bool pdl_enabled();
 int check_cfg(const ft_block_cfg* c);
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
