@@ -17,11 +17,12 @@
 // scores (K) and the probabilities (V).  The n_split CTAs of one (b, h) form a
 // thread-block cluster.  CTA r merges heads r, r + n_split, ...: every CTA
 // pushes its (max, sum, acc) partial of each head into the merging CTA's shared
-// memory with distributed-shared-memory stores, one cluster barrier publishes
-// them, and the merger combines them from its own shared memory with the new
-// token, undoes the rotation and writes o.  The new token is quantised (and
-// written to the cache at L_b by CTA 0) and decoded by every merging CTA before
-// the main loop, while the first K/V tiles are in flight.
+// memory with asynchronous distributed-shared-memory stores that complete on
+// the merger's mbarrier (no cluster-wide barrier at the end), and the merger
+// combines them from its own shared memory with the new token, undoes the
+// rotation and writes o.  The new token's k and v are loaded before the main
+// loop and quantised (written to the cache at L_b by CTA 0) and decoded by the
+// merging CTAs while their peers' partials arrive.
 #include "ft_block.cuh"
 
 namespace ft {
@@ -101,10 +102,12 @@ template <int D>
 __global__ void __launch_bounds__(128) attn_kernel(const AttnParams p) {
   constexpr int NPL = D / 32;
   constexpr int KT = D / 16;  // k-tiles of q.K == m-tiles of P.V
-  constexpr int PW = D + 2;             // one partial: running max, sum, acc[D]
+  constexpr int PW = D + 4;             // one partial: running max, sum, 2 pad, acc[D] (16-byte rows)
   __shared__ float qt[8][D];            // rotated, scaled query (FP16 values)
   __shared__ float qoff[8];             // its operand offsets (magic-number decode)
   __shared__ float knew[D], vnew[D];
+  __shared__ float fac[8][5];           // per head: CTA max, then each warp's rescale factor
+  __shared__ __align__(8) uint64_t inbox_bar;  // completes when every partial of this CTA's heads arrived
   // dynamic: mrg[4][G * PW], each warp's partial of every head, then
   // inbox[n_split * ceil(G / n_split)][PW], the partials of the heads this CTA
   // merges, pushed by every CTA of the cluster (slot j * n_split + r holds CTA
@@ -131,7 +134,16 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnParams p) {
   const int t0 = split * tps, t1 = min(t0 + tps, ntiles);
   const int p1 = min(16 * t1, Lb);
 
-  cluster_arrive_relaxed();  // paired with cluster_wait() before the first DSMEM store
+  // heads this CTA merges: split, split + n_split, ...; the inbox barrier
+  // expects the partials of all n_split CTAs for each
+  int nloc = 0;
+  for (int hh = split; hh < G; hh += p.nsplit) ++nloc;
+  if (tid == 0) {
+    mbar_init(smem_u32(&inbox_bar), 1);
+    mbar_fence_init();
+    if (nloc) mbar_arrive_expect_tx(smem_u32(&inbox_bar), (uint32_t)(nloc * p.nsplit * PW * 4));
+  }
+  cluster_arrive();  // paired with cluster_wait() before the first push into a peer
 
   // history K/V do not depend on earlier kernels: start streaming now
   TileRegs<D> cur;
@@ -176,7 +188,7 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnParams p) {
   if (merger && warp < 2) {
     const float* src = p.qkv + (size_t)b * p.Nqkv + (size_t)(p.nq + warp * p.nkv + h) * D;
 #pragma unroll
-    for (int m = 0; m < NPL; ++m) kvraw[m] = __ldcg(src + lane + 32 * m);
+    for (int m = 0; m < NPL; ++m) kvraw[m] = ld_cg_early(src + lane + 32 * m);
   }
   __syncthreads();
   uint32_t bq[KT][2];
@@ -305,31 +317,39 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnParams p) {
 #pragma unroll
   for (int mt = 0; mt < KT; ++mt) {
     const int c0 = 16 * mt + g, c1 = c0 + 8;
-    if (c0ok) h0[2 + c0] = acc[mt][0], h0[2 + c1] = acc[mt][2];
-    if (c1ok) h1[2 + c0] = acc[mt][1], h1[2 + c1] = acc[mt][3];
+    if (c0ok) h0[4 + c0] = acc[mt][0], h0[4 + c1] = acc[mt][2];
+    if (c1ok) h1[4 + c0] = acc[mt][1], h1[4 + c1] = acc[mt][3];
+  }
+  __syncthreads();
+  if (tid < G) {  // per head: the CTA max and each warp's rescale factor
+    float mx[4], M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) M = fmaxf(M, mx[w] = mrg[(w * G + tid) * PW]);
+    fac[tid][0] = M;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) fac[tid][1 + w] = (mx[w] == -INFINITY) ? 0.0f : exp2f(mx[w] - M);
   }
   __syncthreads();
   // ---- this CTA's partial of every head, pushed into the inbox of the CTA that
-  // merges the head (DSMEM stores; the cluster barrier below publishes them)
+  // merges the head (asynchronous DSMEM stores completing on its inbox barrier)
   cluster_wait();  // every CTA of the cluster has started (arrived at entry)
   const uint32_t inbox0 = smem_u32(inbox);
-  for (int i = tid; i < G * PW; i += 128) {
-    const int hh = i / PW, e = i - hh * PW;
-    float M = -INFINITY;
-    for (int w = 0; w < 4; ++w) M = fmaxf(M, mrg[w * G * PW + hh * PW]);
-    float v;
-    if (e == 0) {
-      v = M;
-    } else {
-      v = 0.0f;
-      if (M != -INFINITY)
-        for (int w = 0; w < 4; ++w) {
-          const float mw2 = mrg[w * G * PW + hh * PW];
-          if (mw2 != -INFINITY) v += mrg[w * G * PW + i] * exp2f(mw2 - M);
-        }
+  constexpr int PW4 = PW / 4;
+  for (int i = tid; i < G * PW4; i += 128) {
+    const int hh = i / PW4, e4 = i - hh * PW4;
+    float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const float4 a = reinterpret_cast<const float4*>(mrg + (w * G + hh) * PW)[e4];
+      const float f = fac[hh][1 + w];
+      v.x = fmaf(a.x, f, v.x);
+      v.y = fmaf(a.y, f, v.y);
+      v.z = fmaf(a.z, f, v.z);
+      v.w = fmaf(a.w, f, v.w);
     }
+    if (e4 == 0) v = make_float4(fac[hh][0], v.y, 0.0f, 0.0f);  // (max, sum)
     const int slot = (hh / p.nsplit) * p.nsplit + split;
-    st_dsmem_f32(inbox0 + 4 * (slot * PW + e), (uint32_t)(hh % p.nsplit), v);
+    st_async_v4(inbox0 + 16 * (slot * PW4 + e4), smem_u32(&inbox_bar), (uint32_t)(hh % p.nsplit), v);
   }
 
   // ---- the new token (merging CTAs): RoPE on k, rotation, INT4 (cache write at
@@ -349,7 +369,12 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnParams p) {
 #pragma unroll
     for (int m = 0; m < NPL; ++m) dst[lane + 32 * m] = v[m];
   }
-  cluster_sync();  // every pushed partial is now in its merger's shared memory
+  if (nloc == 0) return;  // nothing to merge; nobody pushes into this CTA
+  __syncthreads();          // knew / vnew
+  if (!mbar_wait(smem_u32(&inbox_bar), 0)) {  // every partial of this CTA's heads has arrived
+    if (tid == 0) set_status(p.status, FT_DEV_TIMEOUT);
+    return;
+  }
 
   // ---- CTA r merges heads r, r + n_split, ...: the new token and the n_split partials
   for (int j = warp; split + p.nsplit * j < G; j += 4) {
@@ -372,7 +397,7 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnParams p) {
       const float w = exp2f(ms - M);
       lsum += w * part[1];
 #pragma unroll
-      for (int m = 0; m < NPL; ++m) o[m] += w * part[2 + lane + 32 * m];
+      for (int m = 0; m < NPL; ++m) o[m] += w * part[4 + lane + 32 * m];
     }
     const float inv = 1.0f / lsum;
 #pragma unroll
@@ -394,7 +419,6 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnParams p) {
     if (lane == 0) atomicAdd(p.s_o + (kbase / kWGroup) * 32 + b, so);
     if (bad) set_status(p.status, FT_DEV_RANGE);
   }
-  // no DSMEM access follows the last cluster barrier, so no CTA waits for its peers here
 }
 
 int attn_smem_bytes(int G, int nsplit, int d) {

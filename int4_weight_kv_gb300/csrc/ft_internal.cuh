@@ -78,6 +78,14 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       : "memory");
 }
 
+// L2 load issued where it stands (volatile: the compiler may not sink it to
+// its first use), for values fetched early and consumed much later.
+__device__ __forceinline__ float ld_cg_early(const float* p) {
+  float v;
+  asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p));
+  return v;
+}
+
 // Streamed read-once data (KV cache): skip L1.
 __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
   uint4 v;
@@ -122,24 +130,22 @@ __device__ __forceinline__ void mma_f16_zc(float (&d)[4], const uint32_t (&a)[4]
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(0.0f));
 }
 
-// Thread-block cluster barrier (all threads of every CTA of the cluster);
-// release/acquire make shared-memory writes visible across the cluster.
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// Split cluster barrier: arrive early (no ordering), wait before the first
-// access to a peer's shared memory, which must have started executing.
-__device__ __forceinline__ void cluster_arrive_relaxed() {
-  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
-}
+// Split cluster barrier: arrive (release) early, wait (acquire) before the
+// first access to a peer's shared memory, which must have started executing
+// and initialised what the access relies on.
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.aligned;" ::: "memory"); }
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
-// Store a float into the shared memory of CTA `rank` of this cluster at the
-// offset of the local shared address `local` (published by a later
-// cluster_sync()).
-__device__ __forceinline__ void st_dsmem_f32(uint32_t local, uint32_t rank, float v) {
-  uint32_t remote;
+// Asynchronous store of 4 floats into the shared memory of CTA `rank` of this
+// cluster, at the offset of the 16-byte aligned local shared address `local`;
+// its 16 bytes complete on that CTA's mbarrier at the offset of `local_bar`.
+__device__ __forceinline__ void st_async_v4(uint32_t local, uint32_t local_bar, uint32_t rank, float4 v) {
+  uint32_t remote, remote_bar;
   asm("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(rank));
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
+  asm("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote_bar) : "r"(local_bar), "r"(rank));
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                   remote),
+               "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(remote_bar)
+               : "memory");
 }
 
 __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
