@@ -23,6 +23,8 @@
 // rotation and writes o.  The new token's k and v are loaded before the main
 // loop and quantised (written to the cache at L_b by CTA 0) and decoded by the
 // merging CTAs while their peers' partials arrive.
+#include <atomic>
+
 #include "ft_block.cuh"
 
 namespace ft {
@@ -421,11 +423,38 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnParams p) {
   }
 }
 
+// Per-device caches of the kernel attributes the host plan needs (the queries
+// cost microseconds; every block call plans).  Benign races: equal values.
+static std::atomic<int> g_attn_static[64][2];
+static std::atomic<int> g_attn_occ[64][2][9];
+
 int attn_smem_bytes(int G, int nsplit, int d) {
-  cudaFuncAttributes fa = {};
-  const cudaError_t e = (d == 128) ? cudaFuncGetAttributes(&fa, attn_kernel<128>) : cudaFuncGetAttributes(&fa, attn_kernel<64>);
-  const int stat = (e == cudaSuccess) ? (int)fa.sharedSizeBytes : 8 * 1024;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
+  const int di = d == 128 ? 1 : 0;
+  int stat = g_attn_static[dev][di].load(std::memory_order_relaxed);
+  if (stat <= 0) {
+    cudaFuncAttributes fa = {};
+    const cudaError_t e =
+        di ? cudaFuncGetAttributes(&fa, attn_kernel<128>) : cudaFuncGetAttributes(&fa, attn_kernel<64>);
+    stat = (e == cudaSuccess) ? (int)fa.sharedSizeBytes : 8 * 1024;
+    if (e == cudaSuccess) g_attn_static[dev][di].store(stat, std::memory_order_relaxed);
+  }
   return stat + attn_dyn_smem(G, nsplit, d);
+}
+
+int attn_ctas_per_sm(int G, int d) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || G < 1 || G > 8) return 0;
+  const int di = d == 128 ? 1 : 0;
+  int n = g_attn_occ[dev][di][G].load(std::memory_order_relaxed);
+  if (n > 0) return n;
+  const size_t dyn = (size_t)attn_dyn_smem(G, 8, d);  // the largest inbox (8 splits)
+  const cudaError_t e = di ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_kernel<128>, 128, dyn)
+                           : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_kernel<64>, 128, dyn);
+  if (e != cudaSuccess) return 0;
+  g_attn_occ[dev][di][G].store(n, std::memory_order_relaxed);
+  return n;
 }
 
 cudaError_t launch_attn(const AttnParams& p, int head_dim, cudaStream_t st, bool pdl) {

@@ -136,10 +136,13 @@ struct WsPlan {
   size_t x_h, s_x, rho1, ssq1, h1, qkv, o_h, s_o, h1_h, s_h1, ssq2, a_h, s_a, out_acc, tick, total;
 };
 
-static int attn_splits(int B, int nkv, int max_ctx, int sms) {
+// Splits per (request, KV head): as many as keep every attention CTA resident in
+// one wave (a second, partial wave would double the kernel's time).
+static int attn_splits(int B, int nkv, int G, int d, int max_ctx, int sms) {
   const int pairs = B * nkv;
-  const int target = 4 * (sms > 0 ? sms : 148);
-  int ns = (target + pairs - 1) / pairs;
+  const int per_sm = attn_ctas_per_sm(G, d);
+  const int target = (per_sm > 0 ? per_sm : 4) * (sms > 0 ? sms : 148);
+  int ns = target / pairs;
   const int cap = (max_ctx + 63) / 64;
   if (ns > cap) ns = cap;
   if (ns > 8) ns = 8;  // the splits of one (request, KV head) form one portable cluster
@@ -152,7 +155,7 @@ static WsPlan make_plan(const ft_block_cfg& c, int B, int max_ctx) {
   int sms = ft_host::num_sms();
   if (sms <= 0) sms = 148;
   const int nqkv = (c.n_q + 2 * c.n_kv) * c.head_dim;
-  w.nsplit = attn_splits(B, c.n_kv, max_ctx, sms);
+  w.nsplit = attn_splits(B, c.n_kv, c.n_q / c.n_kv, c.head_dim, max_ctx, sms);
   // shared-memory budget of one GEMV CTA (ring + reduction area); the QKV and O
   // CTAs leave room for one attention CTA on their SM, so that attention CTAs
   // start (and load their first K/V tiles) while QKV still runs, and O CTAs
