@@ -20,6 +20,10 @@ struct GemvPlan {
   int ng;                      // groups per stage
   int stages, slot, xoff, soff, xstride;  // ring geometry (bytes)
   int redoff, zerooff, slotoff, smem;  // shared-memory map
+  // tile-split consumers (large batches): each consumer warp owns tpw of the
+  // set's RT = tpw * NCW row tiles over all of a stage's groups, so one stage
+  // of activations serves RT tiles (no cross-warp reduction)
+  int ts, tpw;
 };
 
 __host__ __device__ __forceinline__ int plan_u0(const GemvPlan& p, int c) {

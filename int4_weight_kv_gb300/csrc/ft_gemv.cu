@@ -126,6 +126,57 @@ struct StageWalk {
   }
 };
 
+// Producer warp: streams the CTA's (row-tile set, group) units stage by stage
+// into the ring, with the matching activation chunk and group offsets.  The
+// first `stages` stages of weights are issued before waiting on the previous
+// kernel (weights do not depend on it); their activation chunks right after.
+template <int RT>
+__device__ __forceinline__ void gemv_produce(const GemvParams& p, uint8_t* slots, uint32_t full0, uint32_t empty0,
+                                             int u0, int u1) {
+  const GemvPlan& pl = p.plan;
+  const int lane = threadIdx.x & 31;
+  const int S = pl.stages;
+  auto issue_x = [&](int slot, int kg, int ng) {
+    uint8_t* sb = slots + slot * pl.slot;
+    if (lane < p.B)
+      bulk_g2s(smem_u32(sb + pl.xoff) + lane * pl.xstride, p.x + (size_t)lane * pl.K + (size_t)kg * kWGroup,
+               ng * kWGroup * 2, full0 + 8 * slot);
+    if (lane == 31) bulk_g2s(smem_u32(sb + pl.soff), p.s_in + (size_t)kg * 32, ng * 128, full0 + 8 * slot);
+  };
+  bool waited = false;
+  int s = 0, slot = 0, round = 0;
+  for (StageWalk st(pl, u0, u1); st.valid(); st.next(), ++s) {
+    if (round > 0 && !mbar_wait(empty0 + 8 * slot, (round - 1) & 1)) {
+      set_status(p.status, FT_DEV_TIMEOUT);
+      break;
+    }
+    const int nrt = min(RT, pl.NTILE - st.set * RT);
+    if (lane == 0)
+      mbar_arrive_expect_tx(full0 + 8 * slot,
+                            (uint32_t)(nrt * st.ng * kSlabBytes + p.B * st.ng * kWGroup * 2 + st.ng * 128));
+    __syncwarp();
+    // one bulk copy per row tile, issued by lane rt (a single thread issuing them
+    // one after another limits the stage rate for wide sets)
+    const uint32_t sb = smem_u32(slots + slot * pl.slot);
+    for (int rt = lane; rt < nrt; rt += 32)
+      bulk_g2s(sb + rt * pl.ng * kSlabBytes, p.w + ((size_t)(st.set * RT + rt) * pl.NKG + st.kg) * kSlabBytes,
+               st.ng * kSlabBytes, full0 + 8 * slot);
+    __syncwarp();
+    if (waited) issue_x(slot, st.kg, st.ng);
+    if (!waited && (s == S - 1 || st.u + st.ng >= u1)) {
+      griddep_wait();  // the activation operand comes from the previous kernel
+      waited = true;
+      int ss = 0;
+      for (StageWalk s2(pl, u0, u1); ss <= s; s2.next(), ++ss) issue_x(ss, s2.kg, s2.ng);
+    }
+    if (++slot == S) {
+      slot = 0;
+      ++round;
+    }
+  }
+  if (!waited) griddep_wait();
+}
+
 template <int NT, int ROLE>
 __global__ void __launch_bounds__((GemvShape<NT>::NCW + 2) * 32, 1) gemv_kernel(const GemvParams p) {
   constexpr int RT = gemv_rt<NT, ROLE>(), NCW = GemvShape<NT>::NCW;
@@ -158,44 +209,7 @@ __global__ void __launch_bounds__((GemvShape<NT>::NCW + 2) * 32, 1) gemv_kernel(
   __syncthreads();
 
   if (warp == PRODUCER) {
-    // ------------------------------------------------------------ producer
-    auto issue_x = [&](int slot, int kg, int ng) {
-      uint8_t* sb = slots + slot * pl.slot;
-      if (lane < p.B)
-        bulk_g2s(smem_u32(sb + pl.xoff) + lane * pl.xstride, p.x + (size_t)lane * pl.K + (size_t)kg * kWGroup,
-                 ng * kWGroup * 2, full0 + 8 * slot);
-      if (lane == 31) bulk_g2s(smem_u32(sb + pl.soff), p.s_in + (size_t)kg * 32, ng * 128, full0 + 8 * slot);
-    };
-    bool waited = false;
-    int s = 0, slot = 0, round = 0;
-    for (StageWalk st(pl, u0, u1); st.valid(); st.next(), ++s) {
-      if (round > 0 && !mbar_wait(empty0 + 8 * slot, (round - 1) & 1)) {
-        set_status(p.status, FT_DEV_TIMEOUT);
-        break;
-      }
-      const int nrt = min(RT, pl.NTILE - st.set * RT);
-      if (lane == 0) {
-        mbar_arrive_expect_tx(full0 + 8 * slot,
-                              (uint32_t)(nrt * st.ng * kSlabBytes + p.B * st.ng * kWGroup * 2 + st.ng * 128));
-        const uint32_t sb = smem_u32(slots + slot * pl.slot);
-        for (int rt = 0; rt < nrt; ++rt)
-          bulk_g2s(sb + rt * pl.ng * kSlabBytes, p.w + ((size_t)(st.set * RT + rt) * pl.NKG + st.kg) * kSlabBytes,
-                   st.ng * kSlabBytes, full0 + 8 * slot);
-      }
-      __syncwarp();
-      if (waited) issue_x(slot, st.kg, st.ng);
-      if (!waited && (s == S - 1 || st.u + st.ng >= u1)) {
-        griddep_wait();  // the activation operand comes from the previous kernel
-        waited = true;
-        int ss = 0;
-        for (StageWalk s2(pl, u0, u1); ss <= s; s2.next(), ++ss) issue_x(ss, s2.kg, s2.ng);
-      }
-      if (++slot == S) {
-        slot = 0;
-        ++round;
-      }
-    }
-    if (!waited) griddep_wait();
+    gemv_produce<RT>(p, slots, full0, empty0, u0, u1);
     return;
   }
 
@@ -397,6 +411,238 @@ __global__ void __launch_bounds__((GemvShape<NT>::NCW + 2) * 32, 1) gemv_kernel(
   }
 }
 
+__device__ __forceinline__ void consumer_sync(int nthreads) {
+  asm volatile("bar.sync 2, %0;" ::"r"(nthreads) : "memory");
+}
+
+// Tile-split GEMV for large batches (three or four 8-token column tiles).  The
+// activation chunk of a stage (B x ng x 256 bytes) would otherwise outweigh its
+// weights several times over, re-read for every set of 4 row tiles; here a set
+// has RT = TPW * NCW row tiles and consumer warp w owns tiles w, w + NCW, ... for
+// every group of the stage, so each warp finishes its own sums and applies the
+// role epilogue itself.  Same ring, producer, partition and epilogues as
+// gemv_kernel; one MMA chain per (tile, column tile).
+template <int NT, int ROLE, int TPW, int NCW>
+__global__ void __launch_bounds__((NCW + 1) * 32, 1) gemv_ts_kernel(const GemvParams p) {
+  constexpr int RT = TPW * NCW, PRODUCER = NCW;
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const GemvPlan& pl = p.plan;
+  const int cta = blockIdx.x;
+  const int u0 = plan_u0(pl, cta), u1 = plan_u0(pl, cta + 1);
+  const int S = pl.stages;
+  const uint32_t full0 = smem_u32(smem), empty0 = full0 + 8 * S;
+  uint32_t* tick_bcast = reinterpret_cast<uint32_t*>(smem + pl.redoff);
+  uint8_t* zero_row = smem + pl.zerooff;
+  uint8_t* slots = smem + pl.slotoff;
+
+  griddep_launch();
+  for (int i = tid; i < pl.ng * kWGroup * 2 / 16; i += blockDim.x)
+    reinterpret_cast<uint4*>(zero_row)[i] = make_uint4(0u, 0u, 0u, 0u);
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, NCW);
+    }
+    mbar_fence_init();
+  }
+  __syncthreads();
+
+  if (warp == PRODUCER) {
+    gemv_produce<RT>(p, slots, full0, empty0, u0, u1);
+    return;
+  }
+
+  griddep_wait();
+  const int g = lane >> 2, tig = lane & 3;
+  float rho2_lane = 0.0f;
+  if (ROLE == kRoleGU && lane < p.B) {
+    float t = 0.0f;
+    for (int k = 0; k < p.nssq; ++k) t += __ldcg(p.ssq2 + lane * p.nssq + k);
+    rho2_lane = rsqrtf(t * p.inv_h + p.eps);
+  }
+  float tot[TPW][NT][4];
+#pragma unroll
+  for (int a = 0; a < TPW; ++a)
+#pragma unroll
+    for (int b = 0; b < NT; ++b)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) tot[a][b][r] = 0.0f;
+
+  bool bad = false;
+  int slot = 0, fphase = 0, piece_kg0 = -1;
+  for (StageWalk st(pl, u0, u1); st.valid(); st.next()) {
+    if (piece_kg0 < 0) piece_kg0 = st.kg;
+    if (!mbar_wait(full0 + 8 * slot, fphase)) {
+      set_status(p.status, FT_DEV_TIMEOUT);
+      return;
+    }
+    const uint8_t* sw = slots + slot * pl.slot;
+    const float* ss = reinterpret_cast<const float*>(sw + pl.soff);
+    const int nrt = min(RT, pl.NTILE - st.set * RT);
+    for (int kgl = 0; kgl < st.ng; ++kgl) {
+      const uint8_t* xr[NT];
+      float c0[NT][2];
+#pragma unroll
+      for (int j = 0; j < NT; ++j) {
+        const int row = 8 * j + g, t = 8 * j + 2 * tig;
+        xr[j] = (row < p.B ? sw + pl.xoff + row * pl.xstride : zero_row) + (kgl * kWGroup + 4 * tig) * 2;
+        const float2 sv = *reinterpret_cast<const float2*>(ss + kgl * 32 + t);
+        c0[j][0] = (t < p.B) ? -sv.x : 0.0f;
+        c0[j][1] = (t + 1 < p.B) ? -sv.y : 0.0f;
+      }
+      uint32_t sc[TPW];
+      float acc[TPW][NT][4];
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t wd[TPW][4];
+#pragma unroll
+        for (int t = 0; t < TPW; ++t) {
+          const int rt = warp + t * NCW;
+          if (rt < nrt) {
+            const uint8_t* slab = sw + (rt * pl.ng + kgl) * kSlabBytes;
+            const uint4 q = *reinterpret_cast<const uint4*>(slab + half * 512 + lane * 16);
+            wd[t][0] = q.x; wd[t][1] = q.y; wd[t][2] = q.z; wd[t][3] = q.w;
+            if (half == 0) sc[t] = *reinterpret_cast<const uint32_t*>(slab + kSlabCodes + 4 * g);
+          }
+        }
+#pragma unroll
+        for (int kq = 0; kq < 4; ++kq) {
+          const int ks = 4 * half + kq;
+          uint32_t b0[NT], b1[NT];
+#pragma unroll
+          for (int j = 0; j < NT; ++j) {
+            const uint2 bv = *reinterpret_cast<const uint2*>(xr[j] + ks * 32);
+            b0[j] = bv.x;
+            b1[j] = bv.y;
+          }
+#pragma unroll
+          for (int t = 0; t < TPW; ++t) {
+            if (warp + t * NCW >= nrt) continue;  // warp-uniform: tiles past a short last set
+            uint32_t r[4];
+            magic_word(wd[t][kq], r);
+            const uint32_t a[4] = {r[0], r[2], r[1], r[3]};
+#pragma unroll
+            for (int j = 0; j < NT; ++j) {
+              if (ks == 0) {
+                float* d = acc[t][j];
+                d[0] = c0[j][0]; d[1] = c0[j][1]; d[2] = c0[j][0]; d[3] = c0[j][1];
+              }
+              mma_f16(acc[t][j], a, b0[j], b1[j]);
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < TPW; ++t) {
+        if (warp + t * NCW >= nrt) continue;
+        const float slo = bf16_bits_to_f32((uint16_t)(sc[t] & 0xFFFFu));
+        const float shi = bf16_bits_to_f32((uint16_t)(sc[t] >> 16));
+#pragma unroll
+        for (int j = 0; j < NT; ++j)
+#pragma unroll
+          for (int r = 0; r < 4; ++r) tot[t][j][r] = fmaf((r & 2) ? shi : slo, acc[t][j][r], tot[t][j][r]);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty0 + 8 * slot);
+    if (++slot == S) {
+      slot = 0;
+      fphase ^= 1;
+    }
+
+    if (st.piece_end()) {
+      const bool whole = (piece_kg0 == 0) && (st.kg + st.ng == pl.NKG);
+      piece_kg0 = -1;
+#pragma unroll
+      for (int t = 0; t < TPW; ++t) {
+        const int rt = warp + t * NCW;
+        if (rt < nrt) {
+#pragma unroll
+          for (int j = 0; j < NT; ++j) bad |= gemv_epi<ROLE>(p, st.set * RT + rt, j, tot[t][j], whole, rho2_lane);
+        }
+#pragma unroll
+        for (int j = 0; j < NT; ++j)
+#pragma unroll
+          for (int r = 0; r < 4; ++r) tot[t][j][r] = 0.0f;
+      }
+      if (ROLE == kRoleDown && !whole) {
+        // split set: every warp's red.adds of this piece are done before the
+        // ticket; the last piece writes the block output from the accumulator
+        __threadfence();
+        consumer_sync(NCW * 32);
+        if (tid == 0) {
+          const int first = plan_owner(pl, st.set * pl.NKG);
+          const int np = plan_owner(pl, st.set * pl.NKG + pl.NKG - 1) - first + 1;
+          *tick_bcast = (atomicAdd(p.tick + st.set, 1u) == (uint32_t)(np - 1)) ? 1u : 0u;
+        }
+        consumer_sync(NCW * 32);
+        if (*tick_bcast) {
+          __threadfence();
+          const int rows = nrt * kRowTile;
+          for (int i = tid; i < rows * p.B; i += NCW * 32) {
+            const int t = i / rows, row = st.set * RT * kRowTile + i % rows;
+            const float y = __ldcg(p.out_f32 + (size_t)t * pl.N + row);
+            if (p.out_dtype == FT_F32)
+              static_cast<float*>(p.out_final)[(size_t)t * pl.N + row] = y;
+            else
+              static_cast<uint16_t*>(p.out_final)[(size_t)t * pl.N + row] =
+                  __bfloat16_as_ushort(__float2bfloat16_rn(y));
+          }
+          if (tid == 0) p.tick[st.set] = 0u;
+        }
+        consumer_sync(NCW * 32);  // the broadcast word is reused by the next piece
+      }
+    }
+  }
+  if (bad) set_status(p.status, FT_DEV_RANGE);
+}
+
+template <int NT, int ROLE, int TPW, int NCW>
+static cudaError_t launch_ts_one(const GemvParams& p, cudaStream_t st, bool pdl) {
+  static int attr_smem[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (attr_smem[dev] < p.plan.smem) {
+    cudaError_t e = cudaFuncSetAttribute(gemv_ts_kernel<NT, ROLE, TPW, NCW>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, p.plan.smem);
+    if (e != cudaSuccess) return e;
+    attr_smem[dev] = p.plan.smem;
+  }
+  return launch_ex(gemv_ts_kernel<NT, ROLE, TPW, NCW>, dim3(p.plan.C), dim3((NCW + 1) * 32), (size_t)p.plan.smem,
+                   st, pdl, p);
+}
+
+// Tile-split shapes: gate/up (whole sets, SwiGLU in the epilogue) uses 6 warps and
+// 1-4 tiles per warp so that sets number about one per SM; the split-K roles use
+// 8 warps x 2 tiles (256 rows per set).
+constexpr int kTsNcwGU = 6, kTsNcw = 8, kTsTpw = 2;
+
+template <int NT, int ROLE>
+static cudaError_t launch_ts_nt(const GemvParams& p, cudaStream_t st, bool pdl) {
+  if constexpr (ROLE == kRoleGU) {
+    switch (p.plan.tpw) {
+      case 1: return launch_ts_one<NT, ROLE, 1, kTsNcwGU>(p, st, pdl);
+      case 2: return launch_ts_one<NT, ROLE, 2, kTsNcwGU>(p, st, pdl);
+      case 3: return launch_ts_one<NT, ROLE, 3, kTsNcwGU>(p, st, pdl);
+      case 4: return launch_ts_one<NT, ROLE, 4, kTsNcwGU>(p, st, pdl);
+      default: return cudaErrorInvalidValue;
+    }
+  } else {
+    return launch_ts_one<NT, ROLE, kTsTpw, kTsNcw>(p, st, pdl);
+  }
+}
+
+template <int ROLE>
+static cudaError_t launch_ts(const GemvParams& p, cudaStream_t st, bool pdl) {
+  switch (p.plan.NT) {
+    case 3: return launch_ts_nt<3, ROLE>(p, st, pdl);
+    case 4: return launch_ts_nt<4, ROLE>(p, st, pdl);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 template <int NT, int ROLE>
 static cudaError_t launch_one(const GemvParams& p, cudaStream_t st, bool pdl) {
   constexpr int THREADS = (GemvShape<NT>::NCW + 2) * 32;
@@ -425,6 +671,15 @@ static cudaError_t launch_role(const GemvParams& p, cudaStream_t st, bool pdl) {
 }
 
 cudaError_t launch_gemv(int role, const GemvParams& p, cudaStream_t st, bool pdl) {
+  if (p.plan.ts) {
+    switch (role) {
+      case kRoleQKV: return launch_ts<kRoleQKV>(p, st, pdl);
+      case kRoleO: return launch_ts<kRoleO>(p, st, pdl);
+      case kRoleGU: return launch_ts<kRoleGU>(p, st, pdl);
+      case kRoleDown: return launch_ts<kRoleDown>(p, st, pdl);
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (role) {
     case kRoleQKV: return launch_role<kRoleQKV>(p, st, pdl);
     case kRoleO: return launch_role<kRoleO>(p, st, pdl);
@@ -450,6 +705,17 @@ GemvPlan make_gemv_plan(int role, int N, int K, int B, int sms, int smem_budget)
   p.NT = (B + 7) / 8;
   shape_of(p.NT, p.RT, p.NCW);
   if (role == kRoleDown) p.RT = kDownRT;
+  p.ts = p.NT >= 3 ? 1 : 0;
+  if (p.ts) {
+    p.NCW = role == kRoleGU ? kTsNcwGU : kTsNcw;
+    if (role == kRoleGU) {  // about one whole set per SM
+      const int per = (N / kRowTile + sms * p.NCW - 1) / (sms * p.NCW);
+      p.tpw = std::max(1, std::min(4, per));
+    } else {
+      p.tpw = kTsTpw;
+    }
+    p.RT = p.tpw * p.NCW;
+  }
   p.NTILE = N / kRowTile;
   p.NKG = K / kWGroup;
   p.NSET = (p.NTILE + p.RT - 1) / p.RT;
@@ -471,6 +737,10 @@ GemvPlan make_gemv_plan(int role, int N, int K, int B, int sms, int smem_budget)
   p.per = units / p.C;
   p.rem = units % p.C;
   p.ng = p.NCW * 4 / p.RT;  // stages of 4 row tiles x NCW groups (a group per warp for RT = 4)
+  if (p.ts) {  // stages of about 48 KB (weights of RT tiles + B activation rows per group)
+    const int per_group = p.RT * kSlabBytes + B * kWGroup * 2 + 128;
+    p.ng = std::max(1, 48 * 1024 / per_group);
+  }
   if (p.ng > p.NKG) p.ng = p.NKG;
   p.xstride = p.ng * kWGroup * 2 + 16;
   const int wbytes = p.RT * p.ng * kSlabBytes;
@@ -478,7 +748,7 @@ GemvPlan make_gemv_plan(int role, int N, int K, int B, int sms, int smem_budget)
   p.soff = (int)align_up((size_t)p.xoff + (size_t)B * p.xstride, 16);
   p.slot = (int)align_up((size_t)p.soff + (size_t)p.ng * 128, 128);
   p.redoff = 256;
-  const int redbytes = p.NCW * p.RT * p.NT * 128 * 4;
+  const int redbytes = p.ts ? 128 : p.NCW * p.RT * p.NT * 128 * 4;  // tile-split: the ticket word
   p.zerooff = (int)align_up((size_t)p.redoff + (size_t)redbytes, 128);
   p.slotoff = (int)align_up((size_t)p.zerooff + (size_t)p.ng * kWGroup * 2, 128);
   int stages = (smem_budget - p.slotoff) / p.slot;
