@@ -184,11 +184,14 @@ int ft_decode_block_stages(const ft_block_cfg *cfg, const ft_layer_weights *w, v
 
 /* Byte offsets of intermediate tensors inside the workspace (host struct out),
  * for tests:  qkv FP32 [B, (n_q+2n_kv) d] (the projection before rho1 and
- * RoPE);  rho1 FP32 [B];  o FP16 [B, n_q d] (attention output after the
- * inverse rotation);  h1 FP32 [B, H];  a FP16 [B, I] (SwiGLU output).
- * o and a are stored in the projections' operand layout: within every 16
- * consecutive inputs the order is 0,1,8,9,2,3,10,11,4,5,12,13,6,7,14,15 and
- * inputs 8..15 hold value / 16. */
+ * RoPE);  rho1 FP32 [B];  o FP16, n_q d values per request (attention output
+ * after the inverse rotation);  h1 FP32 [B, H];  a FP16, I values per request
+ * (SwiGLU output).  o and a are stored in the projections' grouped operand
+ * layout: [inputs / 128][B][128], i.e. the B requests' values of each group of
+ * 128 inputs together; within a request's 128 values the order is
+ * 0,1,8,9,2,3,10,11,4,5,12,13,6,7,14,15 per 16 inputs, inputs 8..15 of each 16
+ * hold value / 16, and the 16 runs of 8 stored values are permuted: run r is
+ * stored at position r XOR (request mod 8). */
 typedef struct {
   size_t qkv, rho1, o, h1, a;
   int32_t n_split; /* split-KV chunks per (request, KV head) */

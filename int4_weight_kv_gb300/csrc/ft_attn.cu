@@ -406,7 +406,6 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnParams p) {
     for (int m = 0; m < NPL; ++m) o[m] *= inv;
     warp_fwht<NPL>(o, p.hb);
     const int kbase = (h * G + hh) * D;  // input index of channel 0 of this head in the O projection
-    __half* dst = p.o_h + (size_t)b * p.nq * D;
     bool bad = false;
     float so = 0.0f;
 #pragma unroll
@@ -414,7 +413,7 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnParams p) {
       const int k = kbase + lane + 32 * m;
       bad |= !(fabsf(o[m]) <= 65504.0f);
       float st;
-      dst[op_slot(k)] = op_encode(o[m], k, st);
+      p.o_h[op_index(b, k, p.B)] = op_encode(o[m], k, st);
       so += st;
     }
     so = warp_sum(so);  // a head (d <= 128 channels) lies inside one 128-input group

@@ -10,18 +10,18 @@
 
 namespace ft {
 
-// Encodes 8 consecutive inputs 8 ch .. 8 ch + 7 of one row into the operand
-// layout (op_slot) and returns their contribution to the group offset S.
-__device__ __forceinline__ float encode_chunk8(const float (&v)[8], int ch, __half* row) {
-  const bool high = (ch & 1) != 0;
-  const int base = (ch >> 1) * 16 + (high ? 2 : 0);
+// Encodes 8 consecutive inputs 8 ch .. 8 ch + 7 of row t into the grouped
+// operand buffer `op` of B rows (op_index) and returns their contribution to the
+// group offset S.
+__device__ __forceinline__ float encode_chunk8(const float (&v)[8], int ch, int t, int B, __half* op) {
   float s = 0.0f;
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     float s0, s1;
-    const __half h0 = op_encode(v[2 * i], 8 * ch + 2 * i, s0);
-    const __half h1 = op_encode(v[2 * i + 1], 8 * ch + 2 * i + 1, s1);
-    *reinterpret_cast<__half2*>(row + base + 4 * i) = __halves2half2(h0, h1);
+    const int k = 8 * ch + 2 * i;  // k and k + 1 share one 8-value chunk of the row
+    const __half h0 = op_encode(v[2 * i], k, s0);
+    const __half h1 = op_encode(v[2 * i + 1], k + 1, s1);
+    *reinterpret_cast<__half2*>(op + op_index(t, k, B)) = __halves2half2(h0, h1);
     s += s0 + s1;
   }
   return s;
@@ -56,8 +56,8 @@ __device__ __forceinline__ void load_chunk8(const void* row, int dtype, int ch, 
 // One row part: chunk ch of the row -> FP32 copy, FP16 operand + group offsets,
 // and the part's sum of squares (written by thread 0).  kPrepThreads threads,
 // one chunk each; a part is a whole number of 128-input groups.
-__device__ __forceinline__ bool row_part(const float (&v)[8], bool valid, int ch, int b, float* copy, __half* op,
-                                         float* s_grp, float* ssq_out) {
+__device__ __forceinline__ bool row_part(const float (&v)[8], bool valid, int ch, int b, int B, float* copy,
+                                         __half* op, float* s_grp, float* ssq_out) {
   __shared__ float red[kPrepThreads / 32];
   float ss = 0.0f, sterm = 0.0f;
   bool bad = false;
@@ -72,7 +72,7 @@ __device__ __forceinline__ bool row_part(const float (&v)[8], bool valid, int ch
       dst[0] = make_float4(v[0], v[1], v[2], v[3]);
       dst[1] = make_float4(v[4], v[5], v[6], v[7]);
     }
-    sterm = encode_chunk8(v, ch, op);
+    sterm = encode_chunk8(v, ch, b, B, op);
   }
   // warps stay converged: a group is 16 chunks and parts start on group boundaries
   const float gs = group16_sum(sterm);
@@ -108,8 +108,7 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepParams p) 
   float v[8];
   const size_t esz = p.act_dtype == FT_F32 ? 4 : 2;
   if (valid) load_chunk8(static_cast<const uint8_t*>(p.x_in) + (size_t)b * p.H * esz, p.act_dtype, ch, v);
-  const bool bad = row_part(v, valid, ch, b, p.h1 + (size_t)b * p.H, p.x_h + (size_t)b * p.H, p.s_x,
-                            p.ssq + b * parts + part);
+  const bool bad = row_part(v, valid, ch, b, p.B, p.h1 + (size_t)b * p.H, p.x_h, p.s_x, p.ssq + b * parts + part);
   if (bad) set_status(p.status, FT_DEV_RANGE);
 }
 
@@ -124,8 +123,8 @@ __global__ void __launch_bounds__(kPrepThreads) mid_kernel(const MidParams p) {
   const bool valid = ch < p.H / 8;
   float v[8];
   if (valid) load_chunk8(p.h1 + (size_t)b * p.H, FT_F32, ch, v);
-  const bool bad = row_part(v, valid, ch, b, p.out_acc ? p.out_acc + (size_t)b * p.H : nullptr,
-                            p.h1_h + (size_t)b * p.H, p.s_h1, p.ssq + b * parts + part);
+  const bool bad = row_part(v, valid, ch, b, p.B, p.out_acc ? p.out_acc + (size_t)b * p.H : nullptr, p.h1_h, p.s_h1,
+                            p.ssq + b * parts + part);
   if (bad) set_status(p.status, FT_DEV_RANGE);
 }
 

@@ -39,7 +39,7 @@ __host__ __device__ __forceinline__ int plan_owner(const GemvPlan& p, int u) {
 struct GemvParams {
   GemvPlan plan;
   const uint8_t* w;   // packed weights of this role
-  const __half* x;    // activation operand [B][K] (operand layout, see op_slot)
+  const __half* x;    // activation operand, grouped layout of B rows (op_index)
   const float* s_in;  // its group offsets [K/128][32]
   int B;
   uint32_t* tick;     // DOWN (split sets): per-set completion tickets [NSET]
@@ -65,7 +65,7 @@ struct AttnParams {
   const int32_t* pos;
   int B, nq, nkv, G, hb, nsplit, Nqkv;
   float qscale;       // log2(e) / sqrt(d), folded into the rotated query
-  __half* o_h;        // [B][nq d] attention output (operand layout)
+  __half* o_h;        // attention output, grouped operand layout of B rows (op_index)
   float* s_o;         // its group offsets [nq d / 128][32] (accumulated)
   int32_t* status;
   uint64_t rope_turn[64];  // inv_freq[i] / (2 pi) as 64-bit binary fractions (RoPE angles in turns)
@@ -77,7 +77,7 @@ struct AttnParams {
 struct PrepParams {
   const void* x_in;
   int act_dtype, B, H;
-  __half* x_h;       // [B][H] operand
+  __half* x_h;       // operand, grouped layout (op_index)
   float* s_x;        // [H/128][32]
   float* ssq;        // [B][parts] partial sums of x^2
   float* h1;         // [B][H] <- x
@@ -98,7 +98,7 @@ struct PrepParams {
 struct MidParams {
   const float* h1;   // [B][H] complete after O
   int B, H;
-  __half* h1_h;      // [B][H] operand
+  __half* h1_h;      // operand, grouped layout (op_index)
   float* s_h1;       // [H/128][32]
   float* ssq;        // [B][parts] partial sums of h1^2
   float* out_acc;    // [B][H] <- h1 (down accumulator of split sets) or null

@@ -70,7 +70,7 @@ __device__ __forceinline__ bool gemv_epi(const GemvParams& p, int T, int j, cons
         const float gv = rho2 * v[e], uv = rho2 * v[2 + e];
         const float a = gv / (1.0f + expf(-gv)) * uv;
         bad |= !(fabsf(a) <= 65504.0f);
-        p.out_h[(size_t)t * inter + op_slot(kcol)] = op_encode(a, kcol, st);
+        p.out_h[op_index(t, kcol, p.B)] = op_encode(a, kcol, st);
       }
       st += __shfl_xor_sync(0xffffffffu, st, 4);
       st += __shfl_xor_sync(0xffffffffu, st, 8);
@@ -138,9 +138,9 @@ __device__ __forceinline__ void gemv_produce(const GemvParams& p, uint8_t* slots
   const int S = pl.stages;
   auto issue_x = [&](int slot, int kg, int ng) {
     uint8_t* sb = slots + slot * pl.slot;
-    if (lane < p.B)
-      bulk_g2s(smem_u32(sb + pl.xoff) + lane * pl.xstride, p.x + (size_t)lane * pl.K + (size_t)kg * kWGroup,
-               ng * kWGroup * 2, full0 + 8 * slot);
+    // the B rows of groups kg .. kg + ng - 1 are contiguous in the grouped layout
+    if (lane == 0)
+      bulk_g2s(smem_u32(sb + pl.xoff), p.x + (size_t)kg * p.B * kWGroup, p.B * ng * kWGroup * 2, full0 + 8 * slot);
     if (lane == 31) bulk_g2s(smem_u32(sb + pl.soff), p.s_in + (size_t)kg * 32, ng * 128, full0 + 8 * slot);
   };
   bool waited = false;
@@ -312,7 +312,8 @@ __global__ void __launch_bounds__((GemvShape<NT>::NCW + 2) * 32, 1) gemv_kernel(
 #pragma unroll
       for (int j = 0; j < NT; ++j) {
         const int row = 8 * j + g, t = 8 * j + 2 * tig;
-        xr[j] = (row < p.B ? sw + pl.xoff + row * pl.xstride : zero_row) + (kgl * kWGroup + 4 * tig) * 2;
+        // row `row` of group kgl in the stage's grouped rows; absent tokens read zeros
+        xr[j] = row < p.B ? sw + pl.xoff + (kgl * p.B + row) * (kWGroup * 2) : zero_row + kgl * (kWGroup * 2);
         const float2 sv = *reinterpret_cast<const float2*>(ss + kgl * 32 + t);
         c0[j][0] = (t < p.B) ? -sv.x : 0.0f;
         c0[j][1] = (t + 1 < p.B) ? -sv.y : 0.0f;
@@ -340,7 +341,7 @@ __global__ void __launch_bounds__((GemvShape<NT>::NCW + 2) * 32, 1) gemv_kernel(
           uint32_t b0[NT], b1[NT];
 #pragma unroll
           for (int j = 0; j < NT; ++j) {
-            const uint2 bv = *reinterpret_cast<const uint2*>(xr[j] + ks * 32);
+            const uint2 bv = *reinterpret_cast<const uint2*>(xr[j] + op_frag_off(ks, tig, g));
             b0[j] = bv.x;
             b1[j] = bv.y;
           }
@@ -486,7 +487,8 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) gemv_ts_kernel(const GemvPa
 #pragma unroll
       for (int j = 0; j < NT; ++j) {
         const int row = 8 * j + g, t = 8 * j + 2 * tig;
-        xr[j] = (row < p.B ? sw + pl.xoff + row * pl.xstride : zero_row) + (kgl * kWGroup + 4 * tig) * 2;
+        // row `row` of group kgl in the stage's grouped rows; absent tokens read zeros
+        xr[j] = row < p.B ? sw + pl.xoff + (kgl * p.B + row) * (kWGroup * 2) : zero_row + kgl * (kWGroup * 2);
         const float2 sv = *reinterpret_cast<const float2*>(ss + kgl * 32 + t);
         c0[j][0] = (t < p.B) ? -sv.x : 0.0f;
         c0[j][1] = (t + 1 < p.B) ? -sv.y : 0.0f;
@@ -512,7 +514,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) gemv_ts_kernel(const GemvPa
           uint32_t b0[NT], b1[NT];
 #pragma unroll
           for (int j = 0; j < NT; ++j) {
-            const uint2 bv = *reinterpret_cast<const uint2*>(xr[j] + ks * 32);
+            const uint2 bv = *reinterpret_cast<const uint2*>(xr[j] + op_frag_off(ks, tig, g));
             b0[j] = bv.x;
             b1[j] = bv.y;
           }
@@ -742,7 +744,7 @@ GemvPlan make_gemv_plan(int role, int N, int K, int B, int sms, int smem_budget)
     p.ng = std::max(1, 48 * 1024 / per_group);
   }
   if (p.ng > p.NKG) p.ng = p.NKG;
-  p.xstride = p.ng * kWGroup * 2 + 16;
+  p.xstride = p.ng * kWGroup * 2;  // bytes of one token row of a stage (grouped rows, no padding)
   const int wbytes = p.RT * p.ng * kSlabBytes;
   p.xoff = (int)align_up((size_t)wbytes, 16);
   p.soff = (int)align_up((size_t)p.xoff + (size_t)B * p.xstride, 16);

@@ -227,6 +227,21 @@ __host__ __device__ __forceinline__ int op_slot(int k) {
   return base + ((c < 8) ? (4 * (c >> 1) + (c & 1)) : (4 * ((c - 8) >> 1) + 2 + (c & 1)));
 }
 __host__ __device__ __forceinline__ bool op_high(int k) { return (k & 15) >= 8; }
+// Grouped operand buffer of B rows: the B rows' values of each 128-input group
+// are stored together ([K/128][B][128] FP16), so a stage of consecutive groups is
+// one contiguous copy; within a row the 16 chunks of 8 values (op_slot order)
+// are XOR-permuted by (row & 7), so the B-fragment loads of 8 rows hit
+// different shared-memory banks.  op_index(t, k, B) is the element index of
+// input k of row t.
+__host__ __device__ __forceinline__ int op_index(int t, int k, int B) {
+  const int p = op_slot(k & 127);
+  return ((k >> 7) * B + t) * 128 + (((p >> 3) ^ (t & 7)) << 3) + (p & 7);
+}
+// Byte offset, within a group row of the grouped layout, of lane tig's 8-byte
+// B fragment of k-step ks for a row whose (row & 7) is `key`.
+__device__ __forceinline__ int op_frag_off(int ks, int tig, int key) {
+  return ((((2 * ks) + (tig >> 1)) ^ key) << 4) + ((tig & 1) << 3);
+}
 // FP16 operand value of input k and its contribution to the group offset S.
 __device__ __forceinline__ __half op_encode(float x, int k, float& s_term) {
   const __half h = __float2half_rn(op_high(k) ? x * 0.0625f : x);

@@ -106,9 +106,9 @@ def run_gpu(pb: Problem, act_dtype=ft.FT_F32, cache: Optional[torch.Tensor] = No
         return ws[off:off + nbytes].view(dt).cpu().numpy()
     rho1 = view(lay.rho1, B, torch.float32)
     qkv = view(lay.qkv, B * s.n_qkv, torch.float32).reshape(B, s.n_qkv) * rho1[:, None]
-    o = operand_decode(view(lay.o, B * s.n_q * s.head_dim, torch.float16).reshape(B, -1))
+    o = operand_decode(view(lay.o, B * s.n_q * s.head_dim, torch.float16), B)
     h1 = view(lay.h1, B * H, torch.float32).reshape(B, H)
-    a = operand_decode(view(lay.a, B * s.inter, torch.float16).reshape(B, -1))
+    a = operand_decode(view(lay.a, B * s.inter, torch.float16), B)
     if act_dtype == ft.FT_F32:
         out = y.cpu().numpy()
     else:
@@ -116,16 +116,21 @@ def run_gpu(pb: Problem, act_dtype=ft.FT_F32, cache: Optional[torch.Tensor] = No
     return GpuResult(out, qkv, o, h1, a, int(st.item()), cache)
 
 
-def operand_decode(x16: np.ndarray) -> np.ndarray:
-    """Logical FP32 values of a vector stored in the projections' operand layout
-    (include/ft.h: within each 16 inputs the storage order is
+def operand_decode(x16: np.ndarray, B: int) -> np.ndarray:
+    """Logical FP32 values [B, K] of B rows stored in the projections' grouped
+    operand layout (include/ft.h: [K/128][B][128]; runs of 8 stored values
+    permuted by XOR with row mod 8; within each 16 inputs the storage order is
     0,1,8,9,2,3,10,11,4,5,12,13,6,7,14,15 and inputs 8..15 hold value / 16)."""
+    x = np.asarray(x16, np.float32).reshape(-1, B, 16, 8)          # [group][row][stored run][8]
+    runs = np.empty_like(x)
+    for t in range(B):
+        runs[:, t] = x[:, t, np.arange(16) ^ (t & 7)]               # logical run r sits at r ^ (t & 7)
+    slots = runs.reshape(-1, B, 128).transpose(1, 0, 2).reshape(B, -1, 16)
     order = np.array([0, 1, 8, 9, 2, 3, 10, 11, 4, 5, 12, 13, 6, 7, 14, 15])
-    x = np.asarray(x16, np.float32).reshape(x16.shape[:-1] + (-1, 16))
-    out = np.empty_like(x)
-    out[..., order] = x
+    out = np.empty_like(slots)
+    out[..., order] = slots
     out[..., 8:] *= 16.0
-    return out.reshape(x16.shape)
+    return out.reshape(B, -1)
 
 
 def oracle_cache(pb: Problem) -> KVCacheOracle:
