@@ -210,6 +210,18 @@ int ft_decode_workspace_layout(const ft_block_cfg *cfg, int B, int max_ctx, ft_w
 int ft_embed_bf16(const uint16_t *table, const int32_t *tokens, float *x_out, int B, int V, int H,
                   int32_t *dev_status, ft_stream stream);
 
+/* Final RMSNorm on its own (ft_lm_head_bf16 applies it fused):
+ * z[b, :] = bf16(gamma * rho_b * x[b, :]), rho_b = (mean x[b, :]^2 + eps)^-1/2.
+ * x: FP32 [B, H]; gamma: FP32 [H]; z_out: BF16 bits [B, H]. */
+int ft_rmsnorm_bf16(const float *x, const float *gamma, uint16_t *z_out, int B, int H, float eps,
+                    ft_stream stream);
+
+/* Copies the device status word that the calls above OR their asynchronous
+ * FT_DEV_* conditions into to *host_out, after waiting for `stream` (every
+ * call enqueued before it has finished).  FT_OK, or FT_ERR_CUDA if the copy or
+ * the wait fails. */
+int ft_read_device_status(const int32_t *dev_status, int32_t *host_out, ft_stream stream);
+
 /* logits[b, v] = sum_k W[v, k] * z[b, k] with z = gamma * rho(x_b) * x_b,
  * rho = (mean x^2 + eps)^-1/2.  x: FP32 [B, H]; gamma: FP32 [H]; W: BF16 bits
  * [V, H] (16-byte aligned); logits: FP32 [B, V] (overwritten).  B <= 8,

@@ -71,6 +71,8 @@ _SIGS = {
                                           c_void_p, c_void_p, c_int, c_void_p, c_int, c_void_p, c_void_p]),
     "ft_embed_bf16": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_void_p, c_void_p]),
     "ft_lm_head_bf16": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_float, c_void_p]),
+    "ft_rmsnorm_bf16": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_float, c_void_p]),
+    "ft_read_device_status": (c_int, [c_void_p, c_void_p, c_void_p]),
     "ft_decode_block_launches": (c_int, []),
     "ft_set_pdl": (c_int, [c_int]),
 }
@@ -223,6 +225,17 @@ def ft_embed_bf16(table, tokens, x_out, B, V, H, dev_status=None, stream=None) -
 
 def ft_lm_head_bf16(x, gamma, W, logits, B, V, H, eps, stream=None) -> int:
     return lib().ft_lm_head_bf16(_ptr(x), _ptr(gamma), _ptr(W), _ptr(logits), B, V, H, eps, _stream(stream))
+
+
+def ft_rmsnorm_bf16(x, gamma, z, B, H, eps, stream=None) -> int:
+    return lib().ft_rmsnorm_bf16(_ptr(x), _ptr(gamma), _ptr(z), B, H, eps, _stream(stream))
+
+
+def ft_read_device_status(dev_status, stream=None) -> int:
+    """Waits for `stream` and returns the device status word (raises on a CUDA error)."""
+    out = ctypes.c_int32(0)
+    check(lib().ft_read_device_status(_ptr(dev_status), ctypes.byref(out), _stream(stream)), "ft_read_device_status")
+    return int(out.value)
 
 
 def ft_decode_block_launches() -> int:

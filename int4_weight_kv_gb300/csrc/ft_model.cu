@@ -26,6 +26,29 @@ __global__ void __launch_bounds__(256) embed_kernel(const uint16_t* __restrict__
     out[(size_t)b * H + i] = ok ? bf16_bits_to_f32(table[(size_t)tok * H + i]) : 0.0f;
 }
 
+// z[b, :] = bf16(gamma * rho_b * x[b, :]), rho_b = (mean_i x[b, i]^2 + eps)^-1/2.
+// One CTA per row: sum of squares (FP32, tree over warps), then the scaled row.
+__global__ void __launch_bounds__(256) rmsnorm_kernel(const float* __restrict__ x, const float* __restrict__ gamma,
+                                                      uint16_t* __restrict__ z, int H, float eps) {
+  __shared__ float red[8];
+  const int b = blockIdx.x, tid = threadIdx.x;
+  const float* row = x + (size_t)b * H;
+  float ss = 0.0f;
+  for (int i = tid; i < H; i += 256) {
+    const float v = __ldcg(row + i);
+    ss = fmaf(v, v, ss);
+  }
+  ss = warp_sum(ss);
+  if ((tid & 31) == 0) red[tid >> 5] = ss;
+  __syncthreads();
+  float t = 0.0f;
+#pragma unroll
+  for (int w = 0; w < 8; ++w) t += red[w];
+  const float rho = rsqrtf(t / (float)H + eps);
+  for (int i = tid; i < H; i += 256)
+    z[(size_t)b * H + i] = __bfloat16_as_ushort(__float2bfloat16_rn(gamma[i] * (rho * __ldcg(row + i))));
+}
+
 __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
   asm volatile(
@@ -138,6 +161,20 @@ int ft_embed_bf16(const uint16_t* table, const int32_t* tokens, float* x_out, in
   if (!table || !tokens || !x_out || B < 1 || V < 1 || H < 1) return FT_ERR_INVALID_ARG;
   ft::embed_kernel<<<B, 256, 0, (cudaStream_t)stream>>>(table, tokens, x_out, V, H, dev_status);
   return cudaGetLastError() == cudaSuccess ? FT_OK : FT_ERR_CUDA;
+}
+
+int ft_rmsnorm_bf16(const float* x, const float* gamma, uint16_t* z_out, int B, int H, float eps, ft_stream stream) {
+  if (!x || !gamma || !z_out || B < 1 || H < 1 || !(eps >= 0.0f)) return FT_ERR_INVALID_ARG;
+  ft::rmsnorm_kernel<<<B, 256, 0, (cudaStream_t)stream>>>(x, gamma, z_out, H, eps);
+  return cudaGetLastError() == cudaSuccess ? FT_OK : FT_ERR_CUDA;
+}
+
+int ft_read_device_status(const int32_t* dev_status, int32_t* host_out, ft_stream stream) {
+  if (!dev_status || !host_out) return FT_ERR_INVALID_ARG;
+  if (cudaMemcpyAsync(host_out, dev_status, sizeof(int32_t), cudaMemcpyDeviceToHost, (cudaStream_t)stream) !=
+      cudaSuccess)
+    return FT_ERR_CUDA;
+  return cudaStreamSynchronize((cudaStream_t)stream) == cudaSuccess ? FT_OK : FT_ERR_CUDA;
 }
 
 int ft_lm_head_bf16(const float* x, const float* gamma, const uint16_t* W, float* logits, int B, int V, int H,

@@ -112,5 +112,10 @@ def test_argument_errors_return_before_launch(ft):
     assert lib.ft_kv_append_int4(ctypes.byref(c), 4097, 2, 64, 16, 16, 16, 1, 1, None, None) == ft.FT_ERR_INVALID_ARG
     assert lib.ft_kv_unpack_int4(ctypes.byref(c), 4096, 2, 64, 3, 8, 16, 16, 16, 16, None) == ft.FT_ERR_INVALID_ARG
     assert ft.ft_decode_block_launches() == 7
+    # model-step helpers
+    assert lib.ft_rmsnorm_bf16(None, 4096, 8192, 1, 64, ctypes.c_float(1e-5), None) == ft.FT_ERR_INVALID_ARG
+    assert lib.ft_rmsnorm_bf16(4096, 4096, 8192, 0, 64, ctypes.c_float(1e-5), None) == ft.FT_ERR_INVALID_ARG
+    assert lib.ft_rmsnorm_bf16(4096, 4096, 8192, 1, 64, ctypes.c_float(-1.0), None) == ft.FT_ERR_INVALID_ARG
+    assert lib.ft_read_device_status(None, 4096, None) == ft.FT_ERR_INVALID_ARG
     prev = ft.ft_set_pdl(False)
     assert ft.ft_set_pdl(prev) is False

@@ -54,6 +54,28 @@ def test_embed_and_lm_head_small(B, V, Hd):
     assert H.rel_rms(logits.cpu().numpy(), ref) < 1e-4
 
 
+@pytest.mark.parametrize("B,H", [(1, 512), (3, 4096), (8, 8192)])
+def test_rmsnorm_and_device_status(B, H):
+    """Standalone final RMSNorm against FP64 (one BF16 rounding), and the status
+    word read back through ft_read_device_status after a device-side range flag."""
+    g = np.random.default_rng(B * 7 + H)
+    x = (g.normal(0, 1, (B, H)) * np.where(g.random(H) < 0.01, 20.0, 1.0)).astype(np.float32)
+    gamma = g.uniform(0.5, 1.5, H).astype(np.float32)
+    z = torch.empty((B, H), dtype=torch.int16, device="cuda")
+    ft.check(ft.ft_rmsnorm_bf16(torch.from_numpy(x).cuda(), torch.from_numpy(gamma).cuda(), z, B, H, 1e-5))
+    got = synth.bf16_bits_to_f32(z.cpu().numpy().view(np.uint16)).astype(np.float64)
+    xv = x.astype(np.float64)
+    ref = gamma[None, :] * rms_factor(xv, 1e-5)[:, None] * xv
+    # FP32 arithmetic then one BF16 rounding: within one BF16 ulp of the FP64 value
+    assert np.all(np.abs(got - ref) <= 2.0 ** -7 * np.abs(ref) + 1e-30)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    assert ft.ft_read_device_status(st) == 0
+    emb = torch.zeros((4, H), dtype=torch.int16, device="cuda")
+    out = torch.empty((1, H), dtype=torch.float32, device="cuda")
+    ft.check(ft.ft_embed_bf16(emb, torch.tensor([9], dtype=torch.int32, device="cuda"), out, 1, 4, H, st))
+    assert ft.ft_read_device_status(st) & ft.FT_DEV_RANGE
+
+
 def test_full_model_8b_32_layers_b1_ctx4096():
     """Random-init Llama-3.1-8B architecture, batch 1, context 4096, vocab 128256."""
     wl = synth.workload("8b_full_b1_ctx4096")
