@@ -616,19 +616,20 @@ static cudaError_t launch_ts_one(const GemvParams& p, cudaStream_t st, bool pdl)
                    st, pdl, p);
 }
 
-// Tile-split shapes: gate/up (whole sets, SwiGLU in the epilogue) uses 6 warps and
-// 1-4 tiles per warp so that sets number about one per SM; the split-K roles use
-// 8 warps x 2 tiles (256 rows per set).
-constexpr int kTsNcwGU = 6, kTsNcw = 8, kTsTpw = 2;
+// Tile-split shapes.  Split-K roles: 12 warps x 1 tile (192-row sets).  Gate/up
+// (whole sets, SwiGLU in the epilogue): 12 warps x 1 tile where that makes about
+// one set per SM, else 6 warps x 1-4 tiles (registers bound warps x tiles).
+constexpr int kTsNcw = 12, kTsTpw = 1, kTsNcwGUWide = 6;
 
 template <int NT, int ROLE>
 static cudaError_t launch_ts_nt(const GemvParams& p, cudaStream_t st, bool pdl) {
   if constexpr (ROLE == kRoleGU) {
+    if (p.plan.NCW == kTsNcw) return launch_ts_one<NT, ROLE, 1, kTsNcw>(p, st, pdl);
     switch (p.plan.tpw) {
-      case 1: return launch_ts_one<NT, ROLE, 1, kTsNcwGU>(p, st, pdl);
-      case 2: return launch_ts_one<NT, ROLE, 2, kTsNcwGU>(p, st, pdl);
-      case 3: return launch_ts_one<NT, ROLE, 3, kTsNcwGU>(p, st, pdl);
-      case 4: return launch_ts_one<NT, ROLE, 4, kTsNcwGU>(p, st, pdl);
+      case 1: return launch_ts_one<NT, ROLE, 1, kTsNcwGUWide>(p, st, pdl);
+      case 2: return launch_ts_one<NT, ROLE, 2, kTsNcwGUWide>(p, st, pdl);
+      case 3: return launch_ts_one<NT, ROLE, 3, kTsNcwGUWide>(p, st, pdl);
+      case 4: return launch_ts_one<NT, ROLE, 4, kTsNcwGUWide>(p, st, pdl);
       default: return cudaErrorInvalidValue;
     }
   } else {
@@ -709,12 +710,14 @@ GemvPlan make_gemv_plan(int role, int N, int K, int B, int sms, int smem_budget)
   if (role == kRoleDown) p.RT = kDownRT;
   p.ts = p.NT >= 3 ? 1 : 0;
   if (p.ts) {
-    p.NCW = role == kRoleGU ? kTsNcwGU : kTsNcw;
+    p.NCW = kTsNcw;
+    p.tpw = kTsTpw;
     if (role == kRoleGU) {  // about one whole set per SM
-      const int per = (N / kRowTile + sms * p.NCW - 1) / (sms * p.NCW);
-      p.tpw = std::max(1, std::min(4, per));
-    } else {
-      p.tpw = kTsTpw;
+      const int ntile = N / kRowTile;
+      if ((ntile + sms * kTsNcw - 1) / (sms * kTsNcw) > 1) {
+        p.NCW = kTsNcwGUWide;
+        p.tpw = std::max(1, std::min(4, (ntile + sms * p.NCW - 1) / (sms * p.NCW)));
+      }
     }
     p.RT = p.tpw * p.NCW;
   }
