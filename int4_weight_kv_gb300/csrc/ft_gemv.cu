@@ -9,10 +9,12 @@
 // GB300 design:
 //  * one CTA per SM: one producer warp streams the CTA's contiguous run of
 //    (row tile, group) slabs with 1-D bulk async copies (cp.async.bulk, mbarrier
-//    completion) into a ring of stages sized at launch, next to the matching
-//    chunk of the FP16 activation operand and its group offsets.  Weights do
-//    not depend on earlier kernels, so the ring fills BEFORE the producer waits
-//    on its predecessor (programmatic dependent launch).
+//    completion; one copy per row tile, issued from parallel lanes) into a ring
+//    of stages sized at launch, next to the matching chunk of the FP16
+//    activation operand (one copy: the grouped layout keeps a stage's B rows
+//    contiguous) and its group offsets.  Weights do not depend on earlier
+//    kernels, so the ring fills BEFORE the producer waits on its predecessor
+//    (programmatic dependent launch).
 //  * NCW consumer warps split each stage's groups; each keeps RT row tiles x
 //    NT eight-token column tiles in registers.  Nibbles become FP16 A fragments
 //    with four logic ops and a shift per 8 weights (magic_word: the 1024-offset
@@ -20,9 +22,13 @@
 //    offset is removed by starting each group's chain at -S (see ft_internal).
 //  * warps reduce through shared memory at the end of a row-tile set.  QKV and
 //    O split sets along K across CTAs and red.add the partial sums into an FP32
-//    accumulator that the next kernel reads.  Gate/up and down CTAs own whole
-//    row-tile sets, so SwiGLU and the block output (residual + BF16 rounding)
-//    are written directly, with no cross-CTA step.
+//    accumulator that the next kernel reads.  Gate/up CTAs own whole row-tile
+//    sets (SwiGLU in the epilogue); down owns whole sets where that balances
+//    (block output written directly) and otherwise splits them, the last piece
+//    of each set writing the output (completion ticket, never waits).
+//  * batches of 17-32 (three or four token tiles) use gemv_ts_kernel below:
+//    each consumer warp owns whole row tiles of a wide set, so one activation
+//    stage serves many more weight rows.
 #include <algorithm>
 
 #include "ft_block.cuh"
