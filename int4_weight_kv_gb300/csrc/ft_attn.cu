@@ -4,7 +4,7 @@
 // output, split-KV reduction for long contexts; "전제와 한계": the 8-head INT4
 // cache is read directly by the query heads, no head expansion).
 //
-// One CTA (4 warps) per (request b, KV head h, split): the G = n_q / n_kv query
+// One CTA (kAttnWarps warps) per (request b, KV head h, split): the G = n_q / n_kv query
 // heads of the group share every K/V byte the CTA reads.  Per 16-position tile
 // a warp computes
 //   S[pos][head]  = K^(16 x d) . q~ (d x 8 heads)       (A = K codes, FP16 exact)
@@ -101,14 +101,14 @@ __device__ __forceinline__ void warp_rope(float (&v)[NPL], int pos, const uint64
 }
 
 template <int D>
-__global__ void __launch_bounds__(128) attn_kernel(const AttnParams p) {
+__global__ void __launch_bounds__(kAttnWarps * 32) attn_kernel(const AttnParams p) {
   constexpr int NPL = D / 32;
   constexpr int KT = D / 16;  // k-tiles of q.K == m-tiles of P.V
   constexpr int PW = D + 4;             // one partial: running max, sum, 2 pad, acc[D] (16-byte rows)
   __shared__ float qt[8][D];            // rotated, scaled query (FP16 values)
   __shared__ float qoff[8];             // its operand offsets (magic-number decode)
   __shared__ float knew[D], vnew[D];
-  __shared__ float fac[8][5];           // per head: CTA max, then each warp's rescale factor
+  __shared__ float fac[8][1 + kAttnWarps];  // per head: CTA max, then each warp's rescale factor
   __shared__ __align__(8) uint64_t inbox_bar;  // completes when every partial of this CTA's heads arrived
   // dynamic: mrg[4][G * PW], each warp's partial of every head, then
   // inbox[n_split * ceil(G / n_split)][PW], the partials of the heads this CTA
@@ -162,7 +162,7 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnParams p) {
     if (tid == 0 && h == 0 && split == 0) p.rho1[b] = rho1;
   }
   // ---- rotated, scaled query of each head (rho1, RoPE, Hadamard, softmax scale)
-  for (int u = warp; u < G; u += 4) {
+  for (int u = warp; u < G; u += kAttnWarps) {
     float v[NPL];
     const float* src = p.qkv + (size_t)b * p.Nqkv + (size_t)(h * G + u) * D;
 #pragma unroll
@@ -216,10 +216,10 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnParams p) {
   const uint32_t kappa[4] = {kHOffLo, kHOffLo, kHOffHi, kHOffHi};
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
 
-  for (; ti < t1; ti += 4) {
+  for (; ti < t1; ti += kAttnWarps) {
     TileRegs<D> nxt;
-    const bool more = ti + 4 < t1;
-    if (more) load_tile<D>(nxt, p.cache, p.L, b, h, 16 * (ti + 4), g, tig);
+    const bool more = ti + kAttnWarps < t1;
+    if (more) load_tile<D>(nxt, p.cache, p.L, b, h, 16 * (ti + kAttnWarps), g, tig);
     const int p0 = 16 * ti;
     // S = K . q~   (rows: positions g, g+8; columns: heads 2tig, 2tig+1)
     float sacc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
@@ -300,14 +300,14 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnParams p) {
     acc[mt][3] -= kacc[1];
   }
 
-  // ---- merge the 4 warps of the CTA into this CTA's partial (kept in smem)
+  // ---- merge the warps of the CTA into this CTA's partial (kept in smem)
 #pragma unroll
   for (int o = 4; o < 32; o <<= 1) {
     l0 += __shfl_xor_sync(0xffffffffu, l0, o);
     l1 += __shfl_xor_sync(0xffffffffu, l1, o);
   }
   float* mrg = dyn;                       // [4][G * PW]
-  float* inbox = dyn + 4 * G * PW;        // [n_split * ceil(G / n_split)][PW]
+  float* inbox = dyn + kAttnWarps * G * PW;  // [n_split * ceil(G / n_split)][PW]
   float* mw = mrg + warp * G * PW;
   const bool c0ok = 2 * tig < G, c1ok = 2 * tig + 1 < G;  // this lane's two head columns exist
   float* h0 = mw + (2 * tig) * PW;
@@ -324,12 +324,12 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnParams p) {
   }
   __syncthreads();
   if (tid < G) {  // per head: the CTA max and each warp's rescale factor
-    float mx[4], M = -INFINITY;
+    float mx[kAttnWarps], M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < 4; ++w) M = fmaxf(M, mx[w] = mrg[(w * G + tid) * PW]);
+    for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, mx[w] = mrg[(w * G + tid) * PW]);
     fac[tid][0] = M;
 #pragma unroll
-    for (int w = 0; w < 4; ++w) fac[tid][1 + w] = (mx[w] == -INFINITY) ? 0.0f : exp2f(mx[w] - M);
+    for (int w = 0; w < kAttnWarps; ++w) fac[tid][1 + w] = (mx[w] == -INFINITY) ? 0.0f : exp2f(mx[w] - M);
   }
   __syncthreads();
   // ---- this CTA's partial of every head, pushed into the inbox of the CTA that
@@ -337,11 +337,11 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnParams p) {
   cluster_wait();  // every CTA of the cluster has started (arrived at entry)
   const uint32_t inbox0 = smem_u32(inbox);
   constexpr int PW4 = PW / 4;
-  for (int i = tid; i < G * PW4; i += 128) {
+  for (int i = tid; i < G * PW4; i += kAttnWarps * 32) {
     const int hh = i / PW4, e4 = i - hh * PW4;
     float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
 #pragma unroll
-    for (int w = 0; w < 4; ++w) {
+    for (int w = 0; w < kAttnWarps; ++w) {
       const float4 a = reinterpret_cast<const float4*>(mrg + (w * G + hh) * PW)[e4];
       const float f = fac[hh][1 + w];
       v.x = fmaf(a.x, f, v.x);
@@ -379,7 +379,7 @@ __global__ void __launch_bounds__(128) attn_kernel(const AttnParams p) {
   }
 
   // ---- CTA r merges heads r, r + n_split, ...: the new token and the n_split partials
-  for (int j = warp; split + p.nsplit * j < G; j += 4) {
+  for (int j = warp; split + p.nsplit * j < G; j += kAttnWarps) {
     const int hh = split + p.nsplit * j;
     float sn = 0.0f;
 #pragma unroll
@@ -449,8 +449,9 @@ int attn_ctas_per_sm(int G, int d) {
   int n = g_attn_occ[dev][di][G].load(std::memory_order_relaxed);
   if (n > 0) return n;
   const size_t dyn = (size_t)attn_dyn_smem(G, 8, d);  // the largest inbox (8 splits)
-  const cudaError_t e = di ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_kernel<128>, 128, dyn)
-                           : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_kernel<64>, 128, dyn);
+  const cudaError_t e =
+      di ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_kernel<128>, kAttnWarps * 32, dyn)
+         : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_kernel<64>, kAttnWarps * 32, dyn);
   if (e != cudaSuccess) return 0;
   g_attn_occ[dev][di][G].store(n, std::memory_order_relaxed);
   return n;
@@ -459,7 +460,7 @@ int attn_ctas_per_sm(int G, int d) {
 cudaError_t launch_attn(const AttnParams& p, int head_dim, cudaStream_t st, bool pdl) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(p.B * p.nkv * p.nsplit));
-  cfg.blockDim = dim3(128);
+  cfg.blockDim = dim3(kAttnWarps * 32);
   cfg.dynamicSmemBytes = attn_dyn_smem(p.G, p.nsplit, head_dim);
   cfg.stream = st;
   cudaLaunchAttribute attr[2];

@@ -111,10 +111,11 @@ __host__ __device__ __forceinline__ int rms_parts(int H) { return (H / 8 + kPrep
 // host-side launchers (ft_gemv.cu / ft_attn.cu / ft_block.cu)
 cudaError_t launch_gemv(int role, const GemvParams& p, cudaStream_t st, bool pdl);
 cudaError_t launch_attn(const AttnParams& p, int head_dim, cudaStream_t st, bool pdl);
-// Dynamic shared memory of one attention CTA: 4 warp partials of G heads and
+constexpr int kAttnWarps = 4;  // warps per attention CTA (16-position tiles strided over them)
+// Dynamic shared memory of one attention CTA: the warps' partials of G heads and
 // the inbox of n_split * ceil(G / n_split) pushed partials, (d + 4) floats each.
 __host__ __device__ __forceinline__ int attn_dyn_smem(int G, int nsplit, int d) {
-  return (4 * G + nsplit * ((G + nsplit - 1) / nsplit)) * (d + 4) * 4;
+  return (kAttnWarps * G + nsplit * ((G + nsplit - 1) / nsplit)) * (d + 4) * 4;
 }
 // Static + dynamic shared memory of one attention CTA (host).
 int attn_smem_bytes(int G, int nsplit, int d);
