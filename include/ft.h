@@ -199,6 +199,18 @@ typedef struct {
 
 int ft_decode_workspace_layout(const ft_block_cfg *cfg, int B, int max_ctx, ft_ws_layout *out);
 
+/* How ft_decode_block partitions one projection (role FT_W_*) for this batch
+ * on the current device (148 SMs assumed when no device is visible): ctas
+ * launched; rows per set (row_tiles x 16);
+ * consumer warps; 8-token column tiles; whole = 1 when every CTA owns whole
+ * sets (no split along the inputs); tile_split = 1 for the large-batch kernel
+ * in which each warp owns whole row tiles; ring stages, groups (128 inputs)
+ * per stage and dynamic shared memory per CTA in bytes. */
+typedef struct {
+  int32_t ctas, row_tiles, warps, col_tiles, whole, tile_split, stages, groups_per_stage, smem_bytes;
+} ft_gemv_info;
+int ft_decode_plan_info(const ft_block_cfg *cfg, int B, int max_ctx, int role, ft_gemv_info *out);
+
 /* ---- full decode step helpers (BF16, not INT4) ----------------------------
  * A complete Llama-style decode step is: embedding gather, the decode block
  * per layer (FT_F32 residual between layers), final RMSNorm, LM head (summary

@@ -34,6 +34,11 @@ class LayerWeights(ctypes.Structure):
     _fields_ = [("qkv", c_void_p), ("o", c_void_p), ("gateup", c_void_p), ("down", c_void_p)]
 
 
+class GemvInfo(ctypes.Structure):
+    _fields_ = [(n, c_int32) for n in ("ctas", "row_tiles", "warps", "col_tiles", "whole", "tile_split", "stages",
+                                       "groups_per_stage", "smem_bytes")]
+
+
 class WsLayout(ctypes.Structure):
     _fields_ = [("qkv", c_size_t), ("rho1", c_size_t), ("o", c_size_t), ("h1", c_size_t), ("a", c_size_t),
                 ("n_split", c_int32)]
@@ -73,6 +78,7 @@ _SIGS = {
     "ft_lm_head_bf16": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int, c_int, c_float, c_void_p]),
     "ft_rmsnorm_bf16": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_float, c_void_p]),
     "ft_read_device_status": (c_int, [c_void_p, c_void_p, c_void_p]),
+    "ft_decode_plan_info": (c_int, [c_void_p, c_int, c_int, c_int, c_void_p]),
     "ft_decode_block_launches": (c_int, []),
     "ft_set_pdl": (c_int, [c_int]),
 }
@@ -236,6 +242,13 @@ def ft_read_device_status(dev_status, stream=None) -> int:
     out = ctypes.c_int32(0)
     check(lib().ft_read_device_status(_ptr(dev_status), ctypes.byref(out), _stream(stream)), "ft_read_device_status")
     return int(out.value)
+
+
+def ft_decode_plan_info(cfg, B: int, max_ctx: int, role: int) -> GemvInfo:
+    out = GemvInfo()
+    check(lib().ft_decode_plan_info(ctypes.byref(cfg), int(B), int(max_ctx), int(role), ctypes.byref(out)),
+          "ft_decode_plan_info")
+    return out
 
 
 def ft_decode_block_launches() -> int:

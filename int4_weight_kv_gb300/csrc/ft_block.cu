@@ -372,6 +372,26 @@ int ft_decode_workspace_layout(const ft_block_cfg* c, int B, int max_ctx, ft_ws_
   return FT_OK;
 }
 
+int ft_decode_plan_info(const ft_block_cfg* c, int B, int max_ctx, int role, ft_gemv_info* out) {
+  const int e = ft_host::check_cfg(c);
+  if (e != FT_OK) return e;
+  if (!out || B < 1 || B > 32 || max_ctx < 1 || role < FT_W_QKV || role > FT_W_DOWN) return FT_ERR_INVALID_ARG;
+  const ft::WsPlan P = ft::make_plan(*c, B, max_ctx);
+  const int r = role == FT_W_QKV ? ft::kRoleQKV : role == FT_W_O ? ft::kRoleO : role == FT_W_GATEUP ? ft::kRoleGU
+                                                                                                     : ft::kRoleDown;
+  const ft::GemvPlan& g = P.g[r];
+  out->ctas = g.C;
+  out->row_tiles = g.RT;
+  out->warps = g.NCW;
+  out->col_tiles = g.NT;
+  out->whole = g.whole;
+  out->tile_split = g.ts;
+  out->stages = g.stages;
+  out->groups_per_stage = g.ng;
+  out->smem_bytes = g.smem;
+  return FT_OK;
+}
+
 int ft_decode_block(const ft_block_cfg* c, const ft_layer_weights* w, void* cache, int max_batch, int max_ctx,
                     const void* x_in, void* x_out, int act_dtype, const int32_t* pos, int B, void* ws,
                     size_t ws_bytes, int32_t* status, ft_stream stream) {

@@ -7,6 +7,8 @@ import re
 
 import pytest
 
+import synth
+
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
@@ -119,3 +121,32 @@ def test_argument_errors_return_before_launch(ft):
     assert lib.ft_read_device_status(None, 4096, None) == ft.FT_ERR_INVALID_ARG
     prev = ft.ft_set_pdl(False)
     assert ft.ft_set_pdl(prev) is False
+
+
+def test_plan_partitions(ft):
+    """Host-side partition choices (no GPU needed): whole vs split sets, the
+    tile-split kernel for three or four token tiles, shared memory within one SM."""
+    c8 = ft.cfg_from_shape(synth.workload("8b_b1_ctx1024").shape)
+    c70 = ft.cfg_from_shape(synth.workload("70b_b1_ctx2048").shape)
+    info = lambda c, B, role: ft.ft_decode_plan_info(c, B, 4097, role)
+    for c in (c8, c70):
+        for B in (1, 2, 8, 9, 16, 17, 32):
+            for role in ft.ROLES:
+                g = info(c, B, role)
+                assert g.col_tiles == (B + 7) // 8
+                assert g.tile_split == (1 if B > 16 else 0)
+                assert 2 <= g.stages <= 8 and 1 <= g.groups_per_stage
+                assert 0 < g.smem_bytes <= 227 * 1024
+                assert 1 <= g.ctas <= 148
+                if role == ft.FT_W_GATEUP:
+                    assert g.whole == 1            # SwiGLU needs whole rows
+                if role in (ft.FT_W_QKV, ft.FT_W_O):
+                    assert g.whole == 0            # split along K, red.add into the accumulator
+    # down: whole two-tile sets balance for the 8B shape, not for 70B (long K)
+    assert info(c8, 1, ft.FT_W_DOWN).whole == 1 and info(c8, 1, ft.FT_W_DOWN).row_tiles == 2
+    assert info(c70, 1, ft.FT_W_DOWN).whole == 0
+    # tile-split sets: every consumer warp owns whole row tiles
+    g = info(c8, 32, ft.FT_W_QKV)
+    assert g.row_tiles % g.warps == 0 and g.row_tiles >= 12
+    with pytest.raises(RuntimeError):
+        info(c8, 33, ft.FT_W_QKV)
