@@ -457,6 +457,36 @@ int attn_ctas_per_sm(int G, int d) {
   return n;
 }
 
+static std::atomic<int> g_attn_cl[64][2][9];
+
+int attn_max_cluster(int G, int d) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || G < 1 || G > 8) return 8;
+  const int di = d == 128 ? 1 : 0;
+  int c = g_attn_cl[dev][di][G].load(std::memory_order_relaxed);
+  if (c > 0) return c;
+  c = 8;
+  auto fn = di ? (const void*)attn_kernel<128> : (const void*)attn_kernel<64>;
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(16);
+    cfg.blockDim = dim3(kAttnWarps * 32);
+    cfg.dynamicSmemBytes = attn_dyn_smem(G, 16, d);
+    cudaLaunchAttribute a[1];
+    a[0].id = cudaLaunchAttributeClusterDimension;
+    a[0].val.clusterDim.x = 16;
+    a[0].val.clusterDim.y = 1;
+    a[0].val.clusterDim.z = 1;
+    cfg.attrs = a;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) == cudaSuccess && n > 0) c = 16;
+  }
+  cudaGetLastError();  // a refused query leaves no sticky state behind
+  g_attn_cl[dev][di][G].store(c, std::memory_order_relaxed);
+  return c;
+}
+
 cudaError_t launch_attn(const AttnParams& p, int head_dim, cudaStream_t st, bool pdl) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(p.B * p.nkv * p.nsplit));

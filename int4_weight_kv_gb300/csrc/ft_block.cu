@@ -144,7 +144,8 @@ static int attn_splits(int B, int nkv, int G, int d, int max_ctx, int sms) {
   int ns = target / pairs;
   const int cap = (max_ctx + 63) / 64;
   if (ns > cap) ns = cap;
-  if (ns > 8) ns = 8;  // the splits of one (request, KV head) form one portable cluster
+  const int maxc = attn_max_cluster(G, d);  // the splits of one (request, KV head) form one cluster
+  if (ns > maxc) ns = maxc;
   if (ns < 1) ns = 1;
   return ns;
 }

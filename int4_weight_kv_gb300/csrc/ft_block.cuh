@@ -121,6 +121,9 @@ __host__ __device__ __forceinline__ int attn_dyn_smem(int G, int nsplit, int d) 
 int attn_smem_bytes(int G, int nsplit, int d);
 // Attention CTAs resident per SM (registers, shared memory), 0 if unknown (host).
 int attn_ctas_per_sm(int G, int d);
+// Largest cluster of attention CTAs the device schedules: 16 where the
+// non-portable size is allowed and fits, else 8 (host).
+int attn_max_cluster(int G, int d);
 // Gate/up and down CTAs own whole row-tile sets; QKV and O split sets over
 // CTAs along K (partial sums red.add-ed into an FP32 accumulator).
 GemvPlan make_gemv_plan(int role, int N, int K, int B, int sms, int smem_budget);
