@@ -6,6 +6,8 @@ and the same relative RMS on the two sublayer deltas.  Block outputs are taken
 in FP32 output mode so the gate measures the kernels' arithmetic; a separate
 test checks that BF16 output mode is the BF16 rounding of the FP32 output.
 """
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -106,6 +108,21 @@ def test_block_tiny(tiny):
     o = H.run_oracle(pb)
     rep = H.assert_block_close(g, o, range(1))
     assert rep["qkv_rel_rms"] < 1e-3
+
+
+@pytest.mark.parametrize("bad", [np.nan, np.inf])
+def test_block_nonfinite_input_is_flagged(tiny, bad):
+    """A non-finite activation is reported through the device status word
+    (FT_DEV_RANGE) and the call completes (no wait depends on values); the other
+    request of the batch is unaffected."""
+    pb = H.make_problem(tiny, 1, B=2, ctx=16)
+    x = pb.x_f32.copy()
+    x[1, 5] = bad
+    g = H.run_gpu(dataclasses.replace(pb, x_f32=x))
+    assert g.status & ft.FT_DEV_RANGE
+    assert not np.isfinite(g.out[1]).all()
+    clean = H.run_gpu(pb)
+    assert H.rel_rms(g.out[0], clean.out[0]) < 1e-3  # same arithmetic up to the order of atomic adds
 
 
 def test_block_tiny_ragged_batch(tiny):
