@@ -244,19 +244,20 @@ int ft_lm_head_bf16(const float *x, const float *gamma, const uint16_t *W, float
 
 /* ft_decode_block without a caller-provided workspace.  The FuTransformer paper
  * has no counterpart to this call; it exists for callers that cannot allocate
- * device memory when
- * they run a step (a pool or allocation policy that forbids new device
- * allocations after start-up, a host that hands over only input and output
- * buffers, or a loop that must not pay for an allocation).  The scratch space
- * is a fixed 8 MiB device array inside this library, held by every GPU that
- * loads it until the process exits; problems needing more (see
- * ft_decode_workspace_bytes) return FT_ERR_WORKSPACE and enqueue nothing.  No
- * memory is allocated by this call.  The array is shared by all calls on a
- * device and keeps the previous call's contents (the block clears what it
- * needs itself); calls that overlap on the GPU race on it.  The first call on
- * each device looks up the array's address (cudaGetSymbolAddress) with that
- * device current; make that first call before any stream capture.  Arguments
- * and results are otherwise those of ft_decode_block. */
+ * device memory when they run a step (a pool or allocation policy that forbids
+ * new device allocations after start-up, a host that hands over only input and
+ * output buffers, or a loop that must not pay for an allocation).  The scratch
+ * space is a fixed 32 MiB device array inside this library, held by every GPU
+ * that loads it until the process exits; problems needing more (see
+ * ft_decode_workspace_bytes; the 70B layer shape at batch 32 needs about
+ * 22 MiB) return FT_ERR_WORKSPACE and enqueue nothing.  No memory is allocated
+ * by this call.  The array is shared by all calls on a device and keeps the
+ * previous call's contents (the block clears what it needs itself); calls that
+ * overlap on the GPU race on it.  The first call on each device looks up the
+ * array's address (cudaGetSymbolAddress) with that device current; make that
+ * first call before any stream capture.  The address is kept for the process's
+ * life: do not use this call on a device after cudaDeviceReset in the same
+ * process.  Arguments and results are otherwise those of ft_decode_block. */
 int ft_decode_block_static_ws(const ft_block_cfg *cfg, const ft_layer_weights *w, void *cache, int max_batch,
                               int max_ctx, const void *x_in, void *x_out, int act_dtype, const int32_t *pos, int B,
                               int32_t *dev_status, ft_stream stream);

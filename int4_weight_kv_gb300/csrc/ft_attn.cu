@@ -110,10 +110,11 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_kernel(const AttnParams 
   __shared__ float knew[D], vnew[D];
   __shared__ float fac[8][1 + kAttnWarps];  // per head: CTA max, then each warp's rescale factor
   __shared__ __align__(8) uint64_t inbox_bar;  // completes when every partial of this CTA's heads arrived
-  // dynamic: mrg[4][G * PW], each warp's partial of every head, then
-  // inbox[n_split * ceil(G / n_split)][PW], the partials of the heads this CTA
-  // merges, pushed by every CTA of the cluster (slot j * n_split + r holds CTA
-  // r's partial of head split + j * n_split)
+  // dynamic: mrg[4][G * PW], each warp's partial of every head (before the main
+  // loop the same area holds the staged QKV pieces), then, after the larger of
+  // the two, inbox[n_split * ceil(G / n_split)][PW], the partials of the heads
+  // this CTA merges, pushed by every CTA of the cluster (slot j * n_split + r
+  // holds CTA r's partial of head split + j * n_split)
   extern __shared__ __align__(16) float dyn[];
   __shared__ uint8_t stage[2][D];
   __shared__ __align__(16) uint8_t stage_out[2][D / 2];
@@ -126,9 +127,12 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_kernel(const AttnParams 
   const int G = p.G;
   const int Lb = p.pos[b];
   if (Lb < 0 || Lb >= p.L.max_ctx) {
-    // every CTA of this cluster serves the same request, so all leave here together
+    // every CTA of this cluster serves the same request, so all leave here together;
+    // they still wait for the QKV kernel, so that this kernel's completion implies
+    // its predecessor's (the next kernels rely on that chain)
     if (tid == 0 && split == 0 && h == 0) set_status(p.status, FT_DEV_CAPACITY);
     griddep_launch();
+    griddep_wait();
     return;
   }
   const int ntiles = (Lb + 15) / 16;
@@ -154,6 +158,27 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_kernel(const AttnParams 
 
   griddep_wait();
 
+  // The QKV projection arrives as piece slabs (one per CTA that shared a row
+  // set), added here in slab order.  The CTA first stages the pieces it needs
+  // (its G query heads and, in merging CTAs, k and v) in shared memory with
+  // asynchronous copies, each 16-byte chunk of each piece once (no register
+  // holds the data in flight; the RMSNorm partial sums load meanwhile), in the
+  // area that later holds the warps' partials.  Sets are multiples of 32 rows,
+  // so a 16-byte chunk lies in one set.
+  const GemvPlan& qp = p.qkv_plan;
+  const bool merger = split < G;
+  const int npm = qp.npmax;
+  float* qkv_st = dyn;  // [segment (q heads, then k and v)][piece][D]
+  {
+    const int srows = qp.RT * kRowTile, nseg = G + (merger ? 2 : 0);
+    const size_t slab = (size_t)p.B * qp.N;
+    const float* src0 = p.qkv_part + (size_t)b * qp.N;
+    for (int i = tid; i < nseg * npm * (D / 4); i += kAttnWarps * 32) {
+      const int c4 = i % (D / 4), sj = i / (D / 4), j = sj % npm, sg = sj / npm;
+      const int row = (sg < G ? h * G + sg : p.nq + (sg - G) * p.nkv + h) * D + 4 * c4;
+      if (j < plan_pieces(qp, row / srows)) cp_async16(smem_u32(qkv_st + sj * D + 4 * c4), src0 + j * slab + row);
+    }
+  }
   float rho1;  // RMSNorm row factor of the block input, from the prep kernel's partial sums
   {
     float t = 0.0f;
@@ -161,12 +186,30 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_kernel(const AttnParams 
     rho1 = rsqrtf(warp_sum(t) * p.inv_h + p.eps);
     if (tid == 0 && h == 0 && split == 0) p.rho1[b] = rho1;
   }
+  cp_async_wait_all();
+  __syncthreads();
+  // sums of the staged pieces of channels lane + 32 m of segment sg, in slab order
+  auto staged_sum = [&](int sg, int base, float (&v)[NPL]) {
+#pragma unroll
+    for (int m = 0; m < NPL; ++m) {
+      const int np = plan_pieces(qp, (base + 32 * m) / (qp.RT * kRowTile));
+      const float* q = qkv_st + sg * npm * D + lane + 32 * m;
+      float a = q[0];
+      for (int j = 1; j < np; ++j) a += q[j * D];
+      v[m] = a;
+    }
+  };
   // ---- rotated, scaled query of each head (rho1, RoPE, Hadamard, softmax scale)
   for (int u = warp; u < G; u += kAttnWarps) {
     float v[NPL];
-    const float* src = p.qkv + (size_t)b * p.Nqkv + (size_t)(h * G + u) * D;
+    const int qbase = (h * G + u) * D;
+    staged_sum(u, qbase, v);
+    if (split == 0) {  // the summed projection, recorded for inspection
 #pragma unroll
-    for (int m = 0; m < NPL; ++m) v[m] = __ldcg(src + lane + 32 * m) * rho1;
+      for (int m = 0; m < NPL; ++m) p.qkv[(size_t)b * p.Nqkv + qbase + lane + 32 * m] = v[m];
+    }
+#pragma unroll
+    for (int m = 0; m < NPL; ++m) v[m] *= rho1;
     warp_rope<NPL>(v, Lb, p.rope_turn);
     warp_fwht<NPL>(v, p.hb);
     // q~ as the FP16 B operand (channels c % 16 >= 8 hold q / 16) and its offset
@@ -180,17 +223,19 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_kernel(const AttnParams 
       (void)op_encode(q, c, st);
       sq += st;
     }
-    sq = warp_sum(sq);
+    sq = warp_sum(sq);  // one warp, fixed order: deterministic
     if (lane == 0) qoff[u] = sq;
   }
-  // the new token's k (warp 0) and v (warp 1), needed by the merging CTAs only:
-  // loaded now, processed after the main loop
-  const bool merger = split < G;
+  // the new token's k (warp 0) or v (warp 1) of the merging CTAs, with rho1 applied
   float kvraw[NPL];
   if (merger && warp < 2) {
-    const float* src = p.qkv + (size_t)b * p.Nqkv + (size_t)(p.nq + warp * p.nkv + h) * D;
+    const int kvbase = (p.nq + warp * p.nkv + h) * D;
+    staged_sum(G + warp, kvbase, kvraw);
 #pragma unroll
-    for (int m = 0; m < NPL; ++m) kvraw[m] = ld_cg_early(src + lane + 32 * m);
+    for (int m = 0; m < NPL; ++m) {
+      if (split == 0) p.qkv[(size_t)b * p.Nqkv + kvbase + lane + 32 * m] = kvraw[m];  // for inspection
+      kvraw[m] *= rho1;
+    }
   }
   __syncthreads();
   uint32_t bq[KT][2];
@@ -307,7 +352,9 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_kernel(const AttnParams 
     l1 += __shfl_xor_sync(0xffffffffu, l1, o);
   }
   float* mrg = dyn;                       // [4][G * PW]
-  float* inbox = dyn + kAttnWarps * G * PW;  // [n_split * ceil(G / n_split)][PW]
+  // [n_split * ceil(G / n_split)][PW], after the larger of the partials and the
+  // staged QKV pieces (peers push into it while this CTA may still read those)
+  float* inbox = dyn + max(kAttnWarps * G * PW, attn_stage_floats(G, D, npm));
   float* mw = mrg + warp * G * PW;
   const bool c0ok = 2 * tig < G, c1ok = 2 * tig + 1 < G;  // this lane's two head columns exist
   float* h0 = mw + (2 * tig) * PW;
@@ -359,7 +406,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_kernel(const AttnParams 
   if (merger && warp < 2) {
     float v[NPL];
 #pragma unroll
-    for (int m = 0; m < NPL; ++m) v[m] = kvraw[m] * rho1;
+    for (int m = 0; m < NPL; ++m) v[m] = kvraw[m];
     if (warp == 0) warp_rope<NPL>(v, Lb, p.rope_turn);
     warp_fwht<NPL>(v, p.hb);
     const size_t row = p.L.row(b, h, Lb);
@@ -417,7 +464,8 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_kernel(const AttnParams 
       so += st;
     }
     so = warp_sum(so);  // a head (d <= 128 channels) lies inside one 128-input group
-    if (lane == 0) atomicAdd(p.s_o + (kbase / kWGroup) * 32 + b, so);
+    // the heads of a group (two at d = 64) add exact integers: any order
+    if (lane == 0) sfix_atomic_add(p.s_o + (kbase / kWGroup) * 32 + b, f32_to_sfix(so));
     if (bad) set_status(p.status, FT_DEV_RANGE);
   }
 }
@@ -427,7 +475,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_kernel(const AttnParams 
 static std::atomic<int> g_attn_static[64][2];
 static std::atomic<int> g_attn_occ[64][2][9];
 
-int attn_smem_bytes(int G, int nsplit, int d) {
+int attn_smem_bytes(int G, int nsplit, int d, int npmax) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
   const int di = d == 128 ? 1 : 0;
@@ -439,7 +487,7 @@ int attn_smem_bytes(int G, int nsplit, int d) {
     stat = (e == cudaSuccess) ? (int)fa.sharedSizeBytes : 8 * 1024;
     if (e == cudaSuccess) g_attn_static[dev][di].store(stat, std::memory_order_relaxed);
   }
-  return stat + attn_dyn_smem(G, nsplit, d);
+  return stat + attn_dyn_smem(G, nsplit, d, npmax);
 }
 
 int attn_ctas_per_sm(int G, int d) {
@@ -448,7 +496,7 @@ int attn_ctas_per_sm(int G, int d) {
   const int di = d == 128 ? 1 : 0;
   int n = g_attn_occ[dev][di][G].load(std::memory_order_relaxed);
   if (n > 0) return n;
-  const size_t dyn = (size_t)attn_dyn_smem(G, 8, d);  // the largest inbox (8 splits)
+  const size_t dyn = (size_t)attn_dyn_smem(G, 8, d, kAttnMaxPieces);  // the largest inbox (8 splits) and stage
   const cudaError_t e =
       di ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_kernel<128>, kAttnWarps * 32, dyn)
          : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_kernel<64>, kAttnWarps * 32, dyn);
@@ -459,6 +507,14 @@ int attn_ctas_per_sm(int G, int d) {
 
 static std::atomic<int> g_attn_cl[64][2][9];
 
+// Allows the largest dynamic shared memory an attention CTA can ask for (G = 8,
+// 16 splits, kAttnMaxPieces staged pieces, d = 128: about 50 KB, above the
+// default 48 KB).  Idempotent; false if the runtime refuses.
+static bool attn_allow_smem(const void* fn) {
+  const int most = attn_dyn_smem(8, 16, 128, kAttnMaxPieces);
+  return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, most) == cudaSuccess;
+}
+
 int attn_max_cluster(int G, int d) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || G < 1 || G > 8) return 8;
@@ -467,11 +523,11 @@ int attn_max_cluster(int G, int d) {
   if (c > 0) return c;
   c = 8;
   auto fn = di ? (const void*)attn_kernel<128> : (const void*)attn_kernel<64>;
-  if (cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
+  if (attn_allow_smem(fn) && cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(16);
     cfg.blockDim = dim3(kAttnWarps * 32);
-    cfg.dynamicSmemBytes = attn_dyn_smem(G, 16, d);
+    cfg.dynamicSmemBytes = attn_dyn_smem(G, 16, d, kAttnMaxPieces);
     cudaLaunchAttribute a[1];
     a[0].id = cudaLaunchAttributeClusterDimension;
     a[0].val.clusterDim.x = 16;
@@ -488,10 +544,19 @@ int attn_max_cluster(int G, int d) {
 }
 
 cudaError_t launch_attn(const AttnParams& p, int head_dim, cudaStream_t st, bool pdl) {
+  static std::atomic<int> allowed[64][2];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  const int di = head_dim == 128 ? 1 : 0;
+  if (!allowed[dev][di].load(std::memory_order_relaxed)) {
+    if (!attn_allow_smem(di ? (const void*)attn_kernel<128> : (const void*)attn_kernel<64>))
+      return cudaErrorInvalidValue;
+    allowed[dev][di].store(1, std::memory_order_relaxed);
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(p.B * p.nkv * p.nsplit));
   cfg.blockDim = dim3(kAttnWarps * 32);
-  cfg.dynamicSmemBytes = attn_dyn_smem(p.G, p.nsplit, head_dim);
+  cfg.dynamicSmemBytes = attn_dyn_smem(p.G, p.nsplit, head_dim, p.qkv_plan.npmax);
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;

@@ -11,8 +11,8 @@
 namespace ft {
 
 // Encodes 8 consecutive inputs 8 ch .. 8 ch + 7 of row t into the grouped
-// operand buffer `op` of B rows (op_index) and returns their contribution to the
-// group offset S.
+// operand buffer `op` of B rows (op_index) and returns their contribution to
+// the group offset S.
 __device__ __forceinline__ float encode_chunk8(const float (&v)[8], int ch, int t, int B, __half* op) {
   float s = 0.0f;
 #pragma unroll
@@ -57,7 +57,7 @@ __device__ __forceinline__ void load_chunk8(const void* row, int dtype, int ch, 
 // and the part's sum of squares (written by thread 0).  kPrepThreads threads,
 // one chunk each; a part is a whole number of 128-input groups.
 __device__ __forceinline__ bool row_part(const float (&v)[8], bool valid, int ch, int b, int B, float* copy,
-                                         __half* op, float* s_grp, float* ssq_out) {
+                                         __half* op, sfix_t* s_grp, float* ssq_out) {
   __shared__ float red[kPrepThreads / 32];
   float ss = 0.0f, sterm = 0.0f;
   bool bad = false;
@@ -75,8 +75,8 @@ __device__ __forceinline__ bool row_part(const float (&v)[8], bool valid, int ch
     sterm = encode_chunk8(v, ch, b, B, op);
   }
   // warps stay converged: a group is 16 chunks and parts start on group boundaries
-  const float gs = group16_sum(sterm);
-  if (valid && (ch & 15) == 0) s_grp[(ch >> 4) * 32 + b] = gs;
+  const float gs = group16_sum(sterm);  // fixed shuffle order: deterministic
+  if (valid && (ch & 15) == 0) s_grp[(ch >> 4) * 32 + b] = f32_to_sfix(gs);
   ss = warp_sum(ss);
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
   __syncthreads();
@@ -91,16 +91,15 @@ __device__ __forceinline__ bool row_part(const float (&v)[8], bool valid, int ch
 
 // Block input -> QKV operand + offsets, partial sums of x^2 (the consumers form
 // rho1 from them and apply it after the QKV accumulation, summary page
-// "어떻게 동작하나"), h1 accumulator <- x, and this call's accumulators cleared.
-// Grid (parts, B).
+// "어떻게 동작하나"), an FP32 copy of x (the residual), and this call's
+// accumulators cleared.  Grid (parts, B).
 __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepParams p) {
   griddep_launch();  // the QKV kernel may start streaming its weights
   griddep_wait();    // the previous kernel may have produced x_in or still read the workspace
   const int part = blockIdx.x, parts = gridDim.x, b = blockIdx.y, tid = threadIdx.x;
   const int first = part * kPrepThreads + tid, step = parts * kPrepThreads;
-  for (int i = first; i < p.nqkv; i += step) p.qkv[(size_t)b * p.nqkv + i] = 0.0f;
-  for (int i = first; i < p.nkg_o; i += step) p.s_o[i * 32 + b] = 0.0f;
-  for (int i = first; i < p.nkg_a; i += step) p.s_a[i * 32 + b] = 0.0f;
+  for (int i = first; i < p.nkg_o; i += step) p.s_o[i * 32 + b] = 0;
+  for (int i = first; i < p.nkg_a; i += step) p.s_a[i * 32 + b] = 0;
   if (b == 0)
     for (int i = first; i < p.ntick; i += step) p.tick[i] = 0u;
   const int ch = first;
@@ -108,23 +107,41 @@ __global__ void __launch_bounds__(kPrepThreads) prep_kernel(const PrepParams p) 
   float v[8];
   const size_t esz = p.act_dtype == FT_F32 ? 4 : 2;
   if (valid) load_chunk8(static_cast<const uint8_t*>(p.x_in) + (size_t)b * p.H * esz, p.act_dtype, ch, v);
-  const bool bad = row_part(v, valid, ch, b, p.B, p.h1 + (size_t)b * p.H, p.x_h, p.s_x, p.ssq + b * parts + part);
+  const bool bad =
+      row_part(v, valid, ch, b, p.B, p.xres + (size_t)b * p.H, p.x_h, p.s_x, p.ssq + b * parts + part);
   if (bad) set_status(p.status, FT_DEV_RANGE);
 }
 
-// h1 (complete after the O projection) -> gate/up operand + offsets, partial
-// sums of h1^2 (rho2 is formed and applied after the gate/up accumulation) and,
-// when the down projection splits sets, its accumulator <- h1.  Grid (parts, B).
+// h1 = x + the O projection (its pieces' slabs added in slab order) -> h1,
+// the gate/up operand + offsets and partial sums of h1^2 (rho2 is formed and
+// applied after the gate/up accumulation).  Grid (parts, B).
 __global__ void __launch_bounds__(kPrepThreads) mid_kernel(const MidParams p) {
   griddep_launch();  // the gate/up kernel may start streaming its weights
-  griddep_wait();
   const int part = blockIdx.x, parts = gridDim.x, b = blockIdx.y;
   const int ch = part * kPrepThreads + threadIdx.x;
   const bool valid = ch < p.H / 8;
+  // before the wait (no dependence on earlier kernels): the 8 rows of a chunk
+  // lie in one row-tile set of the O projection, so they share its piece count
+  const GemvPlan& pl = p.o_plan;
+  const int np = valid ? plan_pieces(pl, (8 * ch) / (pl.RT * kRowTile)) : 0;
+  const size_t slab4 = (size_t)p.B * pl.N / 4;
+  const float4* q = reinterpret_cast<const float4*>(p.o_part + (size_t)b * pl.N + 8 * (valid ? ch : 0));
+  griddep_wait();
   float v[8];
-  if (valid) load_chunk8(p.h1 + (size_t)b * p.H, FT_F32, ch, v);
-  const bool bad = row_part(v, valid, ch, b, p.B, p.out_acc ? p.out_acc + (size_t)b * p.H : nullptr, p.h1_h, p.s_h1,
-                            p.ssq + b * parts + part);
+  if (valid) {
+    // x and the first pieces of W_o o, loaded together
+    float4 xa[kPieceBatch], xc[kPieceBatch];
+    pieces_load<kPieceBatch>(q, slab4, np, xa);
+    pieces_load<kPieceBatch>(q + 1, slab4, np, xc);
+    load_chunk8(p.xres + (size_t)b * p.H, FT_F32, ch, v);
+    // h1 = x + W_o o, the pieces added in slab order
+    const float4 a = pieces_sum<kPieceBatch>(q, slab4, np, xa), c = pieces_sum<kPieceBatch>(q + 1, slab4, np, xc);
+    const float o[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
+#pragma unroll
+    for (int k = 0; k < 8; ++k) v[k] += o[k];
+  }
+  const bool bad =
+      row_part(v, valid, ch, b, p.B, p.h1 + (size_t)b * p.H, p.h1_h, p.s_h1, p.ssq + b * parts + part);
   if (bad) set_status(p.status, FT_DEV_RANGE);
 }
 
@@ -132,7 +149,8 @@ struct WsPlan {
   GemvPlan g[4];
   int nsplit;
   int parts;  // prep / mid CTAs per request
-  size_t x_h, s_x, rho1, ssq1, h1, qkv, o_h, s_o, h1_h, s_h1, ssq2, a_h, s_a, out_acc, tick, total;
+  size_t x_h, s_x, rho1, ssq1, xres, h1, qkv, qkv_part, o_part, o_h, s_o, h1_h, s_h1, ssq2, a_h, s_a, down_part,
+      tick, total;
 };
 
 // Splits per (request, KV head): as many as keep every attention CTA resident in
@@ -162,7 +180,9 @@ static WsPlan make_plan(const ft_block_cfg& c, int B, int max_ctx) {
   // start (and fill their rings) while attention runs
   const int bud = 200 * 1024;
   const int per_sm = ft_host::smem_per_sm();
-  const int attn = attn_smem_bytes(c.n_q / c.n_kv, w.nsplit, c.head_dim);
+  // the partition (hence the QKV pieces attention stages) does not depend on the budget
+  const int np_qkv = make_gemv_plan(kRoleQKV, nqkv, c.hidden, B, sms, bud).npmax;
+  const int attn = attn_smem_bytes(c.n_q / c.n_kv, w.nsplit, c.head_dim, np_qkv);
   const int bud_att = per_sm > 0 ? std::min(bud, per_sm - attn - 3 * 1024) : bud;
   w.g[kRoleQKV] = make_gemv_plan(kRoleQKV, nqkv, c.hidden, B, sms, bud_att);
   w.g[kRoleO] = make_gemv_plan(kRoleO, c.hidden, c.n_q * c.head_dim, B, sms, bud_att);
@@ -174,21 +194,25 @@ static WsPlan make_plan(const ft_block_cfg& c, int B, int max_ctx) {
     off = align_up(off + bytes, 256);
     return o;
   };
+  const size_t sfx = sizeof(sfix_t);
   w.x_h = take((size_t)B * c.hidden * 2);
-  w.s_x = take((size_t)(c.hidden / 128) * 32 * 4);
+  w.s_x = take((size_t)(c.hidden / 128) * 32 * sfx);
   w.parts = rms_parts(c.hidden);
   w.rho1 = take((size_t)B * 4);
   w.ssq1 = take((size_t)B * w.parts * 4);
+  w.xres = take((size_t)B * c.hidden * 4);
   w.h1 = take((size_t)B * c.hidden * 4);
   w.qkv = take((size_t)B * nqkv * 4);
+  w.qkv_part = take((size_t)w.g[kRoleQKV].npmax * B * nqkv * 4);
+  w.o_part = take((size_t)w.g[kRoleO].npmax * B * c.hidden * 4);
   w.o_h = take((size_t)B * c.n_q * c.head_dim * 2);
-  w.s_o = take((size_t)(c.n_q * c.head_dim / 128) * 32 * 4);
+  w.s_o = take((size_t)(c.n_q * c.head_dim / 128) * 32 * sfx);
   w.h1_h = take((size_t)B * c.hidden * 2);
-  w.s_h1 = take((size_t)(c.hidden / 128) * 32 * 4);
+  w.s_h1 = take((size_t)(c.hidden / 128) * 32 * sfx);
   w.ssq2 = take((size_t)B * w.parts * 4);
   w.a_h = take((size_t)B * c.inter * 2);
-  w.s_a = take((size_t)(c.inter / 128) * 32 * 4);
-  w.out_acc = w.g[kRoleDown].whole ? 0 : take((size_t)B * c.hidden * 4);
+  w.s_a = take((size_t)(c.inter / 128) * 32 * sfx);
+  w.down_part = w.g[kRoleDown].whole ? 0 : take((size_t)w.g[kRoleDown].npmax * B * c.hidden * 4);
   w.tick = take((size_t)w.g[kRoleDown].NSET * 4);
   w.total = off;
   return w;
@@ -235,12 +259,16 @@ static int run_block(const ft_block_cfg* c, const ft_layer_weights* w, void* cac
   const size_t act_bytes = (size_t)B * c->hidden * (act_dtype == FT_F32 ? 4 : 2);
   if (overlaps(x_in, act_bytes, x_out, act_bytes)) return FT_ERR_INVALID_ARG;
   const WsPlan P = make_plan(*c, B, max_ctx);
+  for (int r = 0; r < 4; ++r)
+    if (!P.g[r].divs_exact) return FT_ERR_UNSUPPORTED;
+  if (P.g[kRoleQKV].npmax > kAttnMaxPieces) return FT_ERR_UNSUPPORTED;  // attention stages at most that many
   if (ws_bytes < P.total) return FT_ERR_WORKSPACE;
   if (overlaps(x_out, act_bytes, ws, ws_bytes) || overlaps(x_in, act_bytes, ws, ws_bytes)) return FT_ERR_INVALID_ARG;
 
   uint8_t* W = static_cast<uint8_t*>(ws);
   auto F = [&](size_t off) { return reinterpret_cast<float*>(W + off); };
   auto Hh = [&](size_t off) { return reinterpret_cast<__half*>(W + off); };
+  auto SF = [&](size_t off) { return reinterpret_cast<sfix_t*>(W + off); };
   const bool pdl = ft_host::pdl_enabled();
   const KVLayout L = kv_layout(*c, max_batch, max_ctx);
 
@@ -251,14 +279,12 @@ static int run_block(const ft_block_cfg* c, const ft_layer_weights* w, void* cac
     pp.B = B;
     pp.H = c->hidden;
     pp.x_h = Hh(P.x_h);
-    pp.s_x = F(P.s_x);
+    pp.s_x = SF(P.s_x);
     pp.ssq = F(P.ssq1);
-    pp.h1 = F(P.h1);
-    pp.qkv = F(P.qkv);
-    pp.nqkv = (c->n_q + 2 * c->n_kv) * c->head_dim;
-    pp.s_o = F(P.s_o);
+    pp.xres = F(P.xres);
+    pp.s_o = SF(P.s_o);
     pp.nkg_o = c->n_q * c->head_dim / 128;
-    pp.s_a = F(P.s_a);
+    pp.s_a = SF(P.s_a);
     pp.nkg_a = c->inter / 128;
     pp.tick = reinterpret_cast<uint32_t*>(W + P.tick);
     pp.ntick = P.g[kRoleDown].whole ? 0 : P.g[kRoleDown].NSET;
@@ -272,23 +298,25 @@ static int run_block(const ft_block_cfg* c, const ft_layer_weights* w, void* cac
     g.plan = P.g[role];
     g.w = static_cast<const uint8_t*>(wptr);
     g.x = Hh(xoff);
-    g.s_in = F(soff);
+    g.s_in = SF(soff);
     g.B = B;
     g.status = status;
     switch (role) {
-      case kRoleQKV: g.out_f32 = F(P.qkv); break;
-      case kRoleO: g.out_f32 = F(P.h1); break;
+      case kRoleQKV: g.part = F(P.qkv_part); break;
+      case kRoleO: g.part = F(P.o_part); break;
       case kRoleGU:
         g.out_h = Hh(P.a_h);
-        g.s_out = F(P.s_a);
+        g.s_out = SF(P.s_a);
         g.ssq2 = F(P.ssq2);
         g.nssq = P.parts;
         g.inv_h = 1.0f / (float)c->hidden;
         g.eps = c->rms_eps;
         break;
       case kRoleDown:
-        // whole sets read the residual h1; split sets accumulate into a copy of it
-        g.out_f32 = P.g[kRoleDown].whole ? F(P.h1) : F(P.out_acc);
+        // whole sets add the residual h1 directly; split sets store partial
+        // sums that the last piece of each set adds to h1
+        g.resid = F(P.h1);
+        g.part = P.g[kRoleDown].whole ? nullptr : F(P.down_part);
         g.tick = reinterpret_cast<uint32_t*>(W + P.tick);
         g.out_final = x_out;
         g.out_dtype = act_dtype;
@@ -302,6 +330,8 @@ static int run_block(const ft_block_cfg* c, const ft_layer_weights* w, void* cac
   }
   if (mask & FT_STAGE_ATTN) {
     AttnParams a;
+    a.qkv_part = F(P.qkv_part);
+    a.qkv_plan = P.g[kRoleQKV];
     a.qkv = F(P.qkv);
     a.ssq1 = F(P.ssq1);
     a.nssq = P.parts;
@@ -320,7 +350,7 @@ static int run_block(const ft_block_cfg* c, const ft_layer_weights* w, void* cac
     a.Nqkv = (c->n_q + 2 * c->n_kv) * c->head_dim;
     a.qscale = (float)(1.4426950408889634 / std::sqrt((double)c->head_dim));
     a.o_h = Hh(P.o_h);
-    a.s_o = F(P.s_o);
+    a.s_o = SF(P.s_o);
     a.status = status;
     rope_turns(c->rope_base, c->head_dim, a.rope_turn);
     if (launch_attn(a, c->head_dim, st, pdl) != cudaSuccess) return FT_ERR_CUDA;
@@ -330,13 +360,15 @@ static int run_block(const ft_block_cfg* c, const ft_layer_weights* w, void* cac
   }
   if (mask & FT_STAGE_MID) {
     MidParams mp = {};
-    mp.h1 = F(P.h1);
+    mp.xres = F(P.xres);
+    mp.o_part = F(P.o_part);
+    mp.o_plan = P.g[kRoleO];
     mp.B = B;
     mp.H = c->hidden;
+    mp.h1 = F(P.h1);
     mp.h1_h = Hh(P.h1_h);
-    mp.s_h1 = F(P.s_h1);
+    mp.s_h1 = SF(P.s_h1);
     mp.ssq = F(P.ssq2);
-    mp.out_acc = P.g[kRoleDown].whole ? nullptr : F(P.out_acc);
     mp.status = status;
     if (launch_ex(mid_kernel, dim3(P.parts, B), dim3(kPrepThreads), 0, st, pdl, mp) != cudaSuccess)
       return FT_ERR_CUDA;

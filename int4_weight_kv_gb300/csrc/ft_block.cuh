@@ -24,28 +24,67 @@ struct GemvPlan {
   // set's RT = tpw * NCW row tiles over all of a stage's groups, so one stage
   // of activations serves RT tiles (no cross-warp reduction)
   int ts, tpw;
+  // split partitions: the most pieces (CTAs) any set is divided into
+  int npmax;
+  // ceil(2^32 / (per + 1)) and ceil(2^32 / per): plan_owner divides with a
+  // multiply-high, exact because units * (per + 1) <= 2^32 (checked on the host)
+  unsigned long long rcp_per1, rcp_per;
+  int divs_exact;  // 0: the partition is too large for that division (refused)
 };
 
 __host__ __device__ __forceinline__ int plan_u0(const GemvPlan& p, int c) {
   const int u = c * p.per + (c < p.rem ? c : p.rem);
   return p.whole ? u * p.NKG : u;
 }
-// CTA owning unit u (split partitions only).
+// CTA owning unit u (split partitions only).  floor(n M / 2^32) with
+// M = ceil(2^32 / d) equals floor(n / d) whenever n d <= 2^32.
 __host__ __device__ __forceinline__ int plan_owner(const GemvPlan& p, int u) {
   const int big = p.rem * (p.per + 1);
-  return (u < big) ? u / (p.per + 1) : p.rem + (u - big) / p.per;
+  if (u < big) return (int)(((unsigned long long)u * p.rcp_per1) >> 32);
+  return p.rem + (int)(((unsigned long long)(u - big) * p.rcp_per) >> 32);
+}
+// Split partitions: the first CTA of set s, and how many CTAs (pieces) share it.
+__host__ __device__ __forceinline__ int plan_first(const GemvPlan& p, int s) { return plan_owner(p, s * p.NKG); }
+__host__ __device__ __forceinline__ int plan_pieces(const GemvPlan& p, int s) {
+  return plan_owner(p, s * p.NKG + p.NKG - 1) - plan_first(p, s) + 1;
+}
+// Split partitions write each piece's partial sums to its own slab: piece j of
+// a set to part[j][t][row] (slabs of B x N floats), so every piece writes whole
+// 32-byte sectors.  Consumers add the pieces of an output in slab order, so a
+// sum does not depend on which CTA finished first.  kPieceBatch pieces are
+// loaded together with no branch (absent pieces read as 0, which adds
+// exactly); more (large batches split sets into up to about 8 pieces) are added
+// one by one.
+constexpr int kPieceBatch = 4;
+template <int NB, typename T>
+__device__ __forceinline__ void pieces_load(const T* src, size_t slab, int np, T (&x)[NB]) {
+#pragma unroll
+  for (int u = 0; u < NB; ++u) x[u] = (u < np) ? __ldcg(src + u * slab) : T{};
+}
+__device__ __forceinline__ void piece_add(float& a, float b) { a += b; }
+__device__ __forceinline__ void piece_add(float4& a, const float4& b) {
+  a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
+}
+template <int NB, typename T>
+__device__ __forceinline__ T pieces_sum(const T* src, size_t slab, int np, const T (&x)[NB]) {
+  T v = x[0];
+#pragma unroll
+  for (int u = 1; u < NB; ++u) piece_add(v, x[u]);
+  for (int j = NB; j < np; ++j) piece_add(v, __ldcg(src + j * slab));
+  return v;
 }
 
 struct GemvParams {
   GemvPlan plan;
   const uint8_t* w;   // packed weights of this role
   const __half* x;    // activation operand, grouped layout of B rows (op_index)
-  const float* s_in;  // its group offsets [K/128][32]
+  const sfix_t* s_in; // its group offsets [K/128][32]
   int B;
   uint32_t* tick;     // DOWN (split sets): per-set completion tickets [NSET]
-  float* out_f32;     // QKV: qkv acc;  O: h1 acc;  DOWN: h1 (whole sets) or its copy accumulating split sets
+  float* part;        // QKV, O, DOWN split sets: piece slabs [npmax][B][N]
+  const float* resid; // DOWN: h1, the residual added to the block output
   __half* out_h;      // GU: a operand [B][I]
-  float* s_out;       // GU: a's group offsets [I/128][32] (accumulated)
+  sfix_t* s_out;      // GU: a's group offsets [I/128][32] (accumulated, exact)
   const float* ssq2;  // GU: partial sums of h1^2 [B][nssq], giving the RMSNorm row factor rho2
   int nssq;
   float inv_h, eps;   // GU: 1 / hidden, RMSNorm epsilon
@@ -55,7 +94,9 @@ struct GemvParams {
 };
 
 struct AttnParams {
-  const float* qkv;   // [B][Nqkv] accumulated projections, before rho1 and RoPE
+  const float* qkv_part;  // QKV piece slabs, before rho1 and RoPE
+  GemvPlan qkv_plan;      // the QKV partition that wrote them
+  float* qkv;         // [B][Nqkv] the summed projection, recorded for inspection
   const float* ssq1;  // [B][nssq] partial sums of x^2, giving the RMSNorm row factor rho1
   int nssq;
   float inv_h, eps;
@@ -66,42 +107,41 @@ struct AttnParams {
   int B, nq, nkv, G, hb, nsplit, Nqkv;
   float qscale;       // log2(e) / sqrt(d), folded into the rotated query
   __half* o_h;        // attention output, grouped operand layout of B rows (op_index)
-  float* s_o;         // its group offsets [nq d / 128][32] (accumulated)
+  sfix_t* s_o;        // its group offsets [nq d / 128][32] (accumulated, exact)
   int32_t* status;
   uint64_t rope_turn[64];  // inv_freq[i] / (2 pi) as 64-bit binary fractions (RoPE angles in turns)
 };
 
-// Block input -> QKV operand, partial sums of x^2, h1 accumulator initialised
-// to x, and the accumulators of this call cleared.  CTA (part, request) covers
-// 512 inputs (kPrepChunk chunks of 8).
+// Block input -> QKV operand, partial sums of x^2, an FP32 copy of x (the
+// residual), and the accumulators of this call cleared.  CTA (part, request)
+// covers 512 inputs (kPrepThreads chunks of 8).
 struct PrepParams {
   const void* x_in;
   int act_dtype, B, H;
   __half* x_h;       // operand, grouped layout (op_index)
-  float* s_x;        // [H/128][32]
+  sfix_t* s_x;       // [H/128][32]
   float* ssq;        // [B][parts] partial sums of x^2
-  float* h1;         // [B][H] <- x
-  float* qkv;        // [B][Nqkv] <- 0
-  int nqkv;
-  float* s_o;        // [NKG_o][32] <- 0 (column b)
+  float* xres;       // [B][H] <- x
+  sfix_t* s_o;       // [NKG_o][32] <- 0 (column b)
   int nkg_o;
-  float* s_a;        // [NKG_a][32] <- 0 (column b)
+  sfix_t* s_a;       // [NKG_a][32] <- 0 (column b)
   int nkg_a;
   uint32_t* tick;    // down completion tickets <- 0 (split sets only)
   int ntick;
   int32_t* status;
 };
 
-// Between O and gate/up: h1 -> its operand and offsets, partial sums of h1^2
-// and (split down sets) the down accumulator.  CTA (part, request) covers 512
-// inputs.
+// Between O and gate/up: h1 = x + the O projection's pieces, its operand and
+// offsets, and partial sums of h1^2.  CTA (part, request) covers 512 inputs.
 struct MidParams {
-  const float* h1;   // [B][H] complete after O
+  const float* xres;    // [B][H] block input (FP32 copy)
+  const float* o_part;  // O piece slabs
+  GemvPlan o_plan;
   int B, H;
+  float* h1;         // [B][H] <- x + W_o o
   __half* h1_h;      // operand, grouped layout (op_index)
-  float* s_h1;       // [H/128][32]
+  sfix_t* s_h1;      // [H/128][32]
   float* ssq;        // [B][parts] partial sums of h1^2
-  float* out_acc;    // [B][H] <- h1 (down accumulator of split sets) or null
   int32_t* status;
 };
 
@@ -112,20 +152,27 @@ __host__ __device__ __forceinline__ int rms_parts(int H) { return (H / 8 + kPrep
 cudaError_t launch_gemv(int role, const GemvParams& p, cudaStream_t st, bool pdl);
 cudaError_t launch_attn(const AttnParams& p, int head_dim, cudaStream_t st, bool pdl);
 constexpr int kAttnWarps = 4;  // warps per attention CTA (16-position tiles strided over them)
-// Dynamic shared memory of one attention CTA: the warps' partials of G heads and
-// the inbox of n_split * ceil(G / n_split) pushed partials, (d + 4) floats each.
-__host__ __device__ __forceinline__ int attn_dyn_smem(int G, int nsplit, int d) {
-  return (kAttnWarps * G + nsplit * ((G + nsplit - 1) / nsplit)) * (d + 4) * 4;
+// The attention kernel stages the QKV pieces it needs (G query heads, k and v:
+// (G + 2) d channels of each of at most kAttnMaxPieces pieces) in the area
+// that later holds its warps' partials.
+constexpr int kAttnMaxPieces = 8;
+__host__ __device__ __forceinline__ int attn_stage_floats(int G, int d, int npmax) { return (G + 2) * d * npmax; }
+// Dynamic shared memory of one attention CTA: the warps' partials of G heads
+// (or, before the main loop, the staged QKV pieces) and the inbox of
+// n_split * ceil(G / n_split) pushed partials, (d + 4) floats each.
+__host__ __device__ __forceinline__ int attn_dyn_smem(int G, int nsplit, int d, int npmax) {
+  const int mrg = kAttnWarps * G * (d + 4), stage = attn_stage_floats(G, d, npmax);
+  return ((mrg > stage ? mrg : stage) + nsplit * ((G + nsplit - 1) / nsplit) * (d + 4)) * 4;
 }
 // Static + dynamic shared memory of one attention CTA (host).
-int attn_smem_bytes(int G, int nsplit, int d);
+int attn_smem_bytes(int G, int nsplit, int d, int npmax);
 // Attention CTAs resident per SM (registers, shared memory), 0 if unknown (host).
 int attn_ctas_per_sm(int G, int d);
 // Largest cluster of attention CTAs the device schedules: 16 where the
 // non-portable size is allowed and fits, else 8 (host).
 int attn_max_cluster(int G, int d);
-// Gate/up and down CTAs own whole row-tile sets; QKV and O split sets over
-// CTAs along K (partial sums red.add-ed into an FP32 accumulator).
+// Gate/up CTAs own whole row-tile sets; QKV and O split sets over CTAs along K
+// (each piece's partial sums go to its own slab); down does either.
 GemvPlan make_gemv_plan(int role, int N, int K, int B, int sms, int smem_budget);
 
 template <typename... Args>

@@ -21,11 +21,13 @@
 //    mantissa trick) and run through mma.m16n8k16 with FP32 accumulation; the
 //    offset is removed by starting each group's chain at -S (see ft_internal).
 //  * warps reduce through shared memory at the end of a row-tile set.  QKV and
-//    O split sets along K across CTAs and red.add the partial sums into an FP32
-//    accumulator that the next kernel reads.  Gate/up CTAs own whole row-tile
-//    sets (SwiGLU in the epilogue); down owns whole sets where that balances
-//    (block output written directly) and otherwise splits them, the last piece
-//    of each set writing the output (completion ticket, never waits).
+//    O split sets along K across CTAs; each CTA's piece of a set stores its
+//    partial sums in its own slab and the next kernel adds the slabs in a fixed
+//    order (no floating-point atomics: results do not depend on which CTA
+//    finished first).  Gate/up CTAs own whole row-tile sets (SwiGLU in the
+//    epilogue); down owns whole sets where that balances (block output written
+//    directly) and otherwise splits them, the last piece of each set adding the
+//    slabs to h1 and writing the output (completion ticket, never waits).
 //  * batches of 17-32 (three or four token tiles) use gemv_ts_kernel below:
 //    each consumer warp owns whole row tiles of a wide set, so one activation
 //    stage serves many more weight rows.
@@ -51,20 +53,19 @@ constexpr int kDownRT = 2;
 template <int NT, int ROLE>
 constexpr int gemv_rt() { return ROLE == kRoleDown ? kDownRT : GemvShape<NT>::RT; }
 
-__device__ __forceinline__ void red_add(float* p, float v) { atomicAdd(p, v); }
-
 // Epilogue of one (row tile, column tile) of fully reduced values.
 // v[0] = (row g, token t0), v[1] = (row g, t0+1), v[2] = (row g+8, t0), v[3] = (row g+8, t0+1).
 // rho2_lane: lane t holds the RMSNorm row factor of token t (gate/up only).
+// direct: the piece is a whole set (down: write the block output);
+// piece: otherwise, this CTA's piece index within the set (its slab).
 template <int ROLE>
 __device__ __forceinline__ bool gemv_epi(const GemvParams& p, int T, int j, const float (&v)[4], bool direct,
-                                         float rho2_lane) {
+                                         float rho2_lane, int piece) {
   const int lane = threadIdx.x & 31, g = lane >> 2, tig = lane & 3;
   const int N = p.plan.N;
   const int r0 = T * kRowTile + g, r1 = r0 + 8;
   bool bad = false;
   if constexpr (ROLE == kRoleGU) {
-    const int inter = N / 2;
     const int kcol = 8 * T + g;  // a column produced by packed rows g (gate) and g + 8 (up)
     const int grp = kcol / kWGroup;
 #pragma unroll
@@ -81,30 +82,71 @@ __device__ __forceinline__ bool gemv_epi(const GemvParams& p, int T, int j, cons
       st += __shfl_xor_sync(0xffffffffu, st, 4);
       st += __shfl_xor_sync(0xffffffffu, st, 8);
       st += __shfl_xor_sync(0xffffffffu, st, 16);
-      if (g == 0 && t < p.B) atomicAdd(p.s_out + grp * 32 + t, st);
+      // the 16 row tiles of a group add exact integers: any order gives the same S
+      if (g == 0 && t < p.B) sfix_atomic_add(p.s_out + grp * 32 + t, f32_to_sfix(st));
     }
     return bad;
   } else {
 #pragma unroll
-  for (int r = 0; r < 4; ++r) {
-    const int t = 8 * j + 2 * tig + (r & 1);
-    if (t >= p.B) continue;
-    const int row = (r & 2) ? r1 : r0;
-    float* acc = p.out_f32 + (size_t)t * N + row;
-    if (ROLE == kRoleDown && direct) {
-      const float y = __ldcg(acc) + v[r];
-      if (p.out_dtype == FT_F32)
-        static_cast<float*>(p.out_final)[(size_t)t * N + row] = y;
-      else
-        static_cast<uint16_t*>(p.out_final)[(size_t)t * N + row] = __bfloat16_as_ushort(__float2bfloat16_rn(y));
-    } else {
-      red_add(acc, v[r]);
+    for (int r = 0; r < 4; ++r) {
+      const int t = 8 * j + 2 * tig + (r & 1);
+      if (t >= p.B) continue;
+      const int row = (r & 2) ? r1 : r0;
+      if (ROLE == kRoleDown && direct) {
+        const float y = __ldcg(p.resid + (size_t)t * N + row) + v[r];
+        if (p.out_dtype == FT_F32)
+          static_cast<float*>(p.out_final)[(size_t)t * N + row] = y;
+        else
+          static_cast<uint16_t*>(p.out_final)[(size_t)t * N + row] = __bfloat16_as_ushort(__float2bfloat16_rn(y));
+      } else {
+        __stcg(p.part + ((size_t)piece * p.B + t) * N + row, v[r]);
+      }
     }
-  }
-  return bad;
+    return bad;
   }
 }
 
+// Down projection, split set `set` whose last piece just finished here: the
+// block output of its rows is the pieces' slabs added in slab order, plus h1.
+// Threads take 4 consecutive rows of one token at a time.
+__device__ __forceinline__ void down_out4(const GemvParams& p, size_t at, const float4& y) {
+  if (p.out_dtype == FT_F32) {
+    *reinterpret_cast<float4*>(static_cast<float*>(p.out_final) + at) = y;
+  } else {
+    const uint32_t lo = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y.x)) |
+                        ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y.y)) << 16);
+    const uint32_t hi = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y.z)) |
+                        ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y.w)) << 16);
+    *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.out_final) + at) = make_uint2(lo, hi);
+  }
+}
+__device__ __forceinline__ void down_finish_set(const GemvParams& p, int set, int rows, int first_row, int i0,
+                                                int stride) {
+  const GemvPlan& pl = p.plan;
+  const int np = plan_pieces(pl, set);
+  const size_t slab4 = (size_t)p.B * pl.N / 4;
+  const int r4 = rows / 4, n = r4 * p.B;
+  for (int i = i0; i < n; i += stride) {
+    const size_t at = (size_t)(i / r4) * pl.N + first_row + 4 * (i % r4);  // 4 rows of one token
+    const float4* q = reinterpret_cast<const float4*>(p.part + at);
+    float4 x[kPieceBatch];
+    pieces_load<kPieceBatch>(q, slab4, np, x);
+    const float4 h = __ldcg(reinterpret_cast<const float4*>(p.resid + at));
+    float4 y = pieces_sum<kPieceBatch>(q, slab4, np, x);
+    piece_add(y, h);
+    down_out4(p, at, y);
+  }
+}
+
+// Programmatic dependent launch.  Every kernel of the block waits for its
+// predecessor before it exits, so a kernel's completion implies that of the
+// whole chain before it.  Most kernels let their successor launch at entry, so
+// its weight stream starts early.  The QKV projection lets the attention kernel
+// launch only after its own wait (every warp triggers after waiting): the prep kernel of
+// this call has then completed, hence the previous call on the stream too, and
+// the attention kernel's history loads issued before its own wait can never
+// overlap a previous call that wrote the same cache.
+//
 // Walks a CTA's unit range stage by stage (set, first group, group count) with
 // no divisions in the loop; every warp role runs the same walk.
 struct StageWalk {
@@ -138,7 +180,7 @@ struct StageWalk {
 // kernel (weights do not depend on it); their activation chunks right after.
 template <int RT>
 __device__ __forceinline__ void gemv_produce(const GemvParams& p, uint8_t* slots, uint32_t full0, uint32_t empty0,
-                                             int u0, int u1) {
+                                             int u0, int u1, bool trigger_after_wait) {
   const GemvPlan& pl = p.plan;
   const int lane = threadIdx.x & 31;
   const int S = pl.stages;
@@ -147,7 +189,7 @@ __device__ __forceinline__ void gemv_produce(const GemvParams& p, uint8_t* slots
     // the B rows of groups kg .. kg + ng - 1 are contiguous in the grouped layout
     if (lane == 0)
       bulk_g2s(smem_u32(sb + pl.xoff), p.x + (size_t)kg * p.B * kWGroup, p.B * ng * kWGroup * 2, full0 + 8 * slot);
-    if (lane == 31) bulk_g2s(smem_u32(sb + pl.soff), p.s_in + (size_t)kg * 32, ng * 128, full0 + 8 * slot);
+    if (lane == 31) bulk_g2s(smem_u32(sb + pl.soff), p.s_in + (size_t)kg * 32, ng * 256, full0 + 8 * slot);
   };
   bool waited = false;
   int s = 0, slot = 0, round = 0;
@@ -159,7 +201,7 @@ __device__ __forceinline__ void gemv_produce(const GemvParams& p, uint8_t* slots
     const int nrt = min(RT, pl.NTILE - st.set * RT);
     if (lane == 0)
       mbar_arrive_expect_tx(full0 + 8 * slot,
-                            (uint32_t)(nrt * st.ng * kSlabBytes + p.B * st.ng * kWGroup * 2 + st.ng * 128));
+                            (uint32_t)(nrt * st.ng * kSlabBytes + p.B * st.ng * kWGroup * 2 + st.ng * 256));
     __syncwarp();
     // one bulk copy per row tile, issued by lane rt (a single thread issuing them
     // one after another limits the stage rate for wide sets)
@@ -171,6 +213,7 @@ __device__ __forceinline__ void gemv_produce(const GemvParams& p, uint8_t* slots
     if (waited) issue_x(slot, st.kg, st.ng);
     if (!waited && (s == S - 1 || st.u + st.ng >= u1)) {
       griddep_wait();  // the activation operand comes from the previous kernel
+      if (trigger_after_wait) griddep_launch();
       waited = true;
       int ss = 0;
       for (StageWalk s2(pl, u0, u1); ss <= s; s2.next(), ++ss) issue_x(ss, s2.kg, s2.ng);
@@ -180,7 +223,10 @@ __device__ __forceinline__ void gemv_produce(const GemvParams& p, uint8_t* slots
       ++round;
     }
   }
-  if (!waited) griddep_wait();
+  if (!waited) {
+    griddep_wait();
+    if (trigger_after_wait) griddep_launch();
+  }
 }
 
 template <int NT, int ROLE>
@@ -200,7 +246,7 @@ __global__ void __launch_bounds__((GemvShape<NT>::NCW + 2) * 32, 1) gemv_kernel(
   uint8_t* zero_row = smem + pl.zerooff;  // stands in for activation rows of absent tokens
   uint8_t* slots = smem + pl.slotoff;
 
-  griddep_launch();
+  if (ROLE != kRoleQKV) griddep_launch();  // QKV: every warp after its own wait (note above StageWalk)
   for (int i = tid; i < pl.ng * kWGroup * 2 / 16; i += blockDim.x)
     reinterpret_cast<uint4*>(zero_row)[i] = make_uint4(0u, 0u, 0u, 0u);
   if (tid == 0) {
@@ -215,7 +261,7 @@ __global__ void __launch_bounds__((GemvShape<NT>::NCW + 2) * 32, 1) gemv_kernel(
   __syncthreads();
 
   if (warp == PRODUCER) {
-    gemv_produce<RT>(p, slots, full0, empty0, u0, u1);
+    gemv_produce<RT>(p, slots, full0, empty0, u0, u1, ROLE == kRoleQKV);
     return;
   }
 
@@ -224,6 +270,7 @@ __global__ void __launch_bounds__((GemvShape<NT>::NCW + 2) * 32, 1) gemv_kernel(
     // Reduces each finished piece over the consumer warps and applies the role
     // epilogue while the consumers already stream the next piece.
     griddep_wait();
+    if (ROLE == kRoleQKV) griddep_launch();
     // loaded once: a dependent global load per epilogue call would sit on the
     // critical path of every piece
     float rho2_lane = 0.0f;
@@ -239,6 +286,7 @@ __global__ void __launch_bounds__((GemvShape<NT>::NCW + 2) * 32, 1) gemv_kernel(
       if (!st.piece_end()) continue;
       const bool whole = (piece_kg0 == 0) && (st.kg + st.ng == pl.NKG);
       piece_kg0 = -1;
+      const int piece = cta - plan_first(pl, st.set);  // split sets: this piece's slab
       const int nrt = min(RT, pl.NTILE - st.set * RT);
       if (!mbar_wait(red_full, k & 1)) {
         set_status(p.status, FT_DEV_TIMEOUT);
@@ -255,31 +303,22 @@ __global__ void __launch_bounds__((GemvShape<NT>::NCW + 2) * 32, 1) gemv_kernel(
           for (int w = 0; w < NCW; ++w) a += red[((w * RT * NT + q) * 4 + r) * 32 + lane];
           v[r] = a;
         }
-        bad |= gemv_epi<ROLE>(p, st.set * RT + rt, j, v, whole, rho2_lane);
+        bad |= gemv_epi<ROLE>(p, st.set * RT + rt, j, v, whole, rho2_lane, piece);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(red_empty);
       if (ROLE == kRoleDown && !whole) {
-        // split set: the last of its pieces writes the block output from the
-        // h1 rows the pieces accumulated into (completion ticket, never waits)
+        // split set: the last of its pieces writes the block output from h1
+        // and the pieces' slabs (completion ticket, never waits)
         __threadfence();
         __syncwarp();
-        const int first = plan_owner(pl, st.set * pl.NKG);
-        const int np = plan_owner(pl, st.set * pl.NKG + pl.NKG - 1) - first + 1;
+        const int np = plan_pieces(pl, st.set);
         uint32_t last = 0;
         if (lane == 0) last = (atomicAdd(p.tick + st.set, 1u) == (uint32_t)(np - 1)) ? 1u : 0u;
         last = __shfl_sync(0xffffffffu, last, 0);
         if (last) {
           __threadfence();
-          const int rows = nrt * kRowTile;
-          for (int i = lane; i < rows * p.B; i += 32) {
-            const int t = i / rows, row = st.set * RT * kRowTile + i % rows;
-            const float y = __ldcg(p.out_f32 + (size_t)t * pl.N + row);
-            if (p.out_dtype == FT_F32)
-              static_cast<float*>(p.out_final)[(size_t)t * pl.N + row] = y;
-            else
-              static_cast<uint16_t*>(p.out_final)[(size_t)t * pl.N + row] = __bfloat16_as_ushort(__float2bfloat16_rn(y));
-          }
+          down_finish_set(p, st.set, nrt * kRowTile, st.set * RT * kRowTile, lane, 32);
           if (lane == 0) p.tick[st.set] = 0u;
         }
       }
@@ -291,6 +330,7 @@ __global__ void __launch_bounds__((GemvShape<NT>::NCW + 2) * 32, 1) gemv_kernel(
 
   // -------------------------------------------------------------- consumers
   griddep_wait();
+  if (ROLE == kRoleQKV) griddep_launch();
   const int g = lane >> 2, tig = lane & 3;
   float tot[RT][NT][4];
 #pragma unroll
@@ -309,7 +349,7 @@ __global__ void __launch_bounds__((GemvShape<NT>::NCW + 2) * 32, 1) gemv_kernel(
       return;
     }
     const uint8_t* sw = slots + slot * pl.slot;
-    const float* ss = reinterpret_cast<const float*>(sw + pl.soff);
+    const sfix_t* ss = reinterpret_cast<const sfix_t*>(sw + pl.soff);
     for (int kgl = warp; kgl < st.ng; kgl += NCW) {
       // activation rows of this lane's B fragments (tokens >= B read zeros) and
       // the group offsets -S for the lane's two token columns
@@ -320,9 +360,9 @@ __global__ void __launch_bounds__((GemvShape<NT>::NCW + 2) * 32, 1) gemv_kernel(
         const int row = 8 * j + g, t = 8 * j + 2 * tig;
         // row `row` of group kgl in the stage's grouped rows; absent tokens read zeros
         xr[j] = row < p.B ? sw + pl.xoff + (kgl * p.B + row) * (kWGroup * 2) : zero_row + kgl * (kWGroup * 2);
-        const float2 sv = *reinterpret_cast<const float2*>(ss + kgl * 32 + t);
-        c0[j][0] = (t < p.B) ? -sv.x : 0.0f;
-        c0[j][1] = (t + 1 < p.B) ? -sv.y : 0.0f;
+        const longlong2 sv = *reinterpret_cast<const longlong2*>(ss + kgl * 32 + t);
+        c0[j][0] = (t < p.B) ? -sfix_to_f32(sv.x) : 0.0f;
+        c0[j][1] = (t + 1 < p.B) ? -sfix_to_f32(sv.y) : 0.0f;
       }
       const uint8_t* slab0 = sw + kgl * kSlabBytes;
       // k-steps 0-3 and 4-7 of the group run as two independent MMA chains
@@ -443,7 +483,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) gemv_ts_kernel(const GemvPa
   uint8_t* zero_row = smem + pl.zerooff;
   uint8_t* slots = smem + pl.slotoff;
 
-  griddep_launch();
+  if (ROLE != kRoleQKV) griddep_launch();  // QKV: every warp after its own wait (note above StageWalk)
   for (int i = tid; i < pl.ng * kWGroup * 2 / 16; i += blockDim.x)
     reinterpret_cast<uint4*>(zero_row)[i] = make_uint4(0u, 0u, 0u, 0u);
   if (tid == 0) {
@@ -456,11 +496,12 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) gemv_ts_kernel(const GemvPa
   __syncthreads();
 
   if (warp == PRODUCER) {
-    gemv_produce<RT>(p, slots, full0, empty0, u0, u1);
+    gemv_produce<RT>(p, slots, full0, empty0, u0, u1, ROLE == kRoleQKV);
     return;
   }
 
   griddep_wait();
+  if (ROLE == kRoleQKV) griddep_launch();
   const int g = lane >> 2, tig = lane & 3;
   float rho2_lane = 0.0f;
   if (ROLE == kRoleGU && lane < p.B) {
@@ -485,7 +526,7 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) gemv_ts_kernel(const GemvPa
       return;
     }
     const uint8_t* sw = slots + slot * pl.slot;
-    const float* ss = reinterpret_cast<const float*>(sw + pl.soff);
+    const sfix_t* ss = reinterpret_cast<const sfix_t*>(sw + pl.soff);
     const int nrt = min(RT, pl.NTILE - st.set * RT);
     for (int kgl = 0; kgl < st.ng; ++kgl) {
       const uint8_t* xr[NT];
@@ -495,9 +536,9 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) gemv_ts_kernel(const GemvPa
         const int row = 8 * j + g, t = 8 * j + 2 * tig;
         // row `row` of group kgl in the stage's grouped rows; absent tokens read zeros
         xr[j] = row < p.B ? sw + pl.xoff + (kgl * p.B + row) * (kWGroup * 2) : zero_row + kgl * (kWGroup * 2);
-        const float2 sv = *reinterpret_cast<const float2*>(ss + kgl * 32 + t);
-        c0[j][0] = (t < p.B) ? -sv.x : 0.0f;
-        c0[j][1] = (t + 1 < p.B) ? -sv.y : 0.0f;
+        const longlong2 sv = *reinterpret_cast<const longlong2*>(ss + kgl * 32 + t);
+        c0[j][0] = (t < p.B) ? -sfix_to_f32(sv.x) : 0.0f;
+        c0[j][1] = (t + 1 < p.B) ? -sfix_to_f32(sv.y) : 0.0f;
       }
       uint32_t sc[TPW];
       float acc[TPW][NT][4];
@@ -562,12 +603,14 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) gemv_ts_kernel(const GemvPa
     if (st.piece_end()) {
       const bool whole = (piece_kg0 == 0) && (st.kg + st.ng == pl.NKG);
       piece_kg0 = -1;
+      const int piece = cta - plan_first(pl, st.set);  // split sets: this piece's slab
 #pragma unroll
       for (int t = 0; t < TPW; ++t) {
         const int rt = warp + t * NCW;
         if (rt < nrt) {
 #pragma unroll
-          for (int j = 0; j < NT; ++j) bad |= gemv_epi<ROLE>(p, st.set * RT + rt, j, tot[t][j], whole, rho2_lane);
+          for (int j = 0; j < NT; ++j)
+            bad |= gemv_epi<ROLE>(p, st.set * RT + rt, j, tot[t][j], whole, rho2_lane, piece);
         }
 #pragma unroll
         for (int j = 0; j < NT; ++j)
@@ -575,28 +618,16 @@ __global__ void __launch_bounds__((NCW + 1) * 32, 1) gemv_ts_kernel(const GemvPa
           for (int r = 0; r < 4; ++r) tot[t][j][r] = 0.0f;
       }
       if (ROLE == kRoleDown && !whole) {
-        // split set: every warp's red.adds of this piece are done before the
-        // ticket; the last piece writes the block output from the accumulator
+        // split set: every warp's slab stores of this piece are done before the
+        // ticket; the last piece writes the block output from h1 and the slabs
         __threadfence();
         consumer_sync(NCW * 32);
-        if (tid == 0) {
-          const int first = plan_owner(pl, st.set * pl.NKG);
-          const int np = plan_owner(pl, st.set * pl.NKG + pl.NKG - 1) - first + 1;
-          *tick_bcast = (atomicAdd(p.tick + st.set, 1u) == (uint32_t)(np - 1)) ? 1u : 0u;
-        }
+        if (tid == 0)
+          *tick_bcast = (atomicAdd(p.tick + st.set, 1u) == (uint32_t)(plan_pieces(pl, st.set) - 1)) ? 1u : 0u;
         consumer_sync(NCW * 32);
         if (*tick_bcast) {
           __threadfence();
-          const int rows = nrt * kRowTile;
-          for (int i = tid; i < rows * p.B; i += NCW * 32) {
-            const int t = i / rows, row = st.set * RT * kRowTile + i % rows;
-            const float y = __ldcg(p.out_f32 + (size_t)t * pl.N + row);
-            if (p.out_dtype == FT_F32)
-              static_cast<float*>(p.out_final)[(size_t)t * pl.N + row] = y;
-            else
-              static_cast<uint16_t*>(p.out_final)[(size_t)t * pl.N + row] =
-                  __bfloat16_as_ushort(__float2bfloat16_rn(y));
-          }
+          down_finish_set(p, st.set, nrt * kRowTile, st.set * RT * kRowTile, tid, NCW * 32);
           if (tid == 0) p.tick[st.set] = 0u;
         }
         consumer_sync(NCW * 32);  // the broadcast word is reused by the next piece
@@ -747,9 +778,15 @@ GemvPlan make_gemv_plan(int role, int N, int K, int B, int sms, int smem_budget)
   if (p.C < 1) p.C = 1;
   p.per = units / p.C;
   p.rem = units % p.C;
+  p.rcp_per1 = ((1ull << 32) + (unsigned long long)p.per) / (unsigned long long)(p.per + 1);  // ceil
+  p.rcp_per = ((1ull << 32) + (unsigned long long)p.per - 1) / (unsigned long long)p.per;     // ceil
+  p.divs_exact = (unsigned long long)units * (unsigned long long)(p.per + 1) <= (1ull << 32) ? 1 : 0;
+  p.npmax = 1;
+  if (!whole_sets)
+    for (int set = 0; set < p.NSET; ++set) p.npmax = std::max(p.npmax, plan_pieces(p, set));
   p.ng = p.NCW * 4 / p.RT;  // stages of 4 row tiles x NCW groups (a group per warp for RT = 4)
   if (p.ts) {  // stages of about 48 KB (weights of RT tiles + B activation rows per group)
-    const int per_group = p.RT * kSlabBytes + B * kWGroup * 2 + 128;
+    const int per_group = p.RT * kSlabBytes + B * kWGroup * 2 + 256;
     p.ng = std::max(1, 48 * 1024 / per_group);
   }
   if (p.ng > p.NKG) p.ng = p.NKG;
@@ -757,7 +794,7 @@ GemvPlan make_gemv_plan(int role, int N, int K, int B, int sms, int smem_budget)
   const int wbytes = p.RT * p.ng * kSlabBytes;
   p.xoff = (int)align_up((size_t)wbytes, 16);
   p.soff = (int)align_up((size_t)p.xoff + (size_t)B * p.xstride, 16);
-  p.slot = (int)align_up((size_t)p.soff + (size_t)p.ng * 128, 128);
+  p.slot = (int)align_up((size_t)p.soff + (size_t)p.ng * 256, 128);
   p.redoff = 256;
   const int redbytes = p.ts ? 128 : p.NCW * p.RT * p.NT * 128 * 4;  // tile-split: the ticket word
   p.zerooff = (int)align_up((size_t)p.redoff + (size_t)redbytes, 128);

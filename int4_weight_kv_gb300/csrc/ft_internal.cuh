@@ -78,6 +78,13 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared (L2 only), no register holds the
+// data in flight; cp_async_wait_all() waits for this thread's copies.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // L2 load issued where it stands (volatile: the compiler may not sink it to
 // its first use), for values fetched early and consumed much later.
 __device__ __forceinline__ float ld_cg_early(const float* p) {
@@ -242,11 +249,40 @@ __host__ __device__ __forceinline__ int op_index(int t, int k, int B) {
 __device__ __forceinline__ int op_frag_off(int ks, int tig, int key) {
   return ((((2 * ks) + (tig >> 1)) ^ key) << 4) + ((tig & 1) << 3);
 }
-// FP16 operand value of input k and its contribution to the group offset S.
+// Group offsets S.  Every FP16 value is a multiple of 2^-24 (the smallest
+// subnormal), so each term 1032 h or 1152 h is an exact FP32 value and an
+// integer number of 2^-24 units.  Terms are first summed in FP32 inside one
+// warp in a fixed order (deterministic), then converted once to a 64-bit count
+// of 2^-24 units; sums of those integers, across warps, CTAs and atomics, do
+// not depend on the order of their terms, so S is the same whichever CTA
+// finishes first.  It is rounded once more, to FP32, where an MMA chain starts
+// at -S.
+typedef long long sfix_t;
+// FP32 -> count of 2^-24 units (nearest), with 32-bit conversions only: the
+// value w = v 2^24 splits exactly into hi 2^32 + rem, 0 <= rem < 2^32.
+__device__ __forceinline__ sfix_t f32_to_sfix(float v) {
+  const float w = v * 16777216.0f;                         // exact (power of two)
+  const float hi = floorf(v * 0.00390625f);                // floor(w / 2^32), exact scaling
+  const float rem = fmaf(-hi, 4294967296.0f, w);           // the low bits of w: exact
+  return (sfix_t)((unsigned long long)(long long)__float2int_rn(hi) << 32) +
+         (sfix_t)__float2uint_rn(rem);
+}
+// Count of 2^-24 units -> FP32 from its two 32-bit halves (32-bit conversions
+// only); deterministic, within 2 FP32 ulps of the exact value.
+__device__ __forceinline__ float sfix_to_f32(sfix_t s) {
+  const float hi = __int2float_rn((int)(s >> 32)), lo = __uint2float_rn((unsigned)(unsigned long long)s);
+  return fmaf(hi, 4294967296.0f, lo) * 5.9604644775390625e-08f;  // x 2^-24
+}
+
+// FP16 operand value of input k and its contribution to the group offset S
+// (exact in FP32: an 11-bit significand times 1032 or 1152).
 __device__ __forceinline__ __half op_encode(float x, int k, float& s_term) {
   const __half h = __float2half_rn(op_high(k) ? x * 0.0625f : x);
   s_term = (op_high(k) ? kOffHi : kOffLo) * __half2float(h);
   return h;
+}
+__device__ __forceinline__ void sfix_atomic_add(sfix_t* p, sfix_t v) {
+  atomicAdd(reinterpret_cast<unsigned long long*>(p), (unsigned long long)v);
 }
 
 // ------------------------------------------------------------------ packed weights
@@ -369,6 +405,7 @@ __device__ __forceinline__ float warp_sum(float v) {
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   return v;
 }
+
 
 // Quantise one rotated d-vector (stride-32 ownership, kv_group = d) and write
 // its K- or V-entry nibbles and BF16 scale.  Returns the decoded values

@@ -11,8 +11,9 @@
 // the scratch space comes from here.
 //
 // Properties a caller must know:
-//  * the array is kStaticWorkspaceBytes (8 MiB) of device memory that every GPU
-//    loading this library keeps until the process exits;
+//  * the array is kStaticWorkspaceBytes (32 MiB) of device memory that every GPU
+//    loading this library keeps until the process exits (the largest layer
+//    shape here, 70B at batch 32, needs about 22 MiB);
 //  * problems whose workspace would exceed it are rejected with
 //    FT_ERR_WORKSPACE before anything is enqueued;
 //  * the array is shared by every call on a device and keeps the previous
@@ -22,14 +23,17 @@
 //    ordering) race on the array and produce wrong results;
 //  * the device address of the array is looked up with cudaGetSymbolAddress
 //    the first time the entry point runs on each device (with that device
-//    current); make that first call before any stream capture begins.
+//    current); make that first call before any stream capture begins.  The
+//    address is kept for the life of the process, so the entry point must not
+//    be used on a device after cudaDeviceReset (or any other teardown of its
+//    primary context) in the same process.
 #include <mutex>
 
 #include "ft_internal.cuh"
 
 namespace {
 
-constexpr size_t kStaticWorkspaceBytes = 8u << 20;
+constexpr size_t kStaticWorkspaceBytes = 32u << 20;
 
 // Device-side scratch.  In host code this name is only a handle for
 // cudaGetSymbolAddress, never a device address.

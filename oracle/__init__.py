@@ -39,7 +39,7 @@ from .weights import quantize_weight, int4_matvec
 from .kv import kv_quantize, KVCacheOracle
 from .attention import attend, attend_split, merge_partials
 from .block import decode_block, BlockWeightsOracle
-from .model import model_step
+from .model import model_step, embed, final_norm, lm_head
 
 __all__ = [
     "bf16_rne", "bf16_bits", "bf16_from_bits",
@@ -47,5 +47,5 @@ __all__ = [
     "sylvester", "blockdiag_apply", "inv_freq", "rope_apply",
     "quantize_weight", "int4_matvec", "kv_quantize", "KVCacheOracle",
     "attend", "attend_split", "merge_partials",
-    "decode_block", "BlockWeightsOracle", "model_step",
+    "decode_block", "BlockWeightsOracle", "model_step", "embed", "final_norm", "lm_head",
 ]

@@ -17,7 +17,7 @@ import oracle
 import synth
 import int4_weight_kv_gb300 as ft
 from int4_weight_kv_gb300 import runtime as rt
-from oracle.block import BlockWeightsOracle, decode_block, rms_factor
+from oracle.block import BlockWeightsOracle, decode_block
 from oracle.kv import KVCacheOracle
 from tests import gpu_harness as H
 
@@ -43,13 +43,11 @@ def test_embed_and_lm_head_small(B, V, Hd):
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     ft.check(ft.ft_embed_bf16(rt.bits_tensor(emb_bits), torch.from_numpy(tok).cuda(), x, B, V, Hd, st))
     torch.cuda.synchronize()
-    np.testing.assert_array_equal(x.cpu().numpy(), emb[tok])
+    np.testing.assert_array_equal(x.cpu().numpy(), oracle.embed(emb, tok))
     logits = torch.empty((B, V), dtype=torch.float32, device="cuda")
     ft.check(ft.ft_lm_head_bf16(x, torch.from_numpy(gamma).cuda(), rt.bits_tensor(lm_bits), logits, B, V, Hd, 1e-5))
     torch.cuda.synchronize()
-    xv = emb[tok].astype(np.float64)
-    z = gamma[None, :] * rms_factor(xv, 1e-5)[:, None] * xv
-    ref = z @ lm.astype(np.float64).T
+    ref = oracle.lm_head(oracle.final_norm(oracle.embed(emb, tok), gamma, 1e-5), lm)
     assert st.item() == 0
     assert H.rel_rms(logits.cpu().numpy(), ref) < 1e-4
 
@@ -64,8 +62,7 @@ def test_rmsnorm_and_device_status(B, H):
     z = torch.empty((B, H), dtype=torch.int16, device="cuda")
     ft.check(ft.ft_rmsnorm_bf16(torch.from_numpy(x).cuda(), torch.from_numpy(gamma).cuda(), z, B, H, 1e-5))
     got = synth.bf16_bits_to_f32(z.cpu().numpy().view(np.uint16)).astype(np.float64)
-    xv = x.astype(np.float64)
-    ref = gamma[None, :] * rms_factor(xv, 1e-5)[:, None] * xv
+    ref = oracle.final_norm(x, gamma, 1e-5)
     # FP32 arithmetic then one BF16 rounding: within one BF16 ulp of the FP64 value
     assert np.all(np.abs(got - ref) <= 2.0 ** -7 * np.abs(ref) + 1e-30)
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
@@ -112,7 +109,7 @@ def test_full_model_8b_32_layers_b1_ctx4096():
     logits = bufs["logits"].cpu().numpy()
     del layers, caches
 
-    x_ref = mt["emb"][mt["tokens"]].astype(np.float64)         # independent oracle chain
+    x_ref = oracle.embed(mt["emb"], mt["tokens"])               # independent oracle chain
     np.testing.assert_array_equal(xs[0], x_ref)
     worst = 0.0
     for li in range(nl):
@@ -126,11 +123,9 @@ def test_full_model_8b_32_layers_b1_ctx4096():
         assert gate <= 5e-3, (li, gate)
         assert H.max_abs_over_rms(xs[li + 1], forced["out"]) <= 2e-2, li
         x_ref = decode_block(s, wts, kc, x_ref, np.full(B, ctx), write_cache=False)["out"]
-    lm64 = mt["lm"].astype(np.float64)
-    zf = mt["gamma_final"][None, :] * rms_factor(xs[nl], s.rms_eps)[:, None] * xs[nl]
-    forced_head = H.rel_rms(logits, zf @ lm64.T)               # LM head on the GPU's own x_32
-    z = mt["gamma_final"][None, :] * rms_factor(x_ref, s.rms_eps)[:, None] * x_ref
-    e2e = H.rel_rms(logits, z @ lm64.T)                          # independent oracle chain
+    head = lambda xx: oracle.lm_head(oracle.final_norm(xx, mt["gamma_final"], s.rms_eps), mt["lm"])
+    forced_head = H.rel_rms(logits, head(xs[nl]))              # LM head on the GPU's own x_32
+    e2e = H.rel_rms(logits, head(x_ref))                         # independent oracle chain
     hidden = H.rel_rms(xs[nl], x_ref)
     print(f"worst teacher-forced layer rel RMS {worst:.2e}; LM head (teacher-forced) {forced_head:.2e}; "
           f"end-to-end hidden {hidden:.2e}, logits {e2e:.2e}")

@@ -402,3 +402,92 @@ def test_block_brute_force_tiny():
     r = decode_block(shape, wts, cache, x, np.array([3]), write_cache=False)
     want = _brute_block(shape, wts, cache, list(x[0]), 3)
     np.testing.assert_allclose(r["out"][0], want, rtol=1e-11, atol=1e-12)
+
+
+# ---------------------------------------------------------------- KV cache placement
+def test_kv_cache_append_places_each_token_at_its_position():
+    """Distinct rows per (request, token, head) land at [request, head, pos0 + token]
+    (offset(request, head, position, channel) placement); nothing else is touched."""
+    B, T, nkv, d, cap = 3, 4, 2, 8, 14
+    c = KVCacheOracle(B, nkv, cap, d, d, d)
+    pos0 = np.array([0, 5, 9])
+    g = np.random.default_rng(4)
+    pat = g.standard_normal(d)
+    k = np.empty((B, T, nkv, d))
+    v = np.empty((B, T, nkv, d))
+    for b in range(B):
+        for t in range(T):
+            for h in range(nkv):
+                amp = 1.0 + 100 * b + 10 * t + h          # a different scale for every slot
+                k[b, t, h] = amp * pat
+                v[b, t, h] = -amp * pat[::-1]
+    c.append(k, v, pos0)
+    seen = np.zeros((B, nkv, cap), bool)
+    for b in range(B):
+        for t in range(T):
+            for h in range(nkv):
+                p = pos0[b] + t
+                for cache_c, cache_s, row in ((c.kc, c.ks, k[b, t, h]), (c.vc, c.vs, v[b, t, h])):
+                    codes, sc, _ = kv_quantize(row, d, d)   # the row quantised on its own
+                    np.testing.assert_array_equal(cache_c[b, h, p], codes)
+                    np.testing.assert_array_equal(cache_s[b, h, p], sc)
+                seen[b, h, p] = True
+    assert np.all(c.kc[~seen] == 8) and np.all(c.vc[~seen] == 8)
+    assert np.all(c.ks[~seen] == 0) and np.all(c.vs[~seen] == 0)
+    assert len(np.unique(c.ks[seen])) == seen.sum()
+    # decoding reads the same slots back
+    np.testing.assert_array_equal(c.k_hat(2, 1, 13)[9:], oracle.dequantize_groups(c.kc[2, 1, 9:13], c.ks[2, 1, 9:13], d))
+
+
+# ---------------------------------------------------------------- full step
+TINY_MODEL = BlockShape(hidden=128, n_q=16, n_kv=4, head_dim=8, inter=128, rope_base=10000.0)
+
+
+def _tiny_model(n_layers=2, L=3, V=11, seed=21):
+    layers, caches = [], []
+    for li in range(n_layers):
+        _, wts, cache, _ = _mini_setup(shape=TINY_MODEL, B=1, L=L, seed=seed + li)
+        layers.append(wts)
+        caches.append(cache)
+    g = np.random.default_rng(seed + 100)
+    emb = g.normal(0, 1.0, (V, TINY_MODEL.hidden))
+    lm = g.normal(0, 0.05, (V, TINY_MODEL.hidden))
+    gamma = g.uniform(0.5, 1.5, TINY_MODEL.hidden)
+    return layers, caches, emb, lm, gamma, np.array([4])
+
+
+def test_model_step_two_layers_brute_force():
+    """Embedding lookup, two blocks, final RMSNorm and LM head against explicit loops."""
+    s, L = TINY_MODEL, 3
+    layers, caches, emb, lm, gamma, tokens = _tiny_model(L=L)
+    x = [float(v) for v in emb[tokens[0]]]
+    for wts, cache in zip(layers, caches):         # before model_step writes the new entries
+        x = _brute_block(s, wts, cache, x, L)
+    rho = 1 / math.sqrt(sum(v * v for v in x) / s.hidden + s.rms_eps)
+    z = [gamma[i] * rho * x[i] for i in range(s.hidden)]
+    want = [sum(lm[v][k] * z[k] for k in range(s.hidden)) for v in range(lm.shape[0])]
+    logits, res = oracle.model_step(s, layers, caches, emb, lm, gamma, tokens, np.array([L]))
+    assert len(res) == 2
+    np.testing.assert_allclose(logits[0], want, rtol=1e-10, atol=1e-12)
+
+
+def test_model_step_final_gain_axis_and_lm_head_orientation():
+    """A one-hot final gain keeps one channel of z; a single nonzero W_lm[v, k]
+    moves exactly logit v by W_lm[v, k] z[k]; teacher-forced inputs are used as given."""
+    s, L = TINY_MODEL, 3
+    layers, caches, emb, lm, gamma, tokens = _tiny_model(n_layers=1, L=L)
+    xf = np.random.default_rng(3).standard_normal((1, s.hidden)) * 3
+    rho = 1 / math.sqrt(float(np.mean(xf[0] ** 2)) + s.rms_eps)
+    g1 = np.zeros(s.hidden)
+    g1[37] = 1.0
+    logits, _ = oracle.model_step(s, layers, caches, emb, lm, g1, tokens, np.array([L]), final_input=xf)
+    np.testing.assert_allclose(logits[0], lm[:, 37] * rho * xf[0, 37], rtol=1e-13, atol=1e-300)
+    lm1 = np.zeros_like(lm)
+    lm1[5, 37] = 0.5
+    logits, _ = oracle.model_step(s, layers, caches, emb, lm1, gamma, tokens, np.array([L]), final_input=xf)
+    assert np.count_nonzero(logits[0]) == 1
+    np.testing.assert_allclose(logits[0, 5], 0.5 * gamma[37] * rho * xf[0, 37], rtol=1e-13)
+    xin = np.random.default_rng(8).standard_normal((1, s.hidden))
+    _, res = oracle.model_step(s, layers, caches, emb, lm, gamma, tokens, np.array([L]), layer_inputs=[xin])
+    np.testing.assert_allclose(res[0]["h1"] - res[0]["attn_delta"], xin, rtol=0, atol=1e-14)
+    np.testing.assert_array_equal(res[0]["rho1"], rms_factor(xin, s.rms_eps))
