@@ -4,10 +4,11 @@ RMSNorm, BF16 LM head) through the C ABI against the CPU oracle.
 Per layer the oracle is teacher-forced with the GPU's own layer input, so each
 of the 32 blocks is held to the block tolerances on its own, and the final
 RMSNorm + LM head is checked on the GPU's own last hidden state.  The logits
-are also compared with a fully independent oracle chain; that difference grows
-with depth (a random-init network amplifies the per-block rounding differences
-through the residual stream), so it is reported and only guarded against gross
-errors.
+are also compared with a fully independent oracle chain.  That difference grows
+with depth: tests/golden/e2e_spread.txt (written by the oracle alone) shows
+that a relative error of 2.8e-4 to 5.6e-4 RMS on every block output, the size
+of the kernels' FP16 operand rounding, moves the 32-layer logits by 1.6e-2 to
+3.2e-2; the end-to-end gate is twice the largest spread recorded there.
 """
 import numpy as np
 import pytest
@@ -20,6 +21,7 @@ from int4_weight_kv_gb300 import runtime as rt
 from oracle.block import BlockWeightsOracle, decode_block
 from oracle.kv import KVCacheOracle
 from tests import gpu_harness as H
+from tests.conftest import golden_path
 
 pytestmark = pytest.mark.gpu
 
@@ -71,6 +73,12 @@ def test_rmsnorm_and_device_status(B, H):
     out = torch.empty((1, H), dtype=torch.float32, device="cuda")
     ft.check(ft.ft_embed_bf16(emb, torch.tensor([9], dtype=torch.int32, device="cuda"), out, 1, 4, H, st))
     assert ft.ft_read_device_status(st) & ft.FT_DEV_RANGE
+
+
+def _e2e_logit_gate() -> float:
+    """Twice the largest oracle-only logit spread under per-block rounding-size errors."""
+    rows = [l.split() for l in open(golden_path("e2e_spread.txt")) if l.strip() and not l.startswith("#")]
+    return 2.0 * max(float(r[3]) for r in rows)
 
 
 def test_full_model_8b_32_layers_b1_ctx4096():
@@ -130,4 +138,4 @@ def test_full_model_8b_32_layers_b1_ctx4096():
     print(f"worst teacher-forced layer rel RMS {worst:.2e}; LM head (teacher-forced) {forced_head:.2e}; "
           f"end-to-end hidden {hidden:.2e}, logits {e2e:.2e}")
     assert forced_head <= 5e-3
-    assert e2e <= 0.1, "end-to-end logits far from the oracle chain"
+    assert e2e <= _e2e_logit_gate(), "end-to-end logits beyond what per-block rounding explains"
