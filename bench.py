@@ -304,6 +304,11 @@ def run_ours(args):
     torch.cuda.synchronize()
     e2e_us = e0.elapsed_time(e1) * 1000.0 / n_e2e
 
+    # per-replay spread of the headline (outside the timed region)
+    g_all = graph_of(R)
+    spread = _time_graph(g_all, max(10, min(args.steps, 200)), R)
+    sweep = None if (args.profile or args.no_sweep) else run_sweep(args, device, hbm_peak()[0])
+
     line = {
         "metric": METRIC, "value": round(us_step, 3), "unit": "us/step", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": us_step / 1000.0, "higher_is_better": False, "scaling": "weak",
@@ -326,6 +331,9 @@ def run_ours(args):
                 "d2h_bytes_per_step": B * s.hidden * 2},
         "gpu_launches": ft.ft_decode_block_launches() * args.steps,
         "clocks": clk,
+        "us_p10": round(float(np.percentile(spread, 10)), 3), "us_median": round(float(np.median(spread)), 3),
+        "us_p90": round(float(np.percentile(spread, 90)), 3),
+        "sweep": sweep,
     }
     if rank == 0:
         line["cpu_baseline"] = None if args.profile else cpu_baseline(wl)
@@ -335,6 +343,217 @@ def run_ours(args):
     if world > 1:
         dist.barrier(device_ids=[local])
         dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------- the metric's sweep
+# (shape, [(batch, context)]) of the metric's batch range on the 8B and 70B layer shapes; the 8B rows at
+# context 1024 (batch 1 is the headline workload), 8B batch 32 at context 4096 (the attention-dominated
+# configuration), the 70B rows at context 2048 and 70B batch 1 at context 32768 (the split-KV reduction).
+SWEEP = (("8B", 2, ((1, 1024), (2, 1024), (4, 1024), (8, 1024), (16, 1024), (32, 1024), (32, 4096))),
+         ("70B", 4, ((1, 2048), (2, 2048), (4, 2048), (8, 2048), (16, 2048), (32, 2048), (1, 32768))))
+
+
+def stage_bytes(shape, B: int, ctx: int, per_role: dict) -> dict:
+    """Algorithmic bytes of each stage that streams a large operand (one launch)."""
+    import int4_weight_kv_gb300 as ft
+    s = shape
+    kv_tok = s.n_kv * 2 * (s.head_dim // 2 + 2 * (s.head_dim // s.kvg))
+    return {ft.FT_STAGE_ATTN: B * (ctx + 1) * kv_tok,
+            ft.FT_STAGE_GU: per_role[ft.FT_W_GATEUP] + B * (s.hidden + s.inter) * 2,
+            ft.FT_STAGE_DOWN: per_role[ft.FT_W_DOWN] + B * (s.inter + 2 * s.hidden) * 2,
+            ft.FT_STAGE_QKV: per_role[ft.FT_W_QKV] + B * (s.hidden * 2 + s.n_qkv * 4)}
+
+
+STAGE_NAMES = {1: "prep", 2: "qkv projection", 4: "attention", 8: "o projection", 16: "mid", 32: "gate/up + SwiGLU",
+               64: "down projection"}
+
+
+def _pct(a: float, b: float) -> float:
+    return round(100.0 * a / b, 1)
+
+
+def _time_graph(g, n: int, per: int) -> list:
+    """Per-step times (us) of n replays of a graph holding `per` steps."""
+    import torch
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+    evs[0].record()
+    for i in range(n):
+        g.replay()
+        evs[i + 1].record()
+    torch.cuda.synchronize()
+    return [evs[i].elapsed_time(evs[i + 1]) * 1000.0 / per for i in range(n)]
+
+
+def run_sweep(args, device, peak: float) -> list:
+    """Every (layer shape, batch, context) of the metric: one graph of R steps over R replicas
+    (R * footprint >= 4x L2), per-replay CUDA events; the stage with the most algorithmic bytes timed
+    alone for its roofline."""
+    import torch
+    import synth
+    import int4_weight_kv_gb300 as ft
+    from int4_weight_kv_gb300 import runtime as rt
+    shapes = {"8B": synth.L8B, "70B": synth.L70B}
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    out = []
+    n_rep = max(10, min(args.steps, 200))
+    for sname, cid, points in SWEEP:
+        s = shapes[sname]
+        cfg = ft.cfg_from_shape(s)
+        w = synth.device_layer_weights(s, cid, 0, device)
+        packed = [rt.pack_layer(cfg, {k: v for k, v in w.items()}, device=device)]
+        del w
+        per_role = {r: ft.ft_packed_weight_bytes(cfg, r) for r in ft.ROLES}
+        wbytes = sum(per_role.values())
+        for B, ctx in points:
+            ab = algorithmic_bytes(s, B, ctx)
+            R = max(2, int(np.ceil(4 * l2 / (ab["weights"] + ab["kv"]))))
+            while len(packed) < R:
+                packed.append({k: v.clone() for k, v in packed[0].items()})
+            max_ctx = ctx + 1
+            cache0 = rt.alloc_cache(cfg, B, max_ctx, device=device)
+            chunk = max(1, (1 << 26) // (B * s.n_kv * s.head_dim))
+            for t0 in range(0, ctx, chunk):
+                t1 = min(ctx, t0 + chunk)
+                kb = synth.device_kv_history(s, cid, B, t0, t1, "k", device)
+                vb = synth.device_kv_history(s, cid, B, t0, t1, "v", device)
+                pos0 = torch.full((B,), t0, dtype=torch.int32, device=device)
+                ft.check(ft.ft_kv_append_int4(cfg, cache0, B, max_ctx, kb, vb, pos0, B, t1 - t0), "ft_kv_append_int4")
+                del kb, vb
+            reps = [{"w": packed[r], "cache": cache0 if r == 0 else cache0.clone(),
+                     "x": synth.device_activations(s, cid, B, device),
+                     "y": torch.empty((B, s.hidden), dtype=torch.int16, device=device),
+                     "ws": rt.alloc_workspace(cfg, B, max_ctx, device=device)} for r in range(R)]
+            pos = torch.full((B,), ctx, dtype=torch.int32, device=device)
+            st = torch.zeros(1, dtype=torch.int32, device=device)
+
+            def step(r, mask=ft.FT_STAGE_ALL):
+                p = reps[r]
+                ft.check(ft.ft_decode_block_stages(cfg, p["w"], p["cache"], B, max_ctx, p["x"], p["y"], ft.FT_BF16,
+                                                   pos, B, p["ws"], mask, st), "ft_decode_block")
+            for r in range(R):
+                step(r)
+            torch.cuda.synchronize()
+            side = torch.cuda.Stream(device)
+            side.wait_stream(torch.cuda.current_stream(device))
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=side):
+                for r in range(R):
+                    step(r)
+            for _ in range(max(args.warmup, 3)):
+                g.replay()
+            torch.cuda.synchronize()
+            ts = _time_graph(g, n_rep, R)
+            if int(st.item()) != 0:
+                raise RuntimeError(f"device status {st.item()} at {sname} B={B} ctx={ctx}")
+            med = float(np.median(ts))
+            # dominant stage: the most algorithmic bytes; timed alone, replicas cycled
+            sb = stage_bytes(s, B, ctx, per_role)
+            dom = max(sb, key=lambda k: sb[k])
+            n_dom = R * 20
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for i in range(n_dom):
+                step(i % R, dom)
+            e1.record()
+            torch.cuda.synchronize()
+            st.zero_()  # stages re-run alone may re-accumulate offsets: timing only
+            dom_us = e0.elapsed_time(e1) * 1000.0 / n_dom
+            ach = sb[dom] / dom_us / 1e3
+            out.append({
+                "workload": f"{sname.lower()}_b{B}_ctx{ctx}", "batch": B, "ctx": ctx, "replicas": R,
+                "us_step": round(med, 2), "us_p10": round(float(np.percentile(ts, 10)), 2),
+                "us_p90": round(float(np.percentile(ts, 90)), 2), "replays": n_rep,
+                "algorithmic_bytes": ab["total"], "gbs": round(ab["total"] / med / 1e3, 1),
+                "pct_of_measured_hbm": _pct(ab["total"] / med / 1e3, peak),
+                "pct_of_8tbs": _pct(ab["total"] / med / 1e3, NOMINAL_HBM_GBS),
+                "dominant": {"stage": STAGE_NAMES[dom], "launch_us": round(dom_us, 2), "algorithmic_bytes": sb[dom],
+                             "achieved_gbs": round(ach, 1), "frac": round(ach / peak, 3)},
+            })
+            print(json.dumps(out[-1]), file=sys.stderr, flush=True)
+            del reps, cache0, g
+            torch.cuda.empty_cache()
+        del packed
+        torch.cuda.empty_cache()
+    out.append(run_full_step(args, device, peak))
+    return out
+
+
+def run_full_step(args, device, peak: float) -> dict:
+    """The full 32-layer Llama-3.1-8B decode step at batch 1, context 4096: embedding, 32 decode blocks
+    (FP32 residual between layers), final RMSNorm + BF16 LM head (vocab 128256), one CUDA graph."""
+    import torch
+    import synth
+    import int4_weight_kv_gb300 as ft
+    from int4_weight_kv_gb300 import runtime as rt
+    wl = synth.workload("8b_full_b1_ctx4096")
+    s, B, ctx, nl, V = wl.shape, wl.batch, wl.ctx, wl.layers, wl.vocab
+    cfg = ft.cfg_from_shape(s)
+    max_ctx = ctx + 1
+    layers, caches = [], []
+    for li in range(nl):
+        w = synth.device_layer_weights(s, wl.config_id, li, device)
+        layers.append(rt.pack_layer(cfg, w, device=device))
+        del w
+        c = rt.alloc_cache(cfg, B, max_ctx, device=device)
+        kb = synth.device_kv_history(s, wl.config_id, B, 0, ctx, "k", device, layer=li)
+        vb = synth.device_kv_history(s, wl.config_id, B, 0, ctx, "v", device, layer=li)
+        ft.check(ft.ft_kv_append_int4(cfg, c, B, max_ctx, kb, vb, torch.zeros(B, dtype=torch.int32, device=device),
+                                      B, ctx), "ft_kv_append_int4")
+        caches.append(c)
+        del kb, vb
+    mt = synth.device_model_tensors(s, wl.config_id, V, B, device)
+    pos = torch.full((B,), ctx, dtype=torch.int32, device=device)
+    bufs = {"x": torch.empty((B, s.hidden), dtype=torch.float32, device=device),
+            "y": torch.empty((B, s.hidden), dtype=torch.float32, device=device),
+            "logits": torch.empty((B, V), dtype=torch.float32, device=device)}
+    ws = [rt.alloc_workspace(cfg, B, max_ctx, device=device)]
+    st = torch.zeros(1, dtype=torch.int32, device=device)
+
+    def step():
+        rt.model_step(cfg, layers, caches, B, max_ctx, mt["emb_bits"], mt["lm_bits"], mt["gamma_final"],
+                      mt["tokens"], pos, bufs, ws, st)
+    step()
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream(device)
+    side.wait_stream(torch.cuda.current_stream(device))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=side):
+        step()
+    for _ in range(max(args.warmup, 3)):
+        g.replay()
+    torch.cuda.synchronize()
+    n = max(10, min(args.steps, 100))
+    ts = _time_graph(g, n, 1)
+    if int(st.item()) != 0:
+        raise RuntimeError(f"device status {st.item()} in the full step")
+    med = float(np.median(ts))
+    per_role = {r: ft.ft_packed_weight_bytes(cfg, r) for r in ft.ROLES}
+    kv_tok = s.n_kv * 2 * (s.head_dim // 2 + 2 * (s.head_dim // s.kvg))
+    lm_bytes = V * s.hidden * 2
+    floor = nl * (sum(per_role.values()) + B * (ctx + 1) * kv_tok) + lm_bytes
+    # the LM head (the largest single launch) timed alone
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    k = 20
+    e0.record()
+    for _ in range(k):
+        ft.check(ft.ft_lm_head_bf16(bufs["x"], mt["gamma_final"], mt["lm_bits"], bufs["logits"], B, V, s.hidden,
+                                    cfg.rms_eps), "ft_lm_head_bf16")
+    e1.record()
+    torch.cuda.synchronize()
+    lm_us = e0.elapsed_time(e1) * 1000.0 / k
+    res = {"workload": "8b_full_b1_ctx4096", "layers": nl, "batch": B, "ctx": ctx, "vocab": V,
+           "us_step": round(med, 1), "us_p10": round(float(np.percentile(ts, 10)), 1),
+           "us_p90": round(float(np.percentile(ts, 90)), 1), "replays": n,
+           "algorithmic_bytes": floor, "gbs": round(floor / med / 1e3, 1),
+           "pct_of_measured_hbm": _pct(floor / med / 1e3, peak), "pct_of_8tbs": _pct(floor / med / 1e3, NOMINAL_HBM_GBS),
+           "dominant": {"stage": "lm head (BF16, final RMSNorm fused)", "launch_us": round(lm_us, 2),
+                        "algorithmic_bytes": lm_bytes, "achieved_gbs": round(lm_bytes / lm_us / 1e3, 1),
+                        "frac": round(lm_bytes / lm_us / 1e3 / peak, 3)},
+           "context": "the pages quote 2.8 ms per full Llama-3.1-8B decode step at batch 1 on one H100 (not comparable)"}
+    print(json.dumps(res), file=sys.stderr, flush=True)
+    del layers, caches, mt, g
+    torch.cuda.empty_cache()
+    return res
 
 
 # ---------------------------------------------------------------------------- oracle timing
@@ -417,6 +636,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="only the headline workload (skip the batch 1-32 sweep and the full 32-layer step)")
     ap.add_argument("--profile", action="store_true",
                     help="short run for a profiler: no clock hold, no oracle baseline; numbers are not bench values")
     args = ap.parse_args()

@@ -16,14 +16,14 @@ ROLE_NAMES = {FT_W_QKV: "qkv", FT_W_O: "o", FT_W_GATEUP: "gateup", FT_W_DOWN: "d
 
 
 def _dev(a, dtype=None, device="cuda"):
-    t = torch.from_numpy(np.ascontiguousarray(a))
+    t = a.contiguous() if isinstance(a, torch.Tensor) else torch.from_numpy(np.ascontiguousarray(a))
     if dtype is not None:
         t = t.to(dtype)
     return t.to(device)
 
 
 def pack_layer(cfg, w: dict, device="cuda", stream=None) -> dict:
-    """Pack the four projections of one layer from FP32 host arrays (synth layout)."""
+    """Pack the four projections of one layer from FP32 arrays or tensors (synth layout)."""
     out = {}
     for role, (wk, gk) in ROLE_KEYS.items():
         W = _dev(w[wk], device=device)

@@ -22,6 +22,7 @@ __all__ = [
     "BlockShape", "Workload", "WORKLOADS", "workload", "rng",
     "layer_weights", "activations", "kv_history", "positions",
     "model_tensors", "bf16_bits_to_f32",
+    "device_layer_weights", "device_activations", "device_kv_history", "device_model_tensors",
 ]
 
 
@@ -179,3 +180,64 @@ def model_tensors(shape: BlockShape, config_id: int, vocab: int, batch: int) -> 
     tok = rng(config_id, 0, T_TOK).integers(0, vocab, size=batch).astype(np.int32)
     return {"emb_bits": emb_bits, "emb": emb_f, "lm_bits": lm_bits, "lm": lm_f,
             "gamma_final": gfin, "tokens": tok}
+
+
+# ---------------------------------------------------------------------------
+# Device-side draws for large timing workloads.  Same distributions as the
+# NumPy draws above (weights N(0, 0.02), gains U(0.5, 1.5), activations and K/V
+# history N(0, 1) with fixed outlier channels x20), drawn on the GPU from a
+# seeded torch generator so that multi-GB workloads (70B layers, the 32-layer
+# step, batch-32 histories) are ready in seconds.  Not bit-identical to the NumPy
+# draws; used where only the shapes and value distributions matter (timing).
+
+def _dev_gen(device, *seed_parts: int):
+    g = torch.Generator(device=device)
+    g.manual_seed(int(np.random.SeedSequence(list(seed_parts)).generate_state(1)[0]))
+    return g
+
+
+def device_layer_weights(shape: BlockShape, config_id: int, layer: int, device) -> dict:
+    """FP32 device tensors with the layout of ``layer_weights``."""
+    s = shape
+    g = _dev_gen(device, config_id, layer, 1000)
+    return {
+        "wqkv": torch.empty((s.n_qkv, s.hidden), device=device).normal_(0.0, 0.02, generator=g),
+        "wo": torch.empty((s.hidden, s.n_q * s.head_dim), device=device).normal_(0.0, 0.02, generator=g),
+        "wgu": torch.empty((2 * s.inter, s.hidden), device=device).normal_(0.0, 0.02, generator=g),
+        "wdown": torch.empty((s.hidden, s.inter), device=device).normal_(0.0, 0.02, generator=g),
+        "gamma_attn": torch.empty(s.hidden, device=device).uniform_(0.5, 1.5, generator=g),
+        "gamma_ffn": torch.empty(s.hidden, device=device).uniform_(0.5, 1.5, generator=g),
+    }
+
+
+def device_activations(shape: BlockShape, config_id: int, batch: int, device, n_outliers: int = 2,
+                       outlier_scale: float = 20.0) -> torch.Tensor:
+    """BF16 block input [batch, hidden] as int16 bits on the device."""
+    g = _dev_gen(device, config_id, 0, 1010)
+    x = torch.empty((batch, shape.hidden), device=device).normal_(0.0, 1.0, generator=g)
+    ch = torch.randperm(shape.hidden, device=device, generator=g)[:n_outliers]
+    x[:, ch] *= outlier_scale
+    return x.to(torch.bfloat16).view(torch.int16)
+
+
+def device_kv_history(shape: BlockShape, config_id: int, batch: int, t0: int, t1: int, which: str, device,
+                      layer: int = 0, n_outliers: int = 4, outlier_scale: float = 20.0) -> torch.Tensor:
+    """BF16 K or V history positions [t0, t1) as int16 bits [batch, t1 - t0, n_kv, head_dim]; the outlier
+    channels of each head are fixed per (config, layer, K/V), the values per chunk."""
+    gch = _dev_gen(device, config_id, layer, 1020 + (which == "v"))
+    a = torch.empty((batch, t1 - t0, shape.n_kv, shape.head_dim), device=device)
+    a.normal_(0.0, 1.0, generator=_dev_gen(device, config_id, layer, 1030 + (which == "v"), t0))
+    for h in range(shape.n_kv):
+        ch = torch.randperm(shape.head_dim, device=device, generator=gch)[:n_outliers]
+        a[:, :, h, ch] *= outlier_scale
+    return a.to(torch.bfloat16).view(torch.int16)
+
+
+def device_model_tensors(shape: BlockShape, config_id: int, vocab: int, batch: int, device) -> dict:
+    """Embedding and LM head BF16 N(0, 0.02) (int16 bits), final gain U(0.5, 1.5), token ids."""
+    g = _dev_gen(device, config_id, 0, 1040)
+    emb = torch.empty((vocab, shape.hidden), device=device).normal_(0.0, 0.02, generator=g)
+    lm = torch.empty((vocab, shape.hidden), device=device).normal_(0.0, 0.02, generator=g)
+    return {"emb_bits": emb.to(torch.bfloat16).view(torch.int16), "lm_bits": lm.to(torch.bfloat16).view(torch.int16),
+            "gamma_final": torch.empty(shape.hidden, device=device).uniform_(0.5, 1.5, generator=g),
+            "tokens": torch.randint(0, vocab, (batch,), device=device, generator=g, dtype=torch.int32)}
