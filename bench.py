@@ -329,7 +329,7 @@ def run_ours(args):
                      "launch_us": round(dom_us, 3), "algorithmic_bytes": dom_bytes},
         "e2e": {"value": round(e2e_us, 3), "unit": "us/step", "h2d_bytes_per_step": B * s.hidden * 2 + B * 4,
                 "d2h_bytes_per_step": B * s.hidden * 2},
-        "gpu_launches": ft.ft_decode_block_launches() * args.steps,
+        "gpu_launches": ft.ft_decode_block_launches(B) * args.steps,
         "clocks": clk,
         "us_p10": round(float(np.percentile(spread, 10)), 3), "us_median": round(float(np.median(spread)), 3),
         "us_p90": round(float(np.percentile(spread, 90)), 3),

@@ -187,11 +187,11 @@ int ft_decode_block_stages(const ft_block_cfg *cfg, const ft_layer_weights *w, v
  * RoPE);  rho1 FP32 [B];  o FP16, n_q d values per request (attention output
  * after the inverse rotation);  h1 FP32 [B, H];  a FP16, I values per request
  * (SwiGLU output).  o and a are stored in the projections' grouped operand
- * layout: [inputs / 128][B][128], i.e. the B requests' values of each group of
- * 128 inputs together; within a request's 128 values the order is
- * 0,1,8,9,2,3,10,11,4,5,12,13,6,7,14,15 per 16 inputs, inputs 8..15 of each 16
- * hold value / 16, and the 16 runs of 8 stored values are permuted: run r is
- * stored at position r XOR (request mod 8). */
+ * layout: [inputs / 64][B][64], i.e. the B requests' values of each half group
+ * of 64 inputs together (one 128-byte row per request); within a request's 64
+ * values the order is 0,1,8,9,2,3,10,11,4,5,12,13,6,7,14,15 per 16 inputs,
+ * inputs 8..15 of each 16 hold value / 16, and the 8 runs of 8 stored values
+ * are permuted: run r is stored at position r XOR (request mod 8). */
 typedef struct {
   size_t qkv, rho1, o, h1, a;
   int32_t n_split; /* split-KV chunks per (request, KV head) */
@@ -201,13 +201,14 @@ int ft_decode_workspace_layout(const ft_block_cfg *cfg, int B, int max_ctx, ft_w
 
 /* How ft_decode_block partitions one projection (role FT_W_*) for this batch
  * on the current device (148 SMs assumed when no device is visible): ctas
- * launched; rows per set (row_tiles x 16);
- * consumer warps; 8-token column tiles; whole = 1 when every CTA owns whole
- * sets (no split along the inputs); tile_split = 1 for the large-batch kernel
- * in which each warp owns whole row tiles; ring stages, groups (128 inputs)
- * per stage and dynamic shared memory per CTA in bytes. */
+ * launched; rows per set (row_tiles x 16); warps per CTA; 8-token column tiles;
+ * whole = 1 when every CTA owns whole sets (no split along the inputs);
+ * tensor_core = 1 for the tcgen05 kernel of batches 17-32 (128-row sets, the
+ * contraction on the fifth-generation tensor cores), 0 for the streaming
+ * mma.sync kernel of batches 1-16; ring stages, groups (128 inputs) per stage
+ * and dynamic shared memory per CTA in bytes. */
 typedef struct {
-  int32_t ctas, row_tiles, warps, col_tiles, whole, tile_split, stages, groups_per_stage, smem_bytes;
+  int32_t ctas, row_tiles, warps, col_tiles, whole, tensor_core, stages, groups_per_stage, smem_bytes;
 } ft_gemv_info;
 int ft_decode_plan_info(const ft_block_cfg *cfg, int B, int max_ctx, int role, ft_gemv_info *out);
 
@@ -247,10 +248,10 @@ int ft_lm_head_bf16(const float *x, const float *gamma, const uint16_t *W, float
  * device memory when they run a step (a pool or allocation policy that forbids
  * new device allocations after start-up, a host that hands over only input and
  * output buffers, or a loop that must not pay for an allocation).  The scratch
- * space is a fixed 32 MiB device array inside this library, held by every GPU
+ * space is a fixed 48 MiB device array inside this library, held by every GPU
  * that loads it until the process exits; problems needing more (see
  * ft_decode_workspace_bytes; the 70B layer shape at batch 32 needs about
- * 22 MiB) return FT_ERR_WORKSPACE and enqueue nothing.  No memory is allocated
+ * 33 MiB) return FT_ERR_WORKSPACE and enqueue nothing.  No memory is allocated
  * by this call.  The array is shared by all calls on a device and keeps the
  * previous call's contents (the block clears what it needs itself); calls that
  * overlap on the GPU race on it.  The first call on each device looks up the
@@ -262,8 +263,11 @@ int ft_decode_block_static_ws(const ft_block_cfg *cfg, const ft_layer_weights *w
                               int max_ctx, const void *x_in, void *x_out, int act_dtype, const int32_t *pos, int B,
                               int32_t *dev_status, ft_stream stream);
 
-/* Number of kernels one ft_decode_block call launches. */
-int ft_decode_block_launches(void);
+/* Number of kernels one ft_decode_block call with batch B launches: 7 for
+ * B <= 16; 9 for 17 <= B <= 32, where the projections run on the tensor cores
+ * and two small kernels finish gate/up (SwiGLU) and the block output from the
+ * projections' per-piece partial sums. */
+int ft_decode_block_launches(int B);
 
 /* Programmatic dependent launch between the block's kernels (default on).
  * Returns the previous setting. */

@@ -35,7 +35,7 @@ class LayerWeights(ctypes.Structure):
 
 
 class GemvInfo(ctypes.Structure):
-    _fields_ = [(n, c_int32) for n in ("ctas", "row_tiles", "warps", "col_tiles", "whole", "tile_split", "stages",
+    _fields_ = [(n, c_int32) for n in ("ctas", "row_tiles", "warps", "col_tiles", "whole", "tensor_core", "stages",
                                        "groups_per_stage", "smem_bytes")]
 
 
@@ -79,7 +79,7 @@ _SIGS = {
     "ft_rmsnorm_bf16": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_float, c_void_p]),
     "ft_read_device_status": (c_int, [c_void_p, c_void_p, c_void_p]),
     "ft_decode_plan_info": (c_int, [c_void_p, c_int, c_int, c_int, c_void_p]),
-    "ft_decode_block_launches": (c_int, []),
+    "ft_decode_block_launches": (c_int, [c_int]),
     "ft_set_pdl": (c_int, [c_int]),
 }
 
@@ -251,8 +251,8 @@ def ft_decode_plan_info(cfg, B: int, max_ctx: int, role: int) -> GemvInfo:
     return out
 
 
-def ft_decode_block_launches() -> int:
-    return lib().ft_decode_block_launches()
+def ft_decode_block_launches(B: int = 1) -> int:
+    return lib().ft_decode_block_launches(int(B))
 
 
 def ft_set_pdl(enabled: bool) -> bool:

@@ -145,12 +145,91 @@ __global__ void __launch_bounds__(kPrepThreads) mid_kernel(const MidParams p) {
   if (bad) set_status(p.status, FT_DEV_RANGE);
 }
 
+// Gate/up slabs (tensor-core path) -> the down projection's operand: a =
+// silu(rho2 g) * (rho2 u) for 128 columns (one group of the operand) and up to 8
+// tokens per CTA; the group offsets are summed over the CTA's four warps in a
+// fixed order and stored (one CTA owns a (group, token)).  Gate row g and up row
+// g + 8 of a 16-row packed tile give column 8 T + g.
+__global__ void __launch_bounds__(128) swiglu_kernel(const SwigluParams p) {
+  __shared__ float wsum[4][8];
+  __shared__ float rho2_s[8];
+  griddep_launch();  // the down projection may start streaming its weights
+  const int grp = blockIdx.x, t0 = 8 * blockIdx.y, c = threadIdx.x, warp = c >> 5, lane = c & 31;
+  const int kcol = grp * kWGroup + c;
+  const int T = kcol >> 3, r = kcol & 7;
+  const int row_g = 16 * T + r, row_u = row_g + 8;
+  const GemvPlan& pl = p.plan;
+  const int np = plan_pieces(pl, row_g / (pl.RT * kRowTile));
+  const size_t slab = (size_t)p.B * pl.N;
+  griddep_wait();
+  float xg[8][kPieceBatch], xu[8][kPieceBatch];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {  // every slab load of the CTA's tokens in flight together
+    const int t = t0 + i;
+    const int n = t < p.B ? np : 0;
+    pieces_load<kPieceBatch>(p.part + (size_t)t * pl.N + row_g, slab, n, xg[i]);
+    pieces_load<kPieceBatch>(p.part + (size_t)t * pl.N + row_u, slab, n, xu[i]);
+  }
+  if (c < 8) {  // the RMSNorm row factor of each of the CTA's tokens, once
+    float a = 0.0f;
+    if (t0 + c < p.B)
+      for (int k = 0; k < p.nssq; ++k) a += __ldcg(p.ssq2 + (t0 + c) * p.nssq + k);
+    rho2_s[c] = rsqrtf(a * p.inv_h + p.eps);
+  }
+  __syncthreads();
+  bool bad = false;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int t = t0 + i;
+    float st = 0.0f;
+    if (t < p.B) {
+      const float rho2 = rho2_s[i];
+      const float gv = rho2 * pieces_sum<kPieceBatch>(p.part + (size_t)t * pl.N + row_g, slab, np, xg[i]);
+      const float uv = rho2 * pieces_sum<kPieceBatch>(p.part + (size_t)t * pl.N + row_u, slab, np, xu[i]);
+      const float a = gv / (1.0f + expf(-gv)) * uv;
+      bad |= !(fabsf(a) <= 65504.0f);
+      p.out_h[op_index(t, kcol, p.B)] = op_encode(a, kcol, st);
+    }
+    st = warp_sum(st);
+    if (lane == 0) wsum[warp][i] = st;
+  }
+  __syncthreads();
+  if (c < 8 && t0 + c < p.B) {
+    const float st = ((wsum[0][c] + wsum[1][c]) + wsum[2][c]) + wsum[3][c];  // fixed order
+    p.s_out[grp * 32 + t0 + c] = f32_to_sfix(st);
+  }
+  if (bad) set_status(p.status, FT_DEV_RANGE);
+}
+
+// Down slabs (tensor-core path) + h1 -> the block output; 4 rows of one token
+// per thread.
+__global__ void __launch_bounds__(128) post_kernel(const PostParams p) {
+  griddep_launch();
+  const GemvPlan& pl = p.plan;
+  const int t = blockIdx.y, row = 512 * blockIdx.x + 4 * threadIdx.x;
+  const bool on = row < pl.N;
+  const int np = on ? plan_pieces(pl, row / (pl.RT * kRowTile)) : 0;
+  const size_t at = (size_t)t * pl.N + (on ? row : 0), slab4 = (size_t)p.B * pl.N / 4;
+  const float4* q = reinterpret_cast<const float4*>(p.part + at);
+  griddep_wait();
+  if (!on) return;
+  float4 x[kPieceBatch];
+  pieces_load<kPieceBatch>(q, slab4, np, x);
+  const float4 h = __ldcg(reinterpret_cast<const float4*>(p.resid + at));
+  float4 y = pieces_sum<kPieceBatch>(q, slab4, np, x);
+  piece_add(y, h);
+  GemvParams gp = {};
+  gp.out_final = p.out_final;
+  gp.out_dtype = p.out_dtype;
+  down_out4(gp, at, y);
+}
+
 struct WsPlan {
   GemvPlan g[4];
   int nsplit;
   int parts;  // prep / mid CTAs per request
-  size_t x_h, s_x, rho1, ssq1, xres, h1, qkv, qkv_part, o_part, o_h, s_o, h1_h, s_h1, ssq2, a_h, s_a, down_part,
-      tick, total;
+  size_t x_h, s_x, rho1, ssq1, xres, h1, qkv, qkv_part, o_part, o_h, s_o, h1_h, s_h1, ssq2, a_h, s_a, gu_part,
+      down_part, tick, total;
 };
 
 // Splits per (request, KV head): as many as keep every attention CTA resident in
@@ -180,14 +259,16 @@ static WsPlan make_plan(const ft_block_cfg& c, int B, int max_ctx) {
   // start (and fill their rings) while attention runs
   const int bud = 200 * 1024;
   const int per_sm = ft_host::smem_per_sm();
+  // batches of 17-32 run the projections on the tensor cores (tcgen05)
+  auto plan = B > 16 ? make_umma_plan : make_gemv_plan;
   // the partition (hence the QKV pieces attention stages) does not depend on the budget
-  const int np_qkv = make_gemv_plan(kRoleQKV, nqkv, c.hidden, B, sms, bud).npmax;
+  const int np_qkv = plan(kRoleQKV, nqkv, c.hidden, B, sms, bud).npmax;
   const int attn = attn_smem_bytes(c.n_q / c.n_kv, w.nsplit, c.head_dim, np_qkv);
   const int bud_att = per_sm > 0 ? std::min(bud, per_sm - attn - 3 * 1024) : bud;
-  w.g[kRoleQKV] = make_gemv_plan(kRoleQKV, nqkv, c.hidden, B, sms, bud_att);
-  w.g[kRoleO] = make_gemv_plan(kRoleO, c.hidden, c.n_q * c.head_dim, B, sms, bud_att);
-  w.g[kRoleGU] = make_gemv_plan(kRoleGU, 2 * c.inter, c.hidden, B, sms, bud);
-  w.g[kRoleDown] = make_gemv_plan(kRoleDown, c.hidden, c.inter, B, sms, bud);
+  w.g[kRoleQKV] = plan(kRoleQKV, nqkv, c.hidden, B, sms, bud_att);
+  w.g[kRoleO] = plan(kRoleO, c.hidden, c.n_q * c.head_dim, B, sms, bud_att);
+  w.g[kRoleGU] = plan(kRoleGU, 2 * c.inter, c.hidden, B, sms, bud);
+  w.g[kRoleDown] = plan(kRoleDown, c.hidden, c.inter, B, sms, bud);
   size_t off = 0;
   auto take = [&](size_t bytes) {
     const size_t o = off;
@@ -212,6 +293,8 @@ static WsPlan make_plan(const ft_block_cfg& c, int B, int max_ctx) {
   w.ssq2 = take((size_t)B * w.parts * 4);
   w.a_h = take((size_t)B * c.inter * 2);
   w.s_a = take((size_t)(c.inter / 128) * 32 * sfx);
+  // tensor-core path: gate/up writes slabs too (the SwiGLU kernel finishes them)
+  w.gu_part = w.g[kRoleGU].umma ? take((size_t)w.g[kRoleGU].npmax * B * 2 * c.inter * 4) : 0;
   w.down_part = w.g[kRoleDown].whole ? 0 : take((size_t)w.g[kRoleDown].npmax * B * c.hidden * 4);
   w.tick = take((size_t)w.g[kRoleDown].NSET * 4);
   w.total = off;
@@ -305,6 +388,7 @@ static int run_block(const ft_block_cfg* c, const ft_layer_weights* w, void* cac
       case kRoleQKV: g.part = F(P.qkv_part); break;
       case kRoleO: g.part = F(P.o_part); break;
       case kRoleGU:
+        g.part = P.g[kRoleGU].umma ? F(P.gu_part) : nullptr;
         g.out_h = Hh(P.a_h);
         g.s_out = SF(P.s_a);
         g.ssq2 = F(P.ssq2);
@@ -373,11 +457,38 @@ static int run_block(const ft_block_cfg* c, const ft_layer_weights* w, void* cac
     if (launch_ex(mid_kernel, dim3(P.parts, B), dim3(kPrepThreads), 0, st, pdl, mp) != cudaSuccess)
       return FT_ERR_CUDA;
   }
+  const bool umma = P.g[kRoleGU].umma != 0;
   if (mask & FT_STAGE_GU) {
     if (gemv(kRoleGU, w->gateup, P.h1_h, P.s_h1) != cudaSuccess) return FT_ERR_CUDA;
+    if (umma) {
+      SwigluParams sp = {};
+      sp.part = F(P.gu_part);
+      sp.plan = P.g[kRoleGU];
+      sp.B = B;
+      sp.ssq2 = F(P.ssq2);
+      sp.nssq = P.parts;
+      sp.inv_h = 1.0f / (float)c->hidden;
+      sp.eps = c->rms_eps;
+      sp.out_h = Hh(P.a_h);
+      sp.s_out = SF(P.s_a);
+      sp.status = status;
+      if (launch_ex(swiglu_kernel, dim3(c->inter / kWGroup, (B + 7) / 8), dim3(128), 0, st, pdl, sp) != cudaSuccess)
+        return FT_ERR_CUDA;
+    }
   }
   if (mask & FT_STAGE_DOWN) {
     if (gemv(kRoleDown, w->down, P.a_h, P.s_a) != cudaSuccess) return FT_ERR_CUDA;
+    if (umma) {
+      PostParams op = {};
+      op.part = F(P.down_part);
+      op.plan = P.g[kRoleDown];
+      op.resid = F(P.h1);
+      op.out_final = x_out;
+      op.out_dtype = act_dtype;
+      op.B = B;
+      if (launch_ex(post_kernel, dim3((c->hidden + 511) / 512, B), dim3(128), 0, st, pdl, op) != cudaSuccess)
+        return FT_ERR_CUDA;
+    }
   }
   return FT_OK;
 }
@@ -415,10 +526,10 @@ int ft_decode_plan_info(const ft_block_cfg* c, int B, int max_ctx, int role, ft_
   const ft::GemvPlan& g = P.g[r];
   out->ctas = g.C;
   out->row_tiles = g.RT;
-  out->warps = g.NCW;
+  out->warps = g.umma ? ft::ft_umma_warps() : g.NCW + 2;
   out->col_tiles = g.NT;
   out->whole = g.whole;
-  out->tile_split = g.ts;
+  out->tensor_core = g.umma;
   out->stages = g.stages;
   out->groups_per_stage = g.ng;
   out->smem_bytes = g.smem;
@@ -440,6 +551,6 @@ int ft_decode_block_stages(const ft_block_cfg* c, const ft_layer_weights* w, voi
                        (cudaStream_t)stream);
 }
 
-int ft_decode_block_launches(void) { return 7; }
+int ft_decode_block_launches(int B) { return B > 16 ? 9 : 7; }
 
 }  // extern "C"

@@ -20,16 +20,13 @@ struct GemvPlan {
   int ng;                      // groups per stage
   int stages, slot, xoff, soff, xstride;  // ring geometry (bytes)
   int redoff, zerooff, slotoff, smem;  // shared-memory map
-  // tile-split consumers (large batches): each consumer warp owns tpw of the
-  // set's RT = tpw * NCW row tiles over all of a stage's groups, so one stage
-  // of activations serves RT tiles (no cross-warp reduction)
-  int ts, tpw;
   // split partitions: the most pieces (CTAs) any set is divided into
   int npmax;
   // ceil(2^32 / (per + 1)) and ceil(2^32 / per): plan_owner divides with a
   // multiply-high, exact because units * (per + 1) <= 2^32 (checked on the host)
   unsigned long long rcp_per1, rcp_per;
   int divs_exact;  // 0: the partition is too large for that division (refused)
+  int umma;        // 1: the tensor-core (tcgen05) kernel, 128-row sets, every role may split sets
 };
 
 __host__ __device__ __forceinline__ int plan_u0(const GemvPlan& p, int c) {
@@ -74,6 +71,33 @@ __device__ __forceinline__ T pieces_sum(const T* src, size_t slab, int np, const
   return v;
 }
 
+// Walks a CTA's unit range stage by stage (set, first group, group count) with
+// no divisions in the loop; every warp role runs the same walk.
+struct StageWalk {
+  int u, u1, set, kg, ng, NKG, cap;
+  __device__ __forceinline__ StageWalk(const GemvPlan& pl, int u0, int u1_) {
+    u = u0;
+    u1 = u1_;
+    NKG = pl.NKG;
+    cap = pl.ng;
+    set = u0 / NKG;
+    kg = u0 - set * NKG;
+    ng = min(min(cap, NKG - kg), u1 - u);
+  }
+  __device__ __forceinline__ bool valid() const { return u < u1; }
+  // true if the stage just finished ends this CTA's piece of its set
+  __device__ __forceinline__ bool piece_end() const { return u + ng >= u1 || kg + ng == NKG; }
+  __device__ __forceinline__ void next() {
+    u += ng;
+    kg += ng;
+    if (kg == NKG) {
+      kg = 0;
+      ++set;
+    }
+    ng = min(min(cap, NKG - kg), u1 - u);
+  }
+};
+
 struct GemvParams {
   GemvPlan plan;
   const uint8_t* w;   // packed weights of this role
@@ -92,6 +116,38 @@ struct GemvParams {
   int out_dtype;
   int32_t* status;
 };
+
+// Down projection, split set `set` whose last piece just finished here: the
+// block output of its rows is the pieces' slabs added in slab order, plus h1.
+// Threads take 4 consecutive rows of one token at a time.
+__device__ __forceinline__ void down_out4(const GemvParams& p, size_t at, const float4& y) {
+  if (p.out_dtype == FT_F32) {
+    *reinterpret_cast<float4*>(static_cast<float*>(p.out_final) + at) = y;
+  } else {
+    const uint32_t lo = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y.x)) |
+                        ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y.y)) << 16);
+    const uint32_t hi = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y.z)) |
+                        ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y.w)) << 16);
+    *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.out_final) + at) = make_uint2(lo, hi);
+  }
+}
+__device__ __forceinline__ void down_finish_set(const GemvParams& p, int set, int rows, int first_row, int i0,
+                                                int stride) {
+  const GemvPlan& pl = p.plan;
+  const int np = plan_pieces(pl, set);
+  const size_t slab4 = (size_t)p.B * pl.N / 4;
+  const int r4 = rows / 4, n = r4 * p.B;
+  for (int i = i0; i < n; i += stride) {
+    const size_t at = (size_t)(i / r4) * pl.N + first_row + 4 * (i % r4);  // 4 rows of one token
+    const float4* q = reinterpret_cast<const float4*>(p.part + at);
+    float4 x[kPieceBatch];
+    pieces_load<kPieceBatch>(q, slab4, np, x);
+    const float4 h = __ldcg(reinterpret_cast<const float4*>(p.resid + at));
+    float4 y = pieces_sum<kPieceBatch>(q, slab4, np, x);
+    piece_add(y, h);
+    down_out4(p, at, y);
+  }
+}
 
 struct AttnParams {
   const float* qkv_part;  // QKV piece slabs, before rho1 and RoPE
@@ -145,11 +201,38 @@ struct MidParams {
   int32_t* status;
 };
 
+// Batches of 17-32 (tensor-core projections, every set split into slabs):
+// gate/up slabs -> a = silu(rho2 g) (rho2 u), the down projection's operand and
+// its group offsets.  CTA (group of 128 columns, 8 tokens), one column per thread.
+struct SwigluParams {
+  const float* part;  // gate/up piece slabs [npmax][B][2I]
+  GemvPlan plan;      // the gate/up partition that wrote them
+  int B;
+  const float* ssq2;  // [B][nssq] partial sums of h1^2 (rho2)
+  int nssq;
+  float inv_h, eps;
+  __half* out_h;      // a operand (op_index)
+  sfix_t* s_out;      // its group offsets [I/128][32] (written, exact)
+  int32_t* status;
+};
+// down slabs + h1 -> block output.  CTA (512 rows, token), 4 rows per thread.
+struct PostParams {
+  const float* part;  // down piece slabs [npmax][B][H]
+  GemvPlan plan;
+  const float* resid; // h1 [B][H]
+  void* out_final;
+  int out_dtype, B;
+};
+
 constexpr int kPrepThreads = 64;  // threads (chunks of 8 inputs) per prep / mid CTA
 __host__ __device__ __forceinline__ int rms_parts(int H) { return (H / 8 + kPrepThreads - 1) / kPrepThreads; }
 
-// host-side launchers (ft_gemv.cu / ft_attn.cu / ft_block.cu)
+// host-side launchers (ft_gemv.cu / ft_umma.cu / ft_attn.cu / ft_block.cu)
 cudaError_t launch_gemv(int role, const GemvParams& p, cudaStream_t st, bool pdl);
+cudaError_t launch_umma(int role, const GemvParams& p, cudaStream_t st, bool pdl);
+// Partition for the tensor-core kernel (batches of 17-32): 128-row sets.
+GemvPlan make_umma_plan(int role, int N, int K, int B, int sms, int smem_budget);
+int ft_umma_warps();  // warps per CTA of the tensor-core kernel
 cudaError_t launch_attn(const AttnParams& p, int head_dim, cudaStream_t st, bool pdl);
 constexpr int kAttnWarps = 4;  // warps per attention CTA (16-position tiles strided over them)
 // The attention kernel stages the QKV pieces it needs (G query heads, k and v:

@@ -28,9 +28,8 @@
 //    epilogue); down owns whole sets where that balances (block output written
 //    directly) and otherwise splits them, the last piece of each set adding the
 //    slabs to h1 and writing the output (completion ticket, never waits).
-//  * batches of 17-32 (three or four token tiles) use gemv_ts_kernel below:
-//    each consumer warp owns whole row tiles of a wide set, so one activation
-//    stage serves many more weight rows.
+//  * batches of 17-32 run on the tensor-core kernel (tcgen05, ft_umma.cu)
+//    instead; this kernel serves 1-16 tokens (one or two column tiles).
 #include <algorithm>
 
 #include "ft_block.cuh"
@@ -43,8 +42,6 @@ template <int NT>
 struct GemvShape;
 template <> struct GemvShape<1> { static constexpr int RT = 4, NCW = 8; };
 template <> struct GemvShape<2> { static constexpr int RT = 4, NCW = 8; };
-template <> struct GemvShape<3> { static constexpr int RT = 4, NCW = 4; };
-template <> struct GemvShape<4> { static constexpr int RT = 4, NCW = 4; };
 // The down projection uses sets of two row tiles: fine enough that whole sets
 // (no split-K, output written directly with the residual added) balance over
 // the SMs for the 8B-class shapes; where whole sets would leave CTAs too
@@ -106,38 +103,6 @@ __device__ __forceinline__ bool gemv_epi(const GemvParams& p, int T, int j, cons
   }
 }
 
-// Down projection, split set `set` whose last piece just finished here: the
-// block output of its rows is the pieces' slabs added in slab order, plus h1.
-// Threads take 4 consecutive rows of one token at a time.
-__device__ __forceinline__ void down_out4(const GemvParams& p, size_t at, const float4& y) {
-  if (p.out_dtype == FT_F32) {
-    *reinterpret_cast<float4*>(static_cast<float*>(p.out_final) + at) = y;
-  } else {
-    const uint32_t lo = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y.x)) |
-                        ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y.y)) << 16);
-    const uint32_t hi = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y.z)) |
-                        ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(y.w)) << 16);
-    *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.out_final) + at) = make_uint2(lo, hi);
-  }
-}
-__device__ __forceinline__ void down_finish_set(const GemvParams& p, int set, int rows, int first_row, int i0,
-                                                int stride) {
-  const GemvPlan& pl = p.plan;
-  const int np = plan_pieces(pl, set);
-  const size_t slab4 = (size_t)p.B * pl.N / 4;
-  const int r4 = rows / 4, n = r4 * p.B;
-  for (int i = i0; i < n; i += stride) {
-    const size_t at = (size_t)(i / r4) * pl.N + first_row + 4 * (i % r4);  // 4 rows of one token
-    const float4* q = reinterpret_cast<const float4*>(p.part + at);
-    float4 x[kPieceBatch];
-    pieces_load<kPieceBatch>(q, slab4, np, x);
-    const float4 h = __ldcg(reinterpret_cast<const float4*>(p.resid + at));
-    float4 y = pieces_sum<kPieceBatch>(q, slab4, np, x);
-    piece_add(y, h);
-    down_out4(p, at, y);
-  }
-}
-
 // Programmatic dependent launch.  Every kernel of the block waits for its
 // predecessor before it exits, so a kernel's completion implies that of the
 // whole chain before it.  Most kernels let their successor launch at entry, so
@@ -147,33 +112,6 @@ __device__ __forceinline__ void down_finish_set(const GemvParams& p, int set, in
 // the attention kernel's history loads issued before its own wait can never
 // overlap a previous call that wrote the same cache.
 //
-// Walks a CTA's unit range stage by stage (set, first group, group count) with
-// no divisions in the loop; every warp role runs the same walk.
-struct StageWalk {
-  int u, u1, set, kg, ng, NKG, cap;
-  __device__ __forceinline__ StageWalk(const GemvPlan& pl, int u0, int u1_) {
-    u = u0;
-    u1 = u1_;
-    NKG = pl.NKG;
-    cap = pl.ng;
-    set = u0 / NKG;
-    kg = u0 - set * NKG;
-    ng = min(min(cap, NKG - kg), u1 - u);
-  }
-  __device__ __forceinline__ bool valid() const { return u < u1; }
-  // true if the stage just finished ends this CTA's piece of its set
-  __device__ __forceinline__ bool piece_end() const { return u + ng >= u1 || kg + ng == NKG; }
-  __device__ __forceinline__ void next() {
-    u += ng;
-    kg += ng;
-    if (kg == NKG) {
-      kg = 0;
-      ++set;
-    }
-    ng = min(min(cap, NKG - kg), u1 - u);
-  }
-};
-
 // Producer warp: streams the CTA's (row-tile set, group) units stage by stage
 // into the ring, with the matching activation chunk and group offsets.  The
 // first `stages` stages of weights are issued before waiting on the previous
@@ -246,7 +184,7 @@ __global__ void __launch_bounds__((GemvShape<NT>::NCW + 2) * 32, 1) gemv_kernel(
   uint8_t* zero_row = smem + pl.zerooff;  // stands in for activation rows of absent tokens
   uint8_t* slots = smem + pl.slotoff;
 
-  if (ROLE != kRoleQKV) griddep_launch();  // QKV: every warp after its own wait (note above StageWalk)
+  if (ROLE != kRoleQKV) griddep_launch();  // QKV: every warp after its own wait (see the note on programmatic dependent launch)
   for (int i = tid; i < pl.ng * kWGroup * 2 / 16; i += blockDim.x)
     reinterpret_cast<uint4*>(zero_row)[i] = make_uint4(0u, 0u, 0u, 0u);
   if (tid == 0) {
@@ -353,13 +291,16 @@ __global__ void __launch_bounds__((GemvShape<NT>::NCW + 2) * 32, 1) gemv_kernel(
     for (int kgl = warp; kgl < st.ng; kgl += NCW) {
       // activation rows of this lane's B fragments (tokens >= B read zeros) and
       // the group offsets -S for the lane's two token columns
-      const uint8_t* xr[NT];
+      const uint8_t* xr[NT];  // row of half 0; half 1 is xh bytes further
+      int xh[NT];
       float c0[NT][2];
 #pragma unroll
       for (int j = 0; j < NT; ++j) {
         const int row = 8 * j + g, t = 8 * j + 2 * tig;
-        // row `row` of group kgl in the stage's grouped rows; absent tokens read zeros
-        xr[j] = row < p.B ? sw + pl.xoff + (kgl * p.B + row) * (kWGroup * 2) : zero_row + kgl * (kWGroup * 2);
+        // row `row` of group kgl in the stage's half-group rows; absent tokens read zeros
+        const bool on = row < p.B;
+        xr[j] = on ? sw + pl.xoff + (2 * kgl * p.B + row) * 128 : zero_row + kgl * (kWGroup * 2);
+        xh[j] = on ? p.B * 128 : 128;
         const longlong2 sv = *reinterpret_cast<const longlong2*>(ss + kgl * 32 + t);
         c0[j][0] = (t < p.B) ? -sfix_to_f32(sv.x) : 0.0f;
         c0[j][1] = (t + 1 < p.B) ? -sfix_to_f32(sv.y) : 0.0f;
@@ -387,7 +328,7 @@ __global__ void __launch_bounds__((GemvShape<NT>::NCW + 2) * 32, 1) gemv_kernel(
           uint32_t b0[NT], b1[NT];
 #pragma unroll
           for (int j = 0; j < NT; ++j) {
-            const uint2 bv = *reinterpret_cast<const uint2*>(xr[j] + op_frag_off(ks, tig, g));
+            const uint2 bv = *reinterpret_cast<const uint2*>(xr[j] + half * xh[j] + op_frag_off(kq, tig, g));
             b0[j] = bv.x;
             b1[j] = bv.y;
           }
@@ -462,227 +403,6 @@ __device__ __forceinline__ void consumer_sync(int nthreads) {
   asm volatile("bar.sync 2, %0;" ::"r"(nthreads) : "memory");
 }
 
-// Tile-split GEMV for large batches (three or four 8-token column tiles).  The
-// activation chunk of a stage (B x ng x 256 bytes) would otherwise outweigh its
-// weights several times over, re-read for every set of 4 row tiles; here a set
-// has RT = TPW * NCW row tiles and consumer warp w owns tiles w, w + NCW, ... for
-// every group of the stage, so each warp finishes its own sums and applies the
-// role epilogue itself.  Same ring, producer, partition and epilogues as
-// gemv_kernel; one MMA chain per (tile, column tile).
-template <int NT, int ROLE, int TPW, int NCW>
-__global__ void __launch_bounds__((NCW + 1) * 32, 1) gemv_ts_kernel(const GemvParams p) {
-  constexpr int RT = TPW * NCW, PRODUCER = NCW;
-  extern __shared__ __align__(128) uint8_t smem[];
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const GemvPlan& pl = p.plan;
-  const int cta = blockIdx.x;
-  const int u0 = plan_u0(pl, cta), u1 = plan_u0(pl, cta + 1);
-  const int S = pl.stages;
-  const uint32_t full0 = smem_u32(smem), empty0 = full0 + 8 * S;
-  uint32_t* tick_bcast = reinterpret_cast<uint32_t*>(smem + pl.redoff);
-  uint8_t* zero_row = smem + pl.zerooff;
-  uint8_t* slots = smem + pl.slotoff;
-
-  if (ROLE != kRoleQKV) griddep_launch();  // QKV: every warp after its own wait (note above StageWalk)
-  for (int i = tid; i < pl.ng * kWGroup * 2 / 16; i += blockDim.x)
-    reinterpret_cast<uint4*>(zero_row)[i] = make_uint4(0u, 0u, 0u, 0u);
-  if (tid == 0) {
-    for (int s = 0; s < S; ++s) {
-      mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, NCW);
-    }
-    mbar_fence_init();
-  }
-  __syncthreads();
-
-  if (warp == PRODUCER) {
-    gemv_produce<RT>(p, slots, full0, empty0, u0, u1, ROLE == kRoleQKV);
-    return;
-  }
-
-  griddep_wait();
-  if (ROLE == kRoleQKV) griddep_launch();
-  const int g = lane >> 2, tig = lane & 3;
-  float rho2_lane = 0.0f;
-  if (ROLE == kRoleGU && lane < p.B) {
-    float t = 0.0f;
-    for (int k = 0; k < p.nssq; ++k) t += __ldcg(p.ssq2 + lane * p.nssq + k);
-    rho2_lane = rsqrtf(t * p.inv_h + p.eps);
-  }
-  float tot[TPW][NT][4];
-#pragma unroll
-  for (int a = 0; a < TPW; ++a)
-#pragma unroll
-    for (int b = 0; b < NT; ++b)
-#pragma unroll
-      for (int r = 0; r < 4; ++r) tot[a][b][r] = 0.0f;
-
-  bool bad = false;
-  int slot = 0, fphase = 0, piece_kg0 = -1;
-  for (StageWalk st(pl, u0, u1); st.valid(); st.next()) {
-    if (piece_kg0 < 0) piece_kg0 = st.kg;
-    if (!mbar_wait(full0 + 8 * slot, fphase)) {
-      set_status(p.status, FT_DEV_TIMEOUT);
-      return;
-    }
-    const uint8_t* sw = slots + slot * pl.slot;
-    const sfix_t* ss = reinterpret_cast<const sfix_t*>(sw + pl.soff);
-    const int nrt = min(RT, pl.NTILE - st.set * RT);
-    for (int kgl = 0; kgl < st.ng; ++kgl) {
-      const uint8_t* xr[NT];
-      float c0[NT][2];
-#pragma unroll
-      for (int j = 0; j < NT; ++j) {
-        const int row = 8 * j + g, t = 8 * j + 2 * tig;
-        // row `row` of group kgl in the stage's grouped rows; absent tokens read zeros
-        xr[j] = row < p.B ? sw + pl.xoff + (kgl * p.B + row) * (kWGroup * 2) : zero_row + kgl * (kWGroup * 2);
-        const longlong2 sv = *reinterpret_cast<const longlong2*>(ss + kgl * 32 + t);
-        c0[j][0] = (t < p.B) ? -sfix_to_f32(sv.x) : 0.0f;
-        c0[j][1] = (t + 1 < p.B) ? -sfix_to_f32(sv.y) : 0.0f;
-      }
-      uint32_t sc[TPW];
-      float acc[TPW][NT][4];
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t wd[TPW][4];
-#pragma unroll
-        for (int t = 0; t < TPW; ++t) {
-          const int rt = warp + t * NCW;
-          if (rt < nrt) {
-            const uint8_t* slab = sw + (rt * pl.ng + kgl) * kSlabBytes;
-            const uint4 q = *reinterpret_cast<const uint4*>(slab + half * 512 + lane * 16);
-            wd[t][0] = q.x; wd[t][1] = q.y; wd[t][2] = q.z; wd[t][3] = q.w;
-            if (half == 0) sc[t] = *reinterpret_cast<const uint32_t*>(slab + kSlabCodes + 4 * g);
-          }
-        }
-#pragma unroll
-        for (int kq = 0; kq < 4; ++kq) {
-          const int ks = 4 * half + kq;
-          uint32_t b0[NT], b1[NT];
-#pragma unroll
-          for (int j = 0; j < NT; ++j) {
-            const uint2 bv = *reinterpret_cast<const uint2*>(xr[j] + op_frag_off(ks, tig, g));
-            b0[j] = bv.x;
-            b1[j] = bv.y;
-          }
-#pragma unroll
-          for (int t = 0; t < TPW; ++t) {
-            if (warp + t * NCW >= nrt) continue;  // warp-uniform: tiles past a short last set
-            uint32_t r[4];
-            magic_word(wd[t][kq], r);
-            const uint32_t a[4] = {r[0], r[2], r[1], r[3]};
-#pragma unroll
-            for (int j = 0; j < NT; ++j) {
-              if (ks == 0) {
-                float* d = acc[t][j];
-                d[0] = c0[j][0]; d[1] = c0[j][1]; d[2] = c0[j][0]; d[3] = c0[j][1];
-              }
-              mma_f16(acc[t][j], a, b0[j], b1[j]);
-            }
-          }
-        }
-      }
-#pragma unroll
-      for (int t = 0; t < TPW; ++t) {
-        if (warp + t * NCW >= nrt) continue;
-        const float slo = bf16_bits_to_f32((uint16_t)(sc[t] & 0xFFFFu));
-        const float shi = bf16_bits_to_f32((uint16_t)(sc[t] >> 16));
-#pragma unroll
-        for (int j = 0; j < NT; ++j)
-#pragma unroll
-          for (int r = 0; r < 4; ++r) tot[t][j][r] = fmaf((r & 2) ? shi : slo, acc[t][j][r], tot[t][j][r]);
-      }
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(empty0 + 8 * slot);
-    if (++slot == S) {
-      slot = 0;
-      fphase ^= 1;
-    }
-
-    if (st.piece_end()) {
-      const bool whole = (piece_kg0 == 0) && (st.kg + st.ng == pl.NKG);
-      piece_kg0 = -1;
-      const int piece = cta - plan_first(pl, st.set);  // split sets: this piece's slab
-#pragma unroll
-      for (int t = 0; t < TPW; ++t) {
-        const int rt = warp + t * NCW;
-        if (rt < nrt) {
-#pragma unroll
-          for (int j = 0; j < NT; ++j)
-            bad |= gemv_epi<ROLE>(p, st.set * RT + rt, j, tot[t][j], whole, rho2_lane, piece);
-        }
-#pragma unroll
-        for (int j = 0; j < NT; ++j)
-#pragma unroll
-          for (int r = 0; r < 4; ++r) tot[t][j][r] = 0.0f;
-      }
-      if (ROLE == kRoleDown && !whole) {
-        // split set: every warp's slab stores of this piece are done before the
-        // ticket; the last piece writes the block output from h1 and the slabs
-        __threadfence();
-        consumer_sync(NCW * 32);
-        if (tid == 0)
-          *tick_bcast = (atomicAdd(p.tick + st.set, 1u) == (uint32_t)(plan_pieces(pl, st.set) - 1)) ? 1u : 0u;
-        consumer_sync(NCW * 32);
-        if (*tick_bcast) {
-          __threadfence();
-          down_finish_set(p, st.set, nrt * kRowTile, st.set * RT * kRowTile, tid, NCW * 32);
-          if (tid == 0) p.tick[st.set] = 0u;
-        }
-        consumer_sync(NCW * 32);  // the broadcast word is reused by the next piece
-      }
-    }
-  }
-  if (bad) set_status(p.status, FT_DEV_RANGE);
-}
-
-template <int NT, int ROLE, int TPW, int NCW>
-static cudaError_t launch_ts_one(const GemvParams& p, cudaStream_t st, bool pdl) {
-  static int attr_smem[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (attr_smem[dev] < p.plan.smem) {
-    cudaError_t e = cudaFuncSetAttribute(gemv_ts_kernel<NT, ROLE, TPW, NCW>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, p.plan.smem);
-    if (e != cudaSuccess) return e;
-    attr_smem[dev] = p.plan.smem;
-  }
-  return launch_ex(gemv_ts_kernel<NT, ROLE, TPW, NCW>, dim3(p.plan.C), dim3((NCW + 1) * 32), (size_t)p.plan.smem,
-                   st, pdl, p);
-}
-
-// Tile-split shapes.  Split-K roles: 12 warps x 1 tile (192-row sets).  Gate/up
-// (whole sets, SwiGLU in the epilogue): 12 warps x 1 tile where that makes about
-// one set per SM, else 6 warps x 1-4 tiles (registers bound warps x tiles).
-constexpr int kTsNcw = 12, kTsTpw = 1, kTsNcwGUWide = 6;
-
-template <int NT, int ROLE>
-static cudaError_t launch_ts_nt(const GemvParams& p, cudaStream_t st, bool pdl) {
-  if constexpr (ROLE == kRoleGU) {
-    if (p.plan.NCW == kTsNcw) return launch_ts_one<NT, ROLE, 1, kTsNcw>(p, st, pdl);
-    switch (p.plan.tpw) {
-      case 1: return launch_ts_one<NT, ROLE, 1, kTsNcwGUWide>(p, st, pdl);
-      case 2: return launch_ts_one<NT, ROLE, 2, kTsNcwGUWide>(p, st, pdl);
-      case 3: return launch_ts_one<NT, ROLE, 3, kTsNcwGUWide>(p, st, pdl);
-      case 4: return launch_ts_one<NT, ROLE, 4, kTsNcwGUWide>(p, st, pdl);
-      default: return cudaErrorInvalidValue;
-    }
-  } else {
-    return launch_ts_one<NT, ROLE, kTsTpw, kTsNcw>(p, st, pdl);
-  }
-}
-
-template <int ROLE>
-static cudaError_t launch_ts(const GemvParams& p, cudaStream_t st, bool pdl) {
-  switch (p.plan.NT) {
-    case 3: return launch_ts_nt<3, ROLE>(p, st, pdl);
-    case 4: return launch_ts_nt<4, ROLE>(p, st, pdl);
-    default: return cudaErrorInvalidValue;
-  }
-}
-
 template <int NT, int ROLE>
 static cudaError_t launch_one(const GemvParams& p, cudaStream_t st, bool pdl) {
   constexpr int THREADS = (GemvShape<NT>::NCW + 2) * 32;
@@ -704,22 +424,12 @@ static cudaError_t launch_role(const GemvParams& p, cudaStream_t st, bool pdl) {
   switch (p.plan.NT) {
     case 1: return launch_one<1, ROLE>(p, st, pdl);
     case 2: return launch_one<2, ROLE>(p, st, pdl);
-    case 3: return launch_one<3, ROLE>(p, st, pdl);
-    case 4: return launch_one<4, ROLE>(p, st, pdl);
     default: return cudaErrorInvalidValue;
   }
 }
 
 cudaError_t launch_gemv(int role, const GemvParams& p, cudaStream_t st, bool pdl) {
-  if (p.plan.ts) {
-    switch (role) {
-      case kRoleQKV: return launch_ts<kRoleQKV>(p, st, pdl);
-      case kRoleO: return launch_ts<kRoleO>(p, st, pdl);
-      case kRoleGU: return launch_ts<kRoleGU>(p, st, pdl);
-      case kRoleDown: return launch_ts<kRoleDown>(p, st, pdl);
-      default: return cudaErrorInvalidValue;
-    }
-  }
+  if (p.plan.umma) return launch_umma(role, p, st, pdl);
   switch (role) {
     case kRoleQKV: return launch_role<kRoleQKV>(p, st, pdl);
     case kRoleO: return launch_role<kRoleO>(p, st, pdl);
@@ -733,8 +443,7 @@ static void shape_of(int NT, int& RT, int& NCW) {
   switch (NT) {
     case 1: RT = GemvShape<1>::RT; NCW = GemvShape<1>::NCW; break;
     case 2: RT = GemvShape<2>::RT; NCW = GemvShape<2>::NCW; break;
-    case 3: RT = GemvShape<3>::RT; NCW = GemvShape<3>::NCW; break;
-    default: RT = GemvShape<4>::RT; NCW = GemvShape<4>::NCW; break;
+    default: RT = GemvShape<2>::RT; NCW = GemvShape<2>::NCW; break;
   }
 }
 
@@ -745,19 +454,6 @@ GemvPlan make_gemv_plan(int role, int N, int K, int B, int sms, int smem_budget)
   p.NT = (B + 7) / 8;
   shape_of(p.NT, p.RT, p.NCW);
   if (role == kRoleDown) p.RT = kDownRT;
-  p.ts = p.NT >= 3 ? 1 : 0;
-  if (p.ts) {
-    p.NCW = kTsNcw;
-    p.tpw = kTsTpw;
-    if (role == kRoleGU) {  // about one whole set per SM
-      const int ntile = N / kRowTile;
-      if ((ntile + sms * kTsNcw - 1) / (sms * kTsNcw) > 1) {
-        p.NCW = kTsNcwGUWide;
-        p.tpw = std::max(1, std::min(4, (ntile + sms * p.NCW - 1) / (sms * p.NCW)));
-      }
-    }
-    p.RT = p.tpw * p.NCW;
-  }
   p.NTILE = N / kRowTile;
   p.NKG = K / kWGroup;
   p.NSET = (p.NTILE + p.RT - 1) / p.RT;
@@ -785,10 +481,6 @@ GemvPlan make_gemv_plan(int role, int N, int K, int B, int sms, int smem_budget)
   if (!whole_sets)
     for (int set = 0; set < p.NSET; ++set) p.npmax = std::max(p.npmax, plan_pieces(p, set));
   p.ng = p.NCW * 4 / p.RT;  // stages of 4 row tiles x NCW groups (a group per warp for RT = 4)
-  if (p.ts) {  // stages of about 48 KB (weights of RT tiles + B activation rows per group)
-    const int per_group = p.RT * kSlabBytes + B * kWGroup * 2 + 256;
-    p.ng = std::max(1, 48 * 1024 / per_group);
-  }
   if (p.ng > p.NKG) p.ng = p.NKG;
   p.xstride = p.ng * kWGroup * 2;  // bytes of one token row of a stage (grouped rows, no padding)
   const int wbytes = p.RT * p.ng * kSlabBytes;
@@ -796,7 +488,7 @@ GemvPlan make_gemv_plan(int role, int N, int K, int B, int sms, int smem_budget)
   p.soff = (int)align_up((size_t)p.xoff + (size_t)B * p.xstride, 16);
   p.slot = (int)align_up((size_t)p.soff + (size_t)p.ng * 256, 128);
   p.redoff = 256;
-  const int redbytes = p.ts ? 128 : p.NCW * p.RT * p.NT * 128 * 4;  // tile-split: the ticket word
+  const int redbytes = p.NCW * p.RT * p.NT * 128 * 4;
   p.zerooff = (int)align_up((size_t)p.redoff + (size_t)redbytes, 128);
   p.slotoff = (int)align_up((size_t)p.zerooff + (size_t)p.ng * kWGroup * 2, 128);
   int stages = (smem_budget - p.slotoff) / p.slot;

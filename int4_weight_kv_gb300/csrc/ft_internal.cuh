@@ -234,18 +234,20 @@ __host__ __device__ __forceinline__ int op_slot(int k) {
   return base + ((c < 8) ? (4 * (c >> 1) + (c & 1)) : (4 * ((c - 8) >> 1) + 2 + (c & 1)));
 }
 __host__ __device__ __forceinline__ bool op_high(int k) { return (k & 15) >= 8; }
-// Grouped operand buffer of B rows: the B rows' values of each 128-input group
-// are stored together ([K/128][B][128] FP16), so a stage of consecutive groups is
-// one contiguous copy; within a row the 16 chunks of 8 values (op_slot order)
-// are XOR-permuted by (row & 7), so the B-fragment loads of 8 rows hit
-// different shared-memory banks.  op_index(t, k, B) is the element index of
-// input k of row t.
+// Grouped operand buffer of B rows: the B rows' values of each 64-input half
+// group are stored together ([K/64][B][64] FP16, one 128-byte row per token), so
+// a stage of consecutive groups is one contiguous copy; within a 128-byte row
+// the 8 chunks of 8 values (op_slot order) are XOR-permuted by (row & 7).  That
+// is the 128-byte-swizzled K-major layout the tensor cores read through a
+// shared-memory descriptor (8-row, 1024-byte atoms), and it keeps the
+// B-fragment loads of 8 rows on different shared-memory banks.  op_index(t, k,
+// B) is the element index of input k of row t.
 __host__ __device__ __forceinline__ int op_index(int t, int k, int B) {
-  const int p = op_slot(k & 127);
-  return ((k >> 7) * B + t) * 128 + (((p >> 3) ^ (t & 7)) << 3) + (p & 7);
+  const int p = op_slot(k & 63);
+  return ((k >> 6) * B + t) * 64 + (((p >> 3) ^ (t & 7)) << 3) + (p & 7);
 }
-// Byte offset, within a group row of the grouped layout, of lane tig's 8-byte
-// B fragment of k-step ks for a row whose (row & 7) is `key`.
+// Byte offset, within a 128-byte half-group row, of lane tig's 8-byte B fragment
+// of k-step ks (0..3 within the half) for a row whose (row & 7) is `key`.
 __device__ __forceinline__ int op_frag_off(int ks, int tig, int key) {
   return ((((2 * ks) + (tig >> 1)) ^ key) << 4) + ((tig & 1) << 3);
 }

@@ -11,9 +11,9 @@
 // the scratch space comes from here.
 //
 // Properties a caller must know:
-//  * the array is kStaticWorkspaceBytes (32 MiB) of device memory that every GPU
+//  * the array is kStaticWorkspaceBytes (48 MiB) of device memory that every GPU
 //    loading this library keeps until the process exits (the largest layer
-//    shape here, 70B at batch 32, needs about 22 MiB);
+//    shape here, 70B at batch 32, needs about 33 MiB);
 //  * problems whose workspace would exceed it are rejected with
 //    FT_ERR_WORKSPACE before anything is enqueued;
 //  * the array is shared by every call on a device and keeps the previous
@@ -33,7 +33,7 @@
 
 namespace {
 
-constexpr size_t kStaticWorkspaceBytes = 32u << 20;
+constexpr size_t kStaticWorkspaceBytes = 48u << 20;
 
 // Device-side scratch.  In host code this name is only a handle for
 // cudaGetSymbolAddress, never a device address.

@@ -118,14 +118,14 @@ def run_gpu(pb: Problem, act_dtype=ft.FT_F32, cache: Optional[torch.Tensor] = No
 
 def operand_decode(x16: np.ndarray, B: int) -> np.ndarray:
     """Logical FP32 values [B, K] of B rows stored in the projections' grouped
-    operand layout (include/ft.h: [K/128][B][128]; runs of 8 stored values
+    operand layout (include/ft.h: [K/64][B][64]; runs of 8 stored values
     permuted by XOR with row mod 8; within each 16 inputs the storage order is
     0,1,8,9,2,3,10,11,4,5,12,13,6,7,14,15 and inputs 8..15 hold value / 16)."""
-    x = np.asarray(x16, np.float32).reshape(-1, B, 16, 8)          # [group][row][stored run][8]
+    x = np.asarray(x16, np.float32).reshape(-1, B, 8, 8)           # [half group][row][stored run][8]
     runs = np.empty_like(x)
     for t in range(B):
-        runs[:, t] = x[:, t, np.arange(16) ^ (t & 7)]               # logical run r sits at r ^ (t & 7)
-    slots = runs.reshape(-1, B, 128).transpose(1, 0, 2).reshape(B, -1, 16)
+        runs[:, t] = x[:, t, np.arange(8) ^ (t & 7)]                # logical run r sits at r ^ (t & 7)
+    slots = runs.reshape(-1, B, 64).transpose(1, 0, 2).reshape(B, -1, 16)
     order = np.array([0, 1, 8, 9, 2, 3, 10, 11, 4, 5, 12, 13, 6, 7, 14, 15])
     out = np.empty_like(slots)
     out[..., order] = slots

@@ -113,7 +113,8 @@ def test_argument_errors_return_before_launch(ft):
     assert lib.ft_kv_append_int4(ctypes.byref(c), 4096, 2, 64, 16, 16, 16, 1, 65, None, None) == ft.FT_ERR_CAPACITY
     assert lib.ft_kv_append_int4(ctypes.byref(c), 4097, 2, 64, 16, 16, 16, 1, 1, None, None) == ft.FT_ERR_INVALID_ARG
     assert lib.ft_kv_unpack_int4(ctypes.byref(c), 4096, 2, 64, 3, 8, 16, 16, 16, 16, None) == ft.FT_ERR_INVALID_ARG
-    assert ft.ft_decode_block_launches() == 7
+    assert ft.ft_decode_block_launches(1) == 7 and ft.ft_decode_block_launches(16) == 7
+    assert ft.ft_decode_block_launches(17) == 9 and ft.ft_decode_block_launches(32) == 9
     # model-step helpers
     assert lib.ft_rmsnorm_bf16(None, 4096, 8192, 1, 64, ctypes.c_float(1e-5), None) == ft.FT_ERR_INVALID_ARG
     assert lib.ft_rmsnorm_bf16(4096, 4096, 8192, 0, 64, ctypes.c_float(1e-5), None) == ft.FT_ERR_INVALID_ARG
@@ -125,7 +126,7 @@ def test_argument_errors_return_before_launch(ft):
 
 def test_plan_partitions(ft):
     """Host-side partition choices (no GPU needed): whole vs split sets, the
-    tile-split kernel for three or four token tiles, shared memory within one SM."""
+    tensor-core kernel for batches of 17-32, shared memory within one SM."""
     c8 = ft.cfg_from_shape(synth.workload("8b_b1_ctx1024").shape)
     c70 = ft.cfg_from_shape(synth.workload("70b_b1_ctx2048").shape)
     info = lambda c, B, role: ft.ft_decode_plan_info(c, B, 4097, role)
@@ -133,20 +134,21 @@ def test_plan_partitions(ft):
         for B in (1, 2, 8, 9, 16, 17, 32):
             for role in ft.ROLES:
                 g = info(c, B, role)
-                assert g.col_tiles == (B + 7) // 8
-                assert g.tile_split == (1 if B > 16 else 0)
+                tc = B > 16
+                assert g.tensor_core == (1 if tc else 0)
+                assert g.col_tiles == (4 if tc else (B + 7) // 8)   # the tensor-core kernel always takes N = 32
                 assert 2 <= g.stages <= 8 and 1 <= g.groups_per_stage
                 assert 0 < g.smem_bytes <= 227 * 1024
                 assert 1 <= g.ctas <= 148
-                if role == ft.FT_W_GATEUP:
-                    assert g.whole == 1            # SwiGLU needs whole rows
+                if tc:
+                    assert g.row_tiles == 8                # one M = 128 tensor-core tile per set
+                    assert g.whole == 0                    # units spread evenly, every piece to a slab
+                elif role == ft.FT_W_GATEUP:
+                    assert g.whole == 1                    # SwiGLU in the epilogue needs whole rows
                 if role in (ft.FT_W_QKV, ft.FT_W_O):
-                    assert g.whole == 0            # split along K, red.add into the accumulator
+                    assert g.whole == 0                    # split along K, one slab per piece
     # down: whole two-tile sets balance for the 8B shape, not for 70B (long K)
     assert info(c8, 1, ft.FT_W_DOWN).whole == 1 and info(c8, 1, ft.FT_W_DOWN).row_tiles == 2
     assert info(c70, 1, ft.FT_W_DOWN).whole == 0
-    # tile-split sets: every consumer warp owns whole row tiles
-    g = info(c8, 32, ft.FT_W_QKV)
-    assert g.row_tiles % g.warps == 0 and g.row_tiles >= 12
     with pytest.raises(RuntimeError):
         info(c8, 33, ft.FT_W_QKV)

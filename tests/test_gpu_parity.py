@@ -134,6 +134,21 @@ def test_block_tiny_ragged_batch(tiny):
     H.assert_block_close(g, o, range(8))
 
 
+@pytest.mark.parametrize("B", [17, 20, 32])
+def test_block_tiny_tensor_core(tiny, B):
+    """Batches of 17-32 run the projections on the tcgen05 kernel (128-row
+    sets split evenly over the CTAs into per-piece slabs, finished by the
+    SwiGLU and output kernels); ragged positions."""
+    assert ft.ft_decode_plan_info(tiny.cfg, B, 140, ft.FT_W_GATEUP).tensor_core == 1
+    pos = synth.positions(B, 129, ragged=True, seed=B)
+    pb = H.make_problem(tiny, 1, B=B, ctx=129, pos=pos, max_ctx=140)
+    g = H.run_gpu(pb)
+    rows = sorted({0, 5, B // 2, B - 1})
+    o = H.run_oracle(pb, rows=rows)
+    rep = H.assert_block_close(g, o, rows)
+    assert rep["qkv_rel_rms"] < 1e-3
+
+
 def test_block_tiny_bf16_io_is_rounding_of_f32(tiny):
     pb = H.make_problem(tiny, 1, B=3, ctx=40)
     g32 = H.run_gpu(pb, ft.FT_F32)

@@ -30,7 +30,7 @@ def _gpu():
     build.build()
 
 
-STATIC_BYTES = 32 << 20  # the library's fixed scratch array
+STATIC_BYTES = 48 << 20  # the library's fixed scratch array
 
 
 def _run_static(pb, cache):
