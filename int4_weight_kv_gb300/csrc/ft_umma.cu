@@ -15,10 +15,11 @@
 //    x / 16 there) and store them straight into tensor memory as the A operand:
 //    the packed fragment order is the 16x256b tensor-memory layout, with K
 //    permuted exactly as the activation operand's storage order;
-//  * one thread issues tcgen05.mma kind::f16 (M = 128 rows, N = 32 tokens,
-//    K = 16), A from tensor memory, B from shared memory through a
-//    128-byte-swizzle descriptor, FP32 accumulation in tensor memory, one
-//    accumulator per group (four groups' A tiles and accumulators in flight);
+//  * two threads (groups taken in turn) issue tcgen05.mma kind::f16 (M = 128
+//    rows, N = 32 tokens, K = 16), A from tensor memory, B from shared memory
+//    through a 128-byte-swizzle descriptor, FP32 accumulation in tensor
+//    memory, one accumulator per group (four groups' A tiles and eight
+//    accumulators in flight);
 //  * four epilogue warps read each group's accumulator (one row per thread),
 //    remove the decode offset S of each token and apply the row's group scale
 //    in FP32 (scales and offsets stashed by the decoders), and at the end of
@@ -38,10 +39,16 @@ namespace ft {
 namespace umma {
 
 constexpr int kDecWarps = 8, kEpiWarps = 4;
-constexpr int kProducer = 0, kMma = 1, kDec0 = 2, kEpi0 = kDec0 + kDecWarps;
-constexpr int kWarps = kEpi0 + kEpiWarps, kThreads = kWarps * 32;
+// Two issuing warps, group gi issued by issuer gi % 2: a thread stalls while its MMAs run, so
+// the other's bookkeeping and waits overlap them and the tensor core stays fed.  Warp w runs on
+// scheduler w % 4; the roles are placed so that each scheduler carries two decoder warps and
+// at most two others (the decoders' pace sets the tensor core's).
+constexpr int kIssuers = 2;
+constexpr int kMma2 = 0, kMma = 1, kDec0 = 2, kEpi0 = kDec0 + kDecWarps, kProducer = kEpi0 + kEpiWarps;
+constexpr int kWarps = kProducer + 1, kThreads = kWarps * 32;
 constexpr int kNBuf = 4;         // A tiles in flight (groups)
 constexpr int kNAcc = 8;         // accumulators (and stashed scales / offsets) in flight (groups)
+static_assert(kNAcc % kIssuers == 0, "each issuer owns the accumulators of its own groups");
 constexpr int kTmemCols = 512;  // D: kNAcc x 32 columns, A: kNBuf x 64 columns
 constexpr int kAccCol = 0, kACol = 32 * kNAcc;
 constexpr int kXTile = 32 * 128;  // one 64-input half group of 32 token rows
@@ -151,7 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const GemvParams p) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full(s), 1);
       // decoders (weights, scales and offsets read) and the tensor core (activations read)
-      mbar_init(empty(s), kDecWarps + 1);
+      mbar_init(empty(s), kDecWarps + kIssuers);
     }
     for (int b = 0; b < kNAcc; ++b) {
       mbar_init(a_full + 8 * b, kDecWarps);
@@ -213,42 +220,46 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const GemvParams p) {
       const int sj = si - 1 - k;
       if (!mbar_wait(full(sj % S), (sj / S) & 1)) ok = false;
     }
-  } else if (warp == kMma) {
-    // ------------------------------------------------------------ tensor-core issue
+  } else if (warp == kMma || warp == kMma2) {
+    // ------------------------------------------------------------ tensor-core issue (one thread per
+    // issuing warp; issuer i takes the groups gi with gi % kIssuers == i)
     griddep_wait();
     if (ROLE == kRoleQKV) griddep_launch();
-    constexpr uint32_t idesc = idesc_f16(128, 32);
-    int si = 0, gi = 0;
-    for (StageWalk st(pl, u0, u1); ok && st.valid(); st.next(), ++si) {
-      const int slot = si % S;
-      if (!mbar_wait(full(slot), (si / S) & 1)) {
-        ok = false;
-        break;
-      }
-      const uint32_t xs = smem_u32(slots + slot * pl.slot + pl.xoff);
-      for (int kgl = 0; kgl < st.ng; ++kgl, ++gi) {
-        const int a = gi % kNAcc, ua = gi / kNAcc, ab = gi % kNBuf;
-        // A tile filled (decoders); accumulator a drained (epilogue, group gi - kNAcc)
-        if (!mbar_wait(a_full + 8 * a, ua & 1) || (ua > 0 && !mbar_wait(acc_empty + 8 * a, (ua - 1) & 1))) {
+    const int issuer = warp == kMma ? 0 : 1;
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_f16(128, 32);
+      int si = 0, gi = 0, last = -1;
+      for (StageWalk st(pl, u0, u1); ok && st.valid(); st.next(), ++si) {
+        const int slot = si % S;
+        if (!mbar_wait(full(slot), (si / S) & 1)) {
           ok = false;
           break;
         }
-        fence_after();
-        if (lane == 0) {
+        const uint32_t xs = smem_u32(slots + slot * pl.slot + pl.xoff);
+        for (int kgl = 0; kgl < st.ng; ++kgl, ++gi) {
+          if (gi % kIssuers != issuer) continue;
+          const int a = gi % kNAcc, ua = gi / kNAcc, ab = gi % kNBuf;
+          // A tile filled (decoders); accumulator a drained (epilogue, group gi - kNAcc)
+          if (!mbar_wait(a_full + 8 * a, ua & 1) || (ua > 0 && !mbar_wait(acc_empty + 8 * a, (ua - 1) & 1))) {
+            ok = false;
+            break;
+          }
+          fence_after();
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks)
             mma_f16_ts(tmem + kAccCol + 32 * a, tmem + kACol + 64 * ab + 8 * ks,
                        desc_sw128(xs + (2 * kgl + (ks >> 2)) * kXTile + 32 * (ks & 3)), idesc, ks > 0 ? 1u : 0u);
           mma_commit(mma_done + 8 * a);
+          last = gi;
         }
-        __syncwarp();
+        if (!ok) break;
+        mma_commit(empty(slot));  // this thread's reads of the stage's activation tiles are done
       }
-      if (!ok) break;
-      if (lane == 0) mma_commit(empty(slot));  // the stage's activation tiles are no longer read
-      __syncwarp();
+      // the tensor core has finished everything issued here before tensor memory is freed (the
+      // issuers use disjoint accumulators and barriers)
+      if (last >= 0 && !mbar_wait(mma_done + 8 * (last % kNAcc), (last / kNAcc) & 1)) ok = false;
     }
-    // the tensor core has finished everything issued here before tensor memory is freed
-    if (gi > 0 && !mbar_wait(mma_done + 8 * ((gi - 1) % kNAcc), ((gi - 1) / kNAcc) & 1)) ok = false;
+    __syncwarp();
   } else if (warp < kEpi0) {
     // ------------------------------------------------------------ decoders
     griddep_wait();
@@ -262,11 +273,13 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const GemvParams p) {
         break;
       }
       const uint8_t* ws = slots + slot * pl.slot;
-      for (int kgl = 0; kgl < st.ng; ++kgl, ++gi) {
-        const int a = gi % kNAcc, ua = gi / kNAcc, ab = gi % kNBuf;
-        // A tile ab: the tensor core finished group gi - kNBuf; stash a: the epilogue drained
-        // group gi - kNAcc
-        if ((gi >= kNBuf && !mbar_wait(mma_done + 8 * ((gi - kNBuf) % kNAcc), ((gi - kNBuf) / kNAcc) & 1)) ||
+      // all of the stage's groups are decoded before one wait for the tensor-memory stores (the
+      // wait's latency, not the decoding, would otherwise set the pace)
+      for (int kgl = 0; kgl < st.ng; ++kgl) {
+        const int g = gi + kgl, a = g % kNAcc, ua = g / kNAcc, ab = g % kNBuf;
+        // A tile ab: the tensor core finished group g - kNBuf; stash a: the epilogue drained
+        // group g - kNAcc
+        if ((g >= kNBuf && !mbar_wait(mma_done + 8 * ((g - kNBuf) % kNAcc), ((g - kNBuf) / kNAcc) & 1)) ||
             (ua > 0 && !mbar_wait(acc_empty + 8 * a, (ua - 1) & 1))) {
           ok = false;
           break;
@@ -276,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const GemvParams p) {
           const uint16_t sb = *reinterpret_cast<const uint16_t*>(
               ws + ((2 * q + (lane >> 4)) * pl.ng + kgl) * kSlabBytes + kSlabCodes + 4 * (rr & 7) + 2 * (rr >> 3));
           scl[a * 128 + 32 * q + lane] = bf16_bits_to_f32(sb);
-        } else if (q == 0) {  // the group's token offsets S (one per token; absent tokens 0)
+        } else if (q == 3) {  // the group's token offsets S (one per token; absent tokens 0)
           const sfix_t* ss = reinterpret_cast<const sfix_t*>(ws + pl.soff);
           sof[a * 32 + lane] = lane < p.B ? sfix_to_f32(ss[kgl * 32 + lane]) : 0.0f;
         }
@@ -297,14 +310,16 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const GemvParams p) {
           }
           tmem_st16x256b_x4(tmem + kACol + 64 * ab + 32 * half + ((uint32_t)(16 * T) << 16), r);
         }
-        tmem_wait_st();
-        fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(a_full + 8 * a);
       }
       if (!ok) break;
+      tmem_wait_st();
+      fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(empty(slot));
+      if (lane == 0) {
+        for (int kgl = 0; kgl < st.ng; ++kgl) mbar_arrive(a_full + 8 * ((gi + kgl) % kNAcc));
+        mbar_arrive(empty(slot));
+      }
+      gi += st.ng;
     }
   } else {
     // ------------------------------------------------------------ epilogue
@@ -393,7 +408,7 @@ cudaError_t launch_umma(int role, const GemvParams& p, cudaStream_t st, bool pdl
 int ft_umma_warps() { return kWarps; }
 
 // Partition of a projection for the tensor-core kernel: 128-row blocks as
-// sets, 2 groups per stage, units (set, group) spread evenly over the CTAs
+// sets, 3 groups per stage, units (set, group) spread evenly over the CTAs
 // (sets split along K); every piece writes its partial sums to its own slab.
 GemvPlan make_umma_plan(int role, int N, int K, int B, int sms, int smem_budget) {
   GemvPlan p = {};
@@ -420,7 +435,7 @@ GemvPlan make_umma_plan(int role, int N, int K, int B, int sms, int smem_budget)
   p.npmax = 1;
   if (!whole_sets)
     for (int set = 0; set < p.NSET; ++set) p.npmax = std::max(p.npmax, plan_pieces(p, set));
-  p.ng = std::min(2, p.NKG);
+  p.ng = std::min(3, p.NKG);  // 3 groups per stage: fewer ring hand-offs than 1 or 2 at the same depth; 4 leaves 3 coarse stages
   // slot: weight slabs of 8 tiles, activation half-group tiles (1024-aligned), offsets
   p.xoff = (int)align_up((size_t)8 * p.ng * kSlabBytes, 1024);
   p.soff = p.xoff + 2 * p.ng * kXTile;
