@@ -237,9 +237,11 @@ int ft_read_device_status(const int32_t *dev_status, int32_t *host_out, ft_strea
 
 /* logits[b, v] = sum_k W[v, k] * z[b, k] with z = gamma * rho(x_b) * x_b,
  * rho = (mean x^2 + eps)^-1/2.  x: FP32 [B, H]; gamma: FP32 [H]; W: BF16 bits
- * [V, H] (16-byte aligned); logits: FP32 [B, V] (overwritten).  B <= 8,
- * H a multiple of 128, B * H * 4 <= 160 KiB, else FT_ERR_UNSUPPORTED.
- * z enters the tensor cores as a BF16 (hi, lo) pair. */
+ * [V, H] (16-byte aligned); logits: FP32 [B, V] (overwritten; every element
+ * is written once, no accumulation, so repeated calls give the same bits).
+ * B <= 32 and H a multiple of 128, else FT_ERR_UNSUPPORTED.  Tokens run in
+ * chunks of min(8, 160 KiB / (4 H)) (one launch each, W streamed once per
+ * chunk).  z enters the tensor cores as a BF16 (hi, lo) pair. */
 int ft_lm_head_bf16(const float *x, const float *gamma, const uint16_t *W, float *logits, int B, int V, int H,
                     float eps, ft_stream stream);
 

@@ -8,9 +8,14 @@
 // inputs the MMA's k order is permuted so that one 16-byte load of a row feeds
 // the A fragments of two MMAs; the normalised activation z = gamma * rho(x) * x
 // sits in shared memory as a BF16 (hi, lo) pair with the same permutation, so
-// the product is accurate to ~2^-16 relative while W is read once.  Work units
-// are (row tile, quarter of H), strided over all warps for balance; partial
-// sums are added into the (zeroed) FP32 logits.
+// the product is accurate to ~2^-16 relative while W is read once per chunk of
+// up to 8 tokens.  Work units are (row tile, quarter of H), strided over all
+// warps for balance; the four quarters of a row tile always fall to four
+// consecutive warps of one CTA, which add their partial sums through shared
+// memory in quarter order and store the logits (no atomics: the result does
+// not depend on timing).
+#include <algorithm>
+
 #include "ft_internal.cuh"
 
 namespace ft {
@@ -59,7 +64,8 @@ __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a1
 }
 
 constexpr int kHeadWarps = 16;
-constexpr int kHeadKSplit = 4;
+constexpr int kHeadKSplit = 4;  // quarters of H: warps 4j .. 4j + 3 of a CTA share a row tile
+static_assert(kHeadWarps % kHeadKSplit == 0, "row tiles are split within groups of warps");
 constexpr int kHeadLook = 4;  // 32-input chunks in flight per warp
 
 // z rows in shared memory: [B][H] hi then [B][H] lo (BF16 bits), natural order.
@@ -70,6 +76,7 @@ __global__ void __launch_bounds__(kHeadWarps * 32, 1) lm_head_kernel(const float
                                                                      float eps) {
   extern __shared__ __align__(16) uint16_t zs[];
   __shared__ float red[kHeadWarps];
+  __shared__ float part[kHeadWarps][4][32];  // [warp][output register][lane]
   __shared__ float rho[8];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, tig = lane & 3;
   // final RMSNorm of every token row, then z = gamma * rho * x as BF16 hi + lo
@@ -102,7 +109,10 @@ __global__ void __launch_bounds__(kHeadWarps * 32, 1) lm_head_kernel(const float
   const int ntile = (V + 15) / 16;
   const int kq = H / kHeadKSplit;  // inputs per unit (a multiple of 32)
   const int nunit = ntile * kHeadKSplit;
+  // unit % kHeadKSplit == warp % kHeadKSplit (nw is a multiple of it): quarter q of row tile T
+  // runs on warp kHeadKSplit * j + q of the CTA that holds the tile, in the same iteration
   const int gw = blockIdx.x * kHeadWarps + warp, nw = gridDim.x * kHeadWarps;
+  const int grp = warp / kHeadKSplit;
   const int zrow = min(g, B - 1);
   const bool zvalid = g < B;
   for (int unit = gw; unit < nunit; unit += nw) {
@@ -142,13 +152,21 @@ __global__ void __launch_bounds__(kHeadWarps * 32, 1) lm_head_kernel(const float
         mma_bf16(acc, p0.z, p1.z, p0.w, p1.w, bl.z, bl.w);
       }
     }
-    // c0 = (row g, token 2tig), c1 = (row g, token 2tig+1), c2, c3: row g + 8
+    // the quarters' partial sums, added in quarter order: warp q of the group finishes output
+    // register q (c0 = (row g, token 2tig), c1 = (row g, token 2tig+1), c2, c3: row g + 8)
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
+    for (int r = 0; r < 4; ++r) part[warp][r][lane] = acc[r];
+    asm volatile("bar.sync %0, %1;" ::"r"(1 + grp), "n"(kHeadKSplit * 32) : "memory");
+    {
+      const int r = q;
+      float v = part[grp * kHeadKSplit][r][lane];
+#pragma unroll
+      for (int j = 1; j < kHeadKSplit; ++j) v += part[grp * kHeadKSplit + j][r][lane];
       const int t = 2 * tig + (r & 1);
       const int row = T * 16 + g + ((r & 2) ? 8 : 0);
-      if (t < B && row < V) atomicAdd(logits + (size_t)t * V + row, acc[r]);
+      if (t < B && row < V) logits[(size_t)t * V + row] = v;
     }
+    asm volatile("bar.sync %0, %1;" ::"r"(1 + grp), "n"(kHeadKSplit * 32) : "memory");  // part is reused
   }
 }
 
@@ -181,9 +199,11 @@ int ft_lm_head_bf16(const float* x, const float* gamma, const uint16_t* W, float
                     float eps, ft_stream stream) {
   if (!x || !gamma || !W || !logits || B < 1 || V < 1 || H < 1) return FT_ERR_INVALID_ARG;
   if (!ft_host::aligned16(W) || !ft_host::aligned16(x)) return FT_ERR_INVALID_ARG;
-  if (B > 8 || H % (32 * ft::kHeadKSplit)) return FT_ERR_UNSUPPORTED;
-  const size_t smem = (size_t)B * H * 4;
-  if (smem > 160 * 1024) return FT_ERR_UNSUPPORTED;
+  if (B > 32 || H % (32 * ft::kHeadKSplit)) return FT_ERR_UNSUPPORTED;
+  // tokens in chunks of up to 8 (one MMA column tile) whose z rows fit in shared memory
+  const int bc = std::min(8, (int)((160 * 1024) / ((size_t)H * 4)));
+  if (bc < 1) return FT_ERR_UNSUPPORTED;
+  const size_t smem = (size_t)std::min(B, bc) * H * 4;
   static int attr_smem[64] = {0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return FT_ERR_CUDA;
@@ -193,12 +213,14 @@ int ft_lm_head_bf16(const float* x, const float* gamma, const uint16_t* W, float
       return FT_ERR_CUDA;
     attr_smem[dev] = (int)smem;
   }
-  if (cudaMemsetAsync(logits, 0, (size_t)B * V * sizeof(float), (cudaStream_t)stream) != cudaSuccess)
-    return FT_ERR_CUDA;
   const int sms = ft_host::num_sms();
-  ft::lm_head_kernel<<<sms > 0 ? sms : 1, ft::kHeadWarps * 32, smem, (cudaStream_t)stream>>>(x, gamma, W, logits, B,
-                                                                                               V, H, eps);
-  return cudaGetLastError() == cudaSuccess ? FT_OK : FT_ERR_CUDA;
+  for (int c0 = 0; c0 < B; c0 += bc) {
+    const int nb = std::min(bc, B - c0);
+    ft::lm_head_kernel<<<sms > 0 ? sms : 1, ft::kHeadWarps * 32, (size_t)nb * H * 4, (cudaStream_t)stream>>>(
+        x + (size_t)c0 * H, gamma, W, logits + (size_t)c0 * V, nb, V, H, eps);
+    if (cudaGetLastError() != cudaSuccess) return FT_ERR_CUDA;
+  }
+  return FT_OK;
 }
 
 }  // extern "C"

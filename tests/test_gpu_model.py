@@ -34,8 +34,12 @@ def _gpu():
     build.build()
 
 
-@pytest.mark.parametrize("B,V,Hd", [(1, 1000, 512), (3, 777, 1024), (8, 4096, 4096)])
+@pytest.mark.parametrize("B,V,Hd", [(1, 1000, 512), (3, 777, 1024), (8, 4096, 4096), (17, 999, 1024),
+                                    (32, 4096, 4096), (12, 1003, 8192)])
 def test_embed_and_lm_head_small(B, V, Hd):
+    """Embedding gather (exact) and the fused final RMSNorm + BF16 LM head against the
+    oracle, for batches up to 32 (chunks of up to 8 tokens; 5 at H = 8192) and ragged
+    vocabularies; a second call gives the same bits (no accumulation order)."""
     g = np.random.default_rng(B * 131 + V)
     emb_bits, emb = synth._to_bf16(g.normal(0, 0.5, (V, Hd)).astype(np.float32))
     lm_bits, lm = synth._to_bf16(g.normal(0, 0.02, (V, Hd)).astype(np.float32))
@@ -51,7 +55,11 @@ def test_embed_and_lm_head_small(B, V, Hd):
     torch.cuda.synchronize()
     ref = oracle.lm_head(oracle.final_norm(oracle.embed(emb, tok), gamma, 1e-5), lm)
     assert st.item() == 0
-    assert H.rel_rms(logits.cpu().numpy(), ref) < 1e-4
+    got = logits.cpu().numpy()
+    assert H.rel_rms(got, ref) < 1e-4
+    logits2 = torch.full((B, V), float("nan"), dtype=torch.float32, device="cuda")
+    ft.check(ft.ft_lm_head_bf16(x, torch.from_numpy(gamma).cuda(), rt.bits_tensor(lm_bits), logits2, B, V, Hd, 1e-5))
+    np.testing.assert_array_equal(logits2.cpu().numpy(), got)
 
 
 @pytest.mark.parametrize("B,H", [(1, 512), (3, 4096), (8, 8192)])
