@@ -36,43 +36,49 @@ struct TileRegs {
   uint16_t ks[2], vs[2];  // K / V scales of positions g and g+8
 };
 
+// Fragments of one 16-position tile from its ring slot: K entries of positions
+// 0..15 (d/2 bytes each), then V entries.  Positions past the copied ones hold
+// stale codes; the caller masks them (scores -inf, V scales 0).
 template <int D>
-__device__ __forceinline__ void load_tile(TileRegs<D>& r, const uint8_t* cache, const KVLayout& L, int b, int h, int p,
-                                          int g, int tig) {
-  const int last = L.max_ctx - 1;
-  const int pk0 = min(p + g, last), pk1 = min(p + g + 8, last);
-  const uint8_t* kb = cache + L.kc;
-  const uint8_t* vb = cache + L.vc;
-  const uint16_t* ksb = reinterpret_cast<const uint16_t*>(cache + L.ks);
-  const uint16_t* vsb = reinterpret_cast<const uint16_t*>(cache + L.vs);
-  const size_t r0 = L.row(b, h, pk0), r1 = L.row(b, h, pk1);
+__device__ __forceinline__ void tile_from_smem(TileRegs<D>& r, const uint8_t* s, int g, int tig) {
+  constexpr int E = D / 2;
+  const uint8_t* ks = s;
+  const uint8_t* vs = s + 16 * E;
   if constexpr (D == 128) {
-    const uint4 a = ld_stream_v4(kb + r0 * L.entry + tig * 16);
-    const uint4 c = ld_stream_v4(kb + r1 * L.entry + tig * 16);
+    const uint4 a = *reinterpret_cast<const uint4*>(ks + g * E + tig * 16);
+    const uint4 c = *reinterpret_cast<const uint4*>(ks + (g + 8) * E + tig * 16);
     r.k[0][0] = a.x; r.k[0][1] = a.y; r.k[0][2] = a.z; r.k[0][3] = a.w;
     r.k[1][0] = c.x; r.k[1][1] = c.y; r.k[1][2] = c.z; r.k[1][3] = c.w;
   } else {
-    const uint2 a = ld_stream_v2(kb + r0 * L.entry + tig * 8);
-    const uint2 c = ld_stream_v2(kb + r1 * L.entry + tig * 8);
+    const uint2 a = *reinterpret_cast<const uint2*>(ks + g * E + tig * 8);
+    const uint2 c = *reinterpret_cast<const uint2*>(ks + (g + 8) * E + tig * 8);
     r.k[0][0] = a.x; r.k[0][1] = a.y;
     r.k[1][0] = c.x; r.k[1][1] = c.y;
   }
-  const int pv[4] = {p + 2 * tig, p + 2 * tig + 1, p + 2 * tig + 8, p + 2 * tig + 9};
+  const int pv[4] = {2 * tig, 2 * tig + 1, 2 * tig + 8, 2 * tig + 9};
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
-    const size_t rv = L.row(b, h, min(pv[q], last));
     if constexpr (D == 128) {
-      const uint2 a = ld_stream_v2(vb + rv * L.entry + g * 8);
+      const uint2 a = *reinterpret_cast<const uint2*>(vs + pv[q] * E + g * 8);
       r.v[q][0] = a.x;
       r.v[q][1] = a.y;
     } else {
-      r.v[q][0] = ld_stream_u32(vb + rv * L.entry + g * 4);
+      r.v[q][0] = *reinterpret_cast<const uint32_t*>(vs + pv[q] * E + g * 4);
     }
   }
-  r.ks[0] = ld_stream_u16(ksb + r0);
-  r.ks[1] = ld_stream_u16(ksb + r1);
-  r.vs[0] = ld_stream_u16(vsb + r0);
-  r.vs[1] = ld_stream_u16(vsb + r1);
+}
+
+// K / V scales of positions p + g and p + g + 8 (clamped into the cache row).
+__device__ __forceinline__ void load_scales(uint16_t (&ks)[2], uint16_t (&vs)[2], const uint8_t* cache,
+                                            const KVLayout& L, int b, int h, int p, int g) {
+  const int last = L.max_ctx - 1;
+  const size_t r0 = L.row(b, h, min(p + g, last)), r1 = L.row(b, h, min(p + g + 8, last));
+  const uint16_t* ksb = reinterpret_cast<const uint16_t*>(cache + L.ks);
+  const uint16_t* vsb = reinterpret_cast<const uint16_t*>(cache + L.vs);
+  ks[0] = ld_stream_u16(ksb + r0);
+  ks[1] = ld_stream_u16(ksb + r1);
+  vs[0] = ld_stream_u16(vsb + r0);
+  vs[1] = ld_stream_u16(vsb + r1);
 }
 
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
@@ -100,6 +106,11 @@ __device__ __forceinline__ void warp_rope(float (&v)[NPL], int pos, const uint64
   }
 }
 
+// Lazy rescaling threshold of the online softmax (log2 units): weights up to
+// 2^4 = 16 times the running max's keep P = weight * V scale within FP16 for V
+// scales up to 4094.
+constexpr float kLazyLog2 = 4.0f;
+
 template <int D>
 __global__ void __launch_bounds__(kAttnWarps * 32) attn_kernel(const AttnParams p) {
   constexpr int NPL = D / 32;
@@ -110,6 +121,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_kernel(const AttnParams 
   __shared__ float knew[D], vnew[D];
   __shared__ float fac[8][1 + kAttnWarps];  // per head: CTA max, then each warp's rescale factor
   __shared__ __align__(8) uint64_t inbox_bar;  // completes when every partial of this CTA's heads arrived
+  __shared__ __align__(8) uint64_t kv_bar[kAttnWarps][kAttnMaxSlots];  // a warp's ring slot has landed
   // dynamic: mrg[4][G * PW], each warp's partial of every head (before the main
   // loop the same area holds the staged QKV pieces), then, after the larger of
   // the two, inbox[n_split * ceil(G / n_split)][PW], the partials of the heads
@@ -151,10 +163,35 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_kernel(const AttnParams 
   }
   cluster_arrive();  // paired with cluster_wait() before the first push into a peer
 
-  // history K/V do not depend on earlier kernels: start streaming now
-  TileRegs<D> cur;
+  // history K/V do not depend on earlier kernels: start streaming now.  Each warp
+  // owns tiles t0 + warp + k kAttnWarps (k = 0, 1, ...) and a ring of kv_slots
+  // slots; lane 0 bulk-copies tile k into slot k % kv_slots (the K entries of
+  // its 16 positions are contiguous in the cache, and so are the V entries) and
+  // refills the slot with tile k + kv_slots once the warp has used it.
+  const int ns = p.kv_slots;
+  const uint32_t kvb0 = smem_u32(&kv_bar[warp][0]);
+  uint8_t* ring = reinterpret_cast<uint8_t*>(dyn + attn_ring_off(G, p.nsplit, D, p.qkv_plan.npmax)) +
+                  warp * ns * 16 * D;
+  auto issue_tile = [&](int k) {
+    const int tile = t0 + warp + k * kAttnWarps;
+    if (tile >= t1) return;
+    const int p0 = 16 * tile, n = min(16, p.L.max_ctx - p0);  // positions in the cache row
+    const uint32_t bar = kvb0 + 8 * (k % ns);
+    const size_t r = p.L.row(b, h, p0);
+    const uint32_t dst = smem_u32(ring + (k % ns) * 16 * D);
+    mbar_arrive_expect_tx(bar, (uint32_t)(n * D));
+    bulk_g2s(dst, p.cache + p.L.kc + r * p.L.entry, (uint32_t)(n * (D / 2)), bar);
+    bulk_g2s(dst + 8 * D, p.cache + p.L.vc + r * p.L.entry, (uint32_t)(n * (D / 2)), bar);
+  };
+  if (lane == 0) {
+    for (int s2 = 0; s2 < ns; ++s2) mbar_init(kvb0 + 8 * s2, 1);
+    mbar_fence_init();
+    for (int k = 0; k < ns; ++k) issue_tile(k);
+  }
+  __syncwarp();
   int ti = t0 + warp;
-  if (ti < t1) load_tile<D>(cur, p.cache, p.L, b, h, 16 * ti, g, tig);
+  uint16_t ksn[2] = {0, 0}, vsn[2] = {0, 0};  // scales of the warp's next tile
+  if (ti < t1) load_scales(ksn, vsn, p.cache, p.L, b, h, 16 * ti, g);
 
   griddep_wait();
 
@@ -261,10 +298,17 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_kernel(const AttnParams 
   const uint32_t kappa[4] = {kHOffLo, kHOffLo, kHOffHi, kHOffHi};
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
 
-  for (; ti < t1; ti += kAttnWarps) {
-    TileRegs<D> nxt;
-    const bool more = ti + kAttnWarps < t1;
-    if (more) load_tile<D>(nxt, p.cache, p.L, b, h, 16 * (ti + kAttnWarps), g, tig);
+  int kt_done = 0;  // tiles of this warp consumed
+  bool kv_ok = true;
+  for (; ti < t1; ti += kAttnWarps, ++kt_done) {
+    TileRegs<D> cur;
+    cur.ks[0] = ksn[0], cur.ks[1] = ksn[1], cur.vs[0] = vsn[0], cur.vs[1] = vsn[1];
+    if (ti + kAttnWarps < t1) load_scales(ksn, vsn, p.cache, p.L, b, h, 16 * (ti + kAttnWarps), g);
+    if (!mbar_wait(kvb0 + 8 * (kt_done % ns), (kt_done / ns) & 1)) {
+      kv_ok = false;
+      break;
+    }
+    tile_from_smem<D>(cur, ring + (kt_done % ns) * 16 * D, g, tig);
     const int p0 = 16 * ti;
     // S = K . q~   (rows: positions g, g+8; columns: heads 2tig, 2tig+1)
     float sacc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
@@ -290,24 +334,32 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_kernel(const AttnParams 
       mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
       mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
     }
-    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-    const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
-    m0 = mn0;
-    m1 = mn1;
-    const float e0 = exp2f(s0 - mn0), e1 = exp2f(s1 - mn1), e2 = exp2f(s2 - mn0), e3 = exp2f(s3 - mn1);
-    l0 = l0 * al0 + e0 + e2;
-    l1 = l1 * al1 + e1 + e3;
+    // The running max moves (and the sums are rescaled) only when a score exceeds it by
+    // more than kLazyLog2 (warp-uniform decision): the result is the same softmax, the
+    // unnormalised weights stay below 2^kLazyLog2, and most tiles of a long context skip
+    // the rescale.  Every tile holds a valid position, so the first one always moves it.
+    if (__any_sync(0xffffffffu, mx0 > m0 + kLazyLog2 || mx1 > m1 + kLazyLog2)) {
+      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+      const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
+      m0 = mn0;
+      m1 = mn1;
+      l0 *= al0;
+      l1 *= al1;
 #pragma unroll
-    for (int mt = 0; mt < KT; ++mt) {
-      acc[mt][0] *= al0;
-      acc[mt][1] *= al1;
-      acc[mt][2] *= al0;
-      acc[mt][3] *= al1;
+      for (int mt = 0; mt < KT; ++mt) {
+        acc[mt][0] *= al0;
+        acc[mt][1] *= al1;
+        acc[mt][2] *= al0;
+        acc[mt][3] *= al1;
+      }
+      kacc[0] *= al0;
+      kacc[1] *= al1;
+      kacc[2] *= al0;
+      kacc[3] *= al1;
     }
-    kacc[0] *= al0;
-    kacc[1] *= al1;
-    kacc[2] *= al0;
-    kacc[3] *= al1;
+    const float e0 = exp2f(s0 - m0), e1 = exp2f(s1 - m1), e2 = exp2f(s2 - m0), e3 = exp2f(s3 - m1);
+    l0 += e0 + e2;
+    l1 += e1 + e3;
     const float vs0 = va ? bf16_bits_to_f32(cur.vs[0]) : 0.0f;
     const float vs1 = vb ? bf16_bits_to_f32(cur.vs[1]) * 0.0625f : 0.0f;  // positions 8..15: operand / 16
     const uint32_t P0 = pack_half2(e0 * vs0, e1 * vs0);  // position g,   heads 2tig, 2tig+1
@@ -332,7 +384,20 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_kernel(const AttnParams 
       mma_f16(acc[4 * j + 3], A3, pb0, pb1);
     }
     mma_f16(kacc, kappa, pb0, pb1);
-    if (more) cur = nxt;
+    // the slot's fragments are consumed (the MMAs above used them): refill it
+    __syncwarp();
+    if (lane == 0) {
+      fence_proxy_async_smem();
+      issue_tile(kt_done + ns);
+    }
+  }
+  if (!kv_ok) {  // a copy never landed: flag it, and wait (bounded) for the ones still in flight
+    if (lane == 0) {
+      set_status(p.status, FT_DEV_TIMEOUT);
+      for (int k = kt_done; k < kt_done + ns; ++k)
+        if (t0 + warp + k * kAttnWarps < t1) mbar_wait(kvb0 + 8 * (k % ns), (k / ns) & 1);
+    }
+    __syncwarp();
   }
   griddep_launch();
 
@@ -473,45 +538,46 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_kernel(const AttnParams 
 // Per-device caches of the kernel attributes the host plan needs (the queries
 // cost microseconds; every block call plans).  Benign races: equal values.
 static std::atomic<int> g_attn_static[64][2];
-static std::atomic<int> g_attn_occ[64][2][9];
+static std::atomic<int> g_attn_occ[64][2][9][kAttnMaxPieces + 1];
 
-int attn_smem_bytes(int G, int nsplit, int d, int npmax) {
+static const void* attn_fn(int d) { return d == 128 ? (const void*)attn_kernel<128> : (const void*)attn_kernel<64>; }
+
+int attn_smem_bytes(int G, int nsplit, int d, int npmax, int kv_slots) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = 0;
   const int di = d == 128 ? 1 : 0;
   int stat = g_attn_static[dev][di].load(std::memory_order_relaxed);
   if (stat <= 0) {
     cudaFuncAttributes fa = {};
-    const cudaError_t e =
-        di ? cudaFuncGetAttributes(&fa, attn_kernel<128>) : cudaFuncGetAttributes(&fa, attn_kernel<64>);
+    const cudaError_t e = cudaFuncGetAttributes(&fa, attn_fn(d));
     stat = (e == cudaSuccess) ? (int)fa.sharedSizeBytes : 8 * 1024;
     if (e == cudaSuccess) g_attn_static[dev][di].store(stat, std::memory_order_relaxed);
   }
-  return stat + attn_dyn_smem(G, nsplit, d, npmax);
+  return stat + attn_dyn_smem(G, nsplit, d, npmax, kv_slots);
 }
 
-int attn_ctas_per_sm(int G, int d) {
+int attn_ctas_per_sm(int G, int d, int npmax) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || G < 1 || G > 8) return 0;
+  if (npmax < 1 || npmax > kAttnMaxPieces) return 0;
   const int di = d == 128 ? 1 : 0;
-  int n = g_attn_occ[dev][di][G].load(std::memory_order_relaxed);
+  int n = g_attn_occ[dev][di][G][npmax].load(std::memory_order_relaxed);
   if (n > 0) return n;
-  const size_t dyn = (size_t)attn_dyn_smem(G, 8, d, kAttnMaxPieces);  // the largest inbox (8 splits) and stage
-  const cudaError_t e =
-      di ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_kernel<128>, kAttnWarps * 32, dyn)
-         : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_kernel<64>, kAttnWarps * 32, dyn);
+  // this many staged QKV pieces, the largest inbox (16 splits) and the ring of CTAs sharing an SM
+  const size_t dyn = (size_t)attn_dyn_smem(G, 16, d, npmax, kAttnSharedSlots);
+  const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attn_fn(d), kAttnWarps * 32, dyn);
   if (e != cudaSuccess) return 0;
-  g_attn_occ[dev][di][G].store(n, std::memory_order_relaxed);
+  g_attn_occ[dev][di][G][npmax].store(n, std::memory_order_relaxed);
   return n;
 }
 
 static std::atomic<int> g_attn_cl[64][2][9];
 
 // Allows the largest dynamic shared memory an attention CTA can ask for (G = 8,
-// 16 splits, kAttnMaxPieces staged pieces, d = 128: about 50 KB, above the
-// default 48 KB).  Idempotent; false if the runtime refuses.
+// 16 splits, kAttnMaxPieces staged pieces, d = 128, the deepest ring: about
+// 114 KB, above the default 48 KB).  Idempotent; false if the runtime refuses.
 static bool attn_allow_smem(const void* fn) {
-  const int most = attn_dyn_smem(8, 16, 128, kAttnMaxPieces);
+  const int most = attn_dyn_smem(8, 16, 128, kAttnMaxPieces, kAttnMaxSlots);
   return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, most) == cudaSuccess;
 }
 
@@ -522,12 +588,12 @@ int attn_max_cluster(int G, int d) {
   int c = g_attn_cl[dev][di][G].load(std::memory_order_relaxed);
   if (c > 0) return c;
   c = 8;
-  auto fn = di ? (const void*)attn_kernel<128> : (const void*)attn_kernel<64>;
+  const void* fn = attn_fn(d);
   if (attn_allow_smem(fn) && cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(16);
     cfg.blockDim = dim3(kAttnWarps * 32);
-    cfg.dynamicSmemBytes = attn_dyn_smem(G, 16, d, kAttnMaxPieces);
+    cfg.dynamicSmemBytes = attn_dyn_smem(G, 16, d, kAttnMaxPieces, kAttnSharedSlots);
     cudaLaunchAttribute a[1];
     a[0].id = cudaLaunchAttributeClusterDimension;
     a[0].val.clusterDim.x = 16;
@@ -549,14 +615,13 @@ cudaError_t launch_attn(const AttnParams& p, int head_dim, cudaStream_t st, bool
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   const int di = head_dim == 128 ? 1 : 0;
   if (!allowed[dev][di].load(std::memory_order_relaxed)) {
-    if (!attn_allow_smem(di ? (const void*)attn_kernel<128> : (const void*)attn_kernel<64>))
-      return cudaErrorInvalidValue;
+    if (!attn_allow_smem(attn_fn(head_dim))) return cudaErrorInvalidValue;
     allowed[dev][di].store(1, std::memory_order_relaxed);
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)(p.B * p.nkv * p.nsplit));
   cfg.blockDim = dim3(kAttnWarps * 32);
-  cfg.dynamicSmemBytes = attn_dyn_smem(p.G, p.nsplit, head_dim, p.qkv_plan.npmax);
+  cfg.dynamicSmemBytes = attn_dyn_smem(p.G, p.nsplit, head_dim, p.qkv_plan.npmax, p.kv_slots);
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;

@@ -227,6 +227,7 @@ __global__ void __launch_bounds__(128) post_kernel(const PostParams p) {
 struct WsPlan {
   GemvPlan g[4];
   int nsplit;
+  int kv_slots;  // attention: K/V tiles in flight per warp
   int parts;  // prep / mid CTAs per request
   size_t x_h, s_x, rho1, ssq1, xres, h1, qkv, qkv_part, o_part, o_h, s_o, h1_h, s_h1, ssq2, a_h, s_a, gu_part,
       down_part, tick, total;
@@ -234,9 +235,9 @@ struct WsPlan {
 
 // Splits per (request, KV head): as many as keep every attention CTA resident in
 // one wave (a second, partial wave would double the kernel's time).
-static int attn_splits(int B, int nkv, int G, int d, int max_ctx, int sms) {
+static int attn_splits(int B, int nkv, int G, int d, int max_ctx, int sms, int npmax) {
   const int pairs = B * nkv;
-  const int per_sm = attn_ctas_per_sm(G, d);
+  const int per_sm = attn_ctas_per_sm(G, d, npmax);
   const int target = (per_sm > 0 ? per_sm : 4) * (sms > 0 ? sms : 148);
   int ns = target / pairs;
   const int cap = (max_ctx + 63) / 64;
@@ -252,18 +253,26 @@ static WsPlan make_plan(const ft_block_cfg& c, int B, int max_ctx) {
   int sms = ft_host::num_sms();
   if (sms <= 0) sms = 148;
   const int nqkv = (c.n_q + 2 * c.n_kv) * c.head_dim;
-  w.nsplit = attn_splits(B, c.n_kv, c.n_q / c.n_kv, c.head_dim, max_ctx, sms);
+  // batches of 17-32 run the projections on the tensor cores (tcgen05)
+  auto plan = B > 16 ? make_umma_plan : make_gemv_plan;
+  // the partition (hence the QKV pieces attention stages) does not depend on the budget
+  const int np_qkv = plan(kRoleQKV, nqkv, c.hidden, B, sms, 200 * 1024).npmax;
+  w.nsplit = attn_splits(B, c.n_kv, c.n_q / c.n_kv, c.head_dim, max_ctx, sms, np_qkv);
   // shared-memory budget of one GEMV CTA (ring + reduction area); the QKV and O
   // CTAs leave room for one attention CTA on their SM, so that attention CTAs
   // start (and load their first K/V tiles) while QKV still runs, and O CTAs
   // start (and fill their rings) while attention runs
   const int bud = 200 * 1024;
   const int per_sm = ft_host::smem_per_sm();
-  // batches of 17-32 run the projections on the tensor cores (tcgen05)
-  auto plan = B > 16 ? make_umma_plan : make_gemv_plan;
-  // the partition (hence the QKV pieces attention stages) does not depend on the budget
-  const int np_qkv = plan(kRoleQKV, nqkv, c.hidden, B, sms, bud).npmax;
-  const int attn = attn_smem_bytes(c.n_q / c.n_kv, w.nsplit, c.head_dim, np_qkv);
+  // ring depth: no deeper than a warp's share of a split; deep where every attention CTA
+  // has an SM to itself (long contexts at small batch: few CTAs, each streaming far)
+  {
+    const int tiles = (max_ctx + 15) / 16, per_cta = (tiles + w.nsplit - 1) / w.nsplit;
+    const long ctas = (long)B * c.n_kv * w.nsplit;
+    const int cap = ctas <= sms ? kAttnMaxSlots : kAttnSharedSlots;
+    w.kv_slots = std::max(1, std::min(cap, (per_cta + kAttnWarps - 1) / kAttnWarps));
+  }
+  const int attn = attn_smem_bytes(c.n_q / c.n_kv, w.nsplit, c.head_dim, np_qkv, w.kv_slots);
   const int bud_att = per_sm > 0 ? std::min(bud, per_sm - attn - 3 * 1024) : bud;
   w.g[kRoleQKV] = plan(kRoleQKV, nqkv, c.hidden, B, sms, bud_att);
   w.g[kRoleO] = plan(kRoleO, c.hidden, c.n_q * c.head_dim, B, sms, bud_att);
@@ -431,6 +440,7 @@ static int run_block(const ft_block_cfg* c, const ft_layer_weights* w, void* cac
     a.G = c->n_q / c->n_kv;
     a.hb = c->had_block;
     a.nsplit = P.nsplit;
+    a.kv_slots = P.kv_slots;
     a.Nqkv = (c->n_q + 2 * c->n_kv) * c->head_dim;
     a.qscale = (float)(1.4426950408889634 / std::sqrt((double)c->head_dim));
     a.o_h = Hh(P.o_h);

@@ -161,6 +161,7 @@ struct AttnParams {
   KVLayout L;
   const int32_t* pos;
   int B, nq, nkv, G, hb, nsplit, Nqkv;
+  int kv_slots;       // K/V tiles each warp keeps in flight (shared-memory ring, 1..kAttnMaxSlots)
   float qscale;       // log2(e) / sqrt(d), folded into the rotated query
   __half* o_h;        // attention output, grouped operand layout of B rows (op_index)
   sfix_t* s_o;        // its group offsets [nq d / 128][32] (accumulated, exact)
@@ -240,17 +241,28 @@ constexpr int kAttnWarps = 4;  // warps per attention CTA (16-position tiles str
 // that later holds its warps' partials.
 constexpr int kAttnMaxPieces = 8;
 __host__ __device__ __forceinline__ int attn_stage_floats(int G, int d, int npmax) { return (G + 2) * d * npmax; }
+// K/V tiles in flight per attention warp: at most kAttnMaxSlots where every
+// attention CTA has an SM to itself, else at most kAttnSharedSlots (the ring
+// size that still lets four CTAs share an SM)
+constexpr int kAttnMaxSlots = 8, kAttnSharedSlots = 3;
 // Dynamic shared memory of one attention CTA: the warps' partials of G heads
-// (or, before the main loop, the staged QKV pieces) and the inbox of
-// n_split * ceil(G / n_split) pushed partials, (d + 4) floats each.
-__host__ __device__ __forceinline__ int attn_dyn_smem(int G, int nsplit, int d, int npmax) {
+// (or, before the main loop, the staged QKV pieces), the inbox of
+// n_split * ceil(G / n_split) pushed partials, (d + 4) floats each, then
+// (128-byte aligned, at float offset attn_ring_off) each warp's ring of
+// kv_slots K/V tiles of 16 positions (16 d bytes: K entries, then V entries).
+__host__ __device__ __forceinline__ int attn_ring_off(int G, int nsplit, int d, int npmax) {
   const int mrg = kAttnWarps * G * (d + 4), stage = attn_stage_floats(G, d, npmax);
-  return ((mrg > stage ? mrg : stage) + nsplit * ((G + nsplit - 1) / nsplit) * (d + 4)) * 4;
+  const int f = (mrg > stage ? mrg : stage) + nsplit * ((G + nsplit - 1) / nsplit) * (d + 4);
+  return (f + 31) & ~31;
+}
+__host__ __device__ __forceinline__ int attn_dyn_smem(int G, int nsplit, int d, int npmax, int kv_slots) {
+  return attn_ring_off(G, nsplit, d, npmax) * 4 + kAttnWarps * kv_slots * 16 * d;
 }
 // Static + dynamic shared memory of one attention CTA (host).
-int attn_smem_bytes(int G, int nsplit, int d, int npmax);
-// Attention CTAs resident per SM (registers, shared memory), 0 if unknown (host).
-int attn_ctas_per_sm(int G, int d);
+int attn_smem_bytes(int G, int nsplit, int d, int npmax, int kv_slots);
+// Attention CTAs resident per SM (registers, shared memory) with npmax staged
+// QKV pieces, 0 if unknown (host).
+int attn_ctas_per_sm(int G, int d, int npmax);
 // Largest cluster of attention CTAs the device schedules: 16 where the
 // non-portable size is allowed and fits, else 8 (host).
 int attn_max_cluster(int G, int d);
