@@ -36,6 +36,55 @@ struct TileRegs {
   uint16_t ks[2], vs[2];  // K / V scales of positions g and g+8
 };
 
+// K / V scales of positions p + g and p + g + 8 (clamped into the cache row).
+__device__ __forceinline__ void load_scales(uint16_t (&ks)[2], uint16_t (&vs)[2], const uint8_t* cache,
+                                            const KVLayout& L, int b, int h, int p, int g) {
+  const int last = L.max_ctx - 1;
+  const size_t r0 = L.row(b, h, min(p + g, last)), r1 = L.row(b, h, min(p + g + 8, last));
+  const uint16_t* ksb = reinterpret_cast<const uint16_t*>(cache + L.ks);
+  const uint16_t* vsb = reinterpret_cast<const uint16_t*>(cache + L.vs);
+  ks[0] = ld_stream_u16(ksb + r0);
+  ks[1] = ld_stream_u16(ksb + r1);
+  vs[0] = ld_stream_u16(vsb + r0);
+  vs[1] = ld_stream_u16(vsb + r1);
+}
+
+// Fragments and scales of one 16-position tile straight from the cache into
+// registers (short contexts: a warp has a tile or two, nothing to pipeline).
+template <int D>
+__device__ __forceinline__ void load_tile(TileRegs<D>& r, const uint8_t* cache, const KVLayout& L, int b, int h, int p,
+                                          int g, int tig) {
+  const int last = L.max_ctx - 1;
+  const int pk0 = min(p + g, last), pk1 = min(p + g + 8, last);
+  const uint8_t* kb = cache + L.kc;
+  const uint8_t* vb = cache + L.vc;
+  const size_t r0 = L.row(b, h, pk0), r1 = L.row(b, h, pk1);
+  if constexpr (D == 128) {
+    const uint4 a = ld_stream_v4(kb + r0 * L.entry + tig * 16);
+    const uint4 c = ld_stream_v4(kb + r1 * L.entry + tig * 16);
+    r.k[0][0] = a.x; r.k[0][1] = a.y; r.k[0][2] = a.z; r.k[0][3] = a.w;
+    r.k[1][0] = c.x; r.k[1][1] = c.y; r.k[1][2] = c.z; r.k[1][3] = c.w;
+  } else {
+    const uint2 a = ld_stream_v2(kb + r0 * L.entry + tig * 8);
+    const uint2 c = ld_stream_v2(kb + r1 * L.entry + tig * 8);
+    r.k[0][0] = a.x; r.k[0][1] = a.y;
+    r.k[1][0] = c.x; r.k[1][1] = c.y;
+  }
+  const int pv[4] = {p + 2 * tig, p + 2 * tig + 1, p + 2 * tig + 8, p + 2 * tig + 9};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const size_t rv = L.row(b, h, min(pv[q], last));
+    if constexpr (D == 128) {
+      const uint2 a = ld_stream_v2(vb + rv * L.entry + g * 8);
+      r.v[q][0] = a.x;
+      r.v[q][1] = a.y;
+    } else {
+      r.v[q][0] = ld_stream_u32(vb + rv * L.entry + g * 4);
+    }
+  }
+  load_scales(r.ks, r.vs, cache, L, b, h, p, g);
+}
+
 // Fragments of one 16-position tile from its ring slot: K entries of positions
 // 0..15 (d/2 bytes each), then V entries.  Positions past the copied ones hold
 // stale codes; the caller masks them (scores -inf, V scales 0).
@@ -68,18 +117,6 @@ __device__ __forceinline__ void tile_from_smem(TileRegs<D>& r, const uint8_t* s,
   }
 }
 
-// K / V scales of positions p + g and p + g + 8 (clamped into the cache row).
-__device__ __forceinline__ void load_scales(uint16_t (&ks)[2], uint16_t (&vs)[2], const uint8_t* cache,
-                                            const KVLayout& L, int b, int h, int p, int g) {
-  const int last = L.max_ctx - 1;
-  const size_t r0 = L.row(b, h, min(p + g, last)), r1 = L.row(b, h, min(p + g + 8, last));
-  const uint16_t* ksb = reinterpret_cast<const uint16_t*>(cache + L.ks);
-  const uint16_t* vsb = reinterpret_cast<const uint16_t*>(cache + L.vs);
-  ks[0] = ld_stream_u16(ksb + r0);
-  ks[1] = ld_stream_u16(ksb + r1);
-  vs[0] = ld_stream_u16(vsb + r0);
-  vs[1] = ld_stream_u16(vsb + r1);
-}
 
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   const __half2 h = __floats2half2_rn(lo, hi);
@@ -112,7 +149,7 @@ __device__ __forceinline__ void warp_rope(float (&v)[NPL], int pos, const uint64
 constexpr float kLazyLog2 = 4.0f;
 
 template <int D>
-__global__ void __launch_bounds__(kAttnWarps * 32) attn_kernel(const AttnParams p) {
+__global__ void __launch_bounds__(kAttnWarps * 32, 4) attn_kernel(const AttnParams p) {
   constexpr int NPL = D / 32;
   constexpr int KT = D / 16;  // k-tiles of q.K == m-tiles of P.V
   constexpr int PW = D + 4;             // one partial: running max, sum, 2 pad, acc[D] (16-byte rows)
@@ -183,15 +220,21 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_kernel(const AttnParams 
     bulk_g2s(dst, p.cache + p.L.kc + r * p.L.entry, (uint32_t)(n * (D / 2)), bar);
     bulk_g2s(dst + 8 * D, p.cache + p.L.vc + r * p.L.entry, (uint32_t)(n * (D / 2)), bar);
   };
-  if (lane == 0) {
+  if (lane == 0 && ns > 0) {
     for (int s2 = 0; s2 < ns; ++s2) mbar_init(kvb0 + 8 * s2, 1);
     mbar_fence_init();
     for (int k = 0; k < ns; ++k) issue_tile(k);
   }
   __syncwarp();
   int ti = t0 + warp;
-  uint16_t ksn[2] = {0, 0}, vsn[2] = {0, 0};  // scales of the warp's next tile
-  if (ti < t1) load_scales(ksn, vsn, p.cache, p.L, b, h, 16 * ti, g);
+  uint16_t ksn[2] = {0, 0}, vsn[2] = {0, 0};  // ring: scales of the warp's next tile
+  TileRegs<D> reg_cur;                        // no ring (kv_slots 0): the warp's first tile
+  if (ti < t1) {
+    if (ns > 0)
+      load_scales(ksn, vsn, p.cache, p.L, b, h, 16 * ti, g);
+    else
+      load_tile<D>(reg_cur, p.cache, p.L, b, h, 16 * ti, g, tig);
+  }
 
   griddep_wait();
 
@@ -298,17 +341,8 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_kernel(const AttnParams 
   const uint32_t kappa[4] = {kHOffLo, kHOffLo, kHOffHi, kHOffHi};
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
 
-  int kt_done = 0;  // tiles of this warp consumed
-  bool kv_ok = true;
-  for (; ti < t1; ti += kAttnWarps, ++kt_done) {
-    TileRegs<D> cur;
-    cur.ks[0] = ksn[0], cur.ks[1] = ksn[1], cur.vs[0] = vsn[0], cur.vs[1] = vsn[1];
-    if (ti + kAttnWarps < t1) load_scales(ksn, vsn, p.cache, p.L, b, h, 16 * (ti + kAttnWarps), g);
-    if (!mbar_wait(kvb0 + 8 * (kt_done % ns), (kt_done / ns) & 1)) {
-      kv_ok = false;
-      break;
-    }
-    tile_from_smem<D>(cur, ring + (kt_done % ns) * 16 * D, g, tig);
+  // one 16-position tile of this warp: scores, online softmax, P.V
+  auto tile_step = [&](const TileRegs<D>& cur, int ti, bool lazy) {
     const int p0 = 16 * ti;
     // S = K . q~   (rows: positions g, g+8; columns: heads 2tig, 2tig+1)
     float sacc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
@@ -334,11 +368,12 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_kernel(const AttnParams 
       mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
       mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
     }
-    // The running max moves (and the sums are rescaled) only when a score exceeds it by
-    // more than kLazyLog2 (warp-uniform decision): the result is the same softmax, the
-    // unnormalised weights stay below 2^kLazyLog2, and most tiles of a long context skip
-    // the rescale.  Every tile holds a valid position, so the first one always moves it.
-    if (__any_sync(0xffffffffu, mx0 > m0 + kLazyLog2 || mx1 > m1 + kLazyLog2)) {
+    // With `lazy` (long shares) the running max moves (and the sums are rescaled) only when
+    // a score exceeds it by more than kLazyLog2 (warp-uniform decision): the result is the
+    // same softmax, the unnormalised weights stay below 2^kLazyLog2, and most tiles of a
+    // long context skip the rescale.  Every tile holds a valid position, so the first one
+    // always moves it.
+    if (!lazy || __any_sync(0xffffffffu, mx0 > m0 + kLazyLog2 || mx1 > m1 + kLazyLog2)) {
       const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
       const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
       m0 = mn0;
@@ -384,6 +419,28 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_kernel(const AttnParams 
       mma_f16(acc[4 * j + 3], A3, pb0, pb1);
     }
     mma_f16(kacc, kappa, pb0, pb1);
+  };
+  int kt_done = 0;  // tiles of this warp consumed (ring)
+  bool kv_ok = true;
+  if (ns == 0) {
+    for (; ti < t1; ti += kAttnWarps) {  // plain loads, the next tile in flight in registers
+      TileRegs<D> nxt;
+      const bool more = ti + kAttnWarps < t1;
+      if (more) load_tile<D>(nxt, p.cache, p.L, b, h, 16 * (ti + kAttnWarps), g, tig);
+      tile_step(reg_cur, ti, false);
+      if (more) reg_cur = nxt;
+    }
+  }
+  for (; ns > 0 && ti < t1; ti += kAttnWarps, ++kt_done) {
+    TileRegs<D> cur;
+    cur.ks[0] = ksn[0], cur.ks[1] = ksn[1], cur.vs[0] = vsn[0], cur.vs[1] = vsn[1];
+    if (ti + kAttnWarps < t1) load_scales(ksn, vsn, p.cache, p.L, b, h, 16 * (ti + kAttnWarps), g);
+    if (!mbar_wait(kvb0 + 8 * (kt_done % ns), (kt_done / ns) & 1)) {
+      kv_ok = false;
+      break;
+    }
+    tile_from_smem<D>(cur, ring + (kt_done % ns) * 16 * D, g, tig);
+    tile_step(cur, ti, true);
     // the slot's fragments are consumed (the MMAs above used them): refill it
     __syncwarp();
     if (lane == 0) {

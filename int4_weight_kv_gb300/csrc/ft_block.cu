@@ -264,13 +264,16 @@ static WsPlan make_plan(const ft_block_cfg& c, int B, int max_ctx) {
   // start (and fill their rings) while attention runs
   const int bud = 200 * 1024;
   const int per_sm = ft_host::smem_per_sm();
-  // ring depth: no deeper than a warp's share of a split; deep where every attention CTA
-  // has an SM to itself (long contexts at small batch: few CTAs, each streaming far)
+  // attention K/V: a warp with a tile or two loads them straight into registers (kv_slots
+  // 0: a bulk copy's longer latency would only add to the kernel's); longer shares stream
+  // through a ring no deeper than the share, deep where every attention CTA has an SM to
+  // itself (long contexts at small batch: few CTAs, each streaming far)
   {
     const int tiles = (max_ctx + 15) / 16, per_cta = (tiles + w.nsplit - 1) / w.nsplit;
+    const int per_warp = (per_cta + kAttnWarps - 1) / kAttnWarps;
     const long ctas = (long)B * c.n_kv * w.nsplit;
     const int cap = ctas <= sms ? kAttnMaxSlots : kAttnSharedSlots;
-    w.kv_slots = std::max(1, std::min(cap, (per_cta + kAttnWarps - 1) / kAttnWarps));
+    w.kv_slots = per_warp <= 2 ? 0 : std::min(cap, per_warp);
   }
   const int attn = attn_smem_bytes(c.n_q / c.n_kv, w.nsplit, c.head_dim, np_qkv, w.kv_slots);
   const int bud_att = per_sm > 0 ? std::min(bud, per_sm - attn - 3 * 1024) : bud;

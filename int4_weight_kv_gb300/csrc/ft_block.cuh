@@ -161,7 +161,8 @@ struct AttnParams {
   KVLayout L;
   const int32_t* pos;
   int B, nq, nkv, G, hb, nsplit, Nqkv;
-  int kv_slots;       // K/V tiles each warp keeps in flight (shared-memory ring, 1..kAttnMaxSlots)
+  int kv_slots;       // K/V tiles each warp keeps in flight in a shared-memory ring (1..kAttnMaxSlots),
+                      // or 0: plain loads into registers, one tile ahead
   float qscale;       // log2(e) / sqrt(d), folded into the rotated query
   __half* o_h;        // attention output, grouped operand layout of B rows (op_index)
   sfix_t* s_o;        // its group offsets [nq d / 128][32] (accumulated, exact)
