@@ -394,6 +394,8 @@ def run_sweep(args, device, peak: float) -> list:
     from int4_weight_kv_gb300 import runtime as rt
     shapes = {"8B": synth.L8B, "70B": synth.L70B}
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    tr_path = os.path.join(ROOT, "profiles", "traffic.json")
+    traffic = json.load(open(tr_path)) if os.path.exists(tr_path) else {}  # DRAM bytes per dominant launch (ncu)
     out = []
     n_rep = max(10, min(args.steps, 200))
     for sname, cid, points in SWEEP:
@@ -467,7 +469,8 @@ def run_sweep(args, device, peak: float) -> list:
                 "pct_of_measured_hbm": _pct(ab["total"] / med / 1e3, peak),
                 "pct_of_8tbs": _pct(ab["total"] / med / 1e3, NOMINAL_HBM_GBS),
                 "dominant": {"stage": STAGE_NAMES[dom], "launch_us": round(dom_us, 2), "algorithmic_bytes": sb[dom],
-                             "achieved_gbs": round(ach, 1), "frac": round(ach / peak, 3)},
+                             "achieved_gbs": round(ach, 1), "frac": round(ach / peak, 3),
+                             "traffic": traffic.get(f"{sname.lower()}_b{B}_ctx{ctx}")},
             })
             print(json.dumps(out[-1]), file=sys.stderr, flush=True)
             del reps, cache0, g
