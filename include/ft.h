@@ -127,6 +127,28 @@ int ft_kv_append_int4(const ft_block_cfg *cfg, void *cache, int max_batch, int m
                       const uint16_t *k_bf16, const uint16_t *v_bf16, const int32_t *pos, int B,
                       int T, int32_t *dev_status, ft_stream stream);
 
+/* Append packed variable-length requests: the K/V rows the prefill side
+ * produces for a batch of prompts of different lengths, placed straight at
+ * offset(request, head, position, channel) (summary page, "어떻게 동작하나":
+ * the QKV epilogue writes the KV cache directly; requests of different lengths
+ * are packed).  The prefill GEMM itself is not part of this library; this call
+ * is its placement step, with the same rotation and quantiser as
+ * ft_kv_append_int4.
+ *   k_bf16, v_bf16: BF16 bits [total, n_kv, d] (post-RoPE), the rows of request
+ *     0, then request 1, ... back to back.
+ *   cu_seqlens: device int32 [B + 1], the prefix sums of the request lengths
+ *     (cu_seqlens[0] = 0, cu_seqlens[B] = total, non-decreasing); request b
+ *     owns rows cu_seqlens[b] .. cu_seqlens[b+1]-1 (a zero-length request owns
+ *     none).
+ *   pos: device int32 [B], the first position written for request b.
+ * Row cu_seqlens[b] + t goes to position pos[b] + t of request b.  A request
+ * whose positions fall outside 0 .. max_ctx-1 is skipped and sets
+ * FT_DEV_CAPACITY; a map that is not such a prefix sum writes nothing and sets
+ * FT_DEV_RANGE.  B <= max_batch or FT_ERR_CAPACITY; total = 0 enqueues nothing. */
+int ft_kv_append_ragged_int4(const ft_block_cfg *cfg, void *cache, int max_batch, int max_ctx,
+                             const uint16_t *k_bf16, const uint16_t *v_bf16, const int32_t *cu_seqlens,
+                             const int32_t *pos, int B, int total, int32_t *dev_status, ft_stream stream);
+
 /* Inverse view for tests: positions [0, len) of requests [0, B).  codes uint8
  * [B, n_kv, len, d] in logical channel order; scales BF16 bits [B, n_kv, len, 1]. */
 int ft_kv_unpack_int4(const ft_block_cfg *cfg, const void *cache, int max_batch, int max_ctx, int B,

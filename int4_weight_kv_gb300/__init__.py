@@ -63,6 +63,8 @@ _SIGS = {
     "ft_kv_cache_bytes": (c_size_t, [POINTER(BlockCfg), c_int, c_int]),
     "ft_kv_append_int4": (c_int, [POINTER(BlockCfg), c_void_p, c_int, c_int, c_void_p, c_void_p, c_void_p,
                                   c_int, c_int, c_void_p, c_void_p]),
+    "ft_kv_append_ragged_int4": (c_int, [POINTER(BlockCfg), c_void_p, c_int, c_int, c_void_p, c_void_p, c_void_p,
+                                         c_void_p, c_int, c_int, c_void_p, c_void_p]),
     "ft_kv_unpack_int4": (c_int, [POINTER(BlockCfg), c_void_p, c_int, c_int, c_int, c_int, c_void_p, c_void_p,
                                   c_void_p, c_void_p, c_void_p]),
     "ft_decode_workspace_bytes": (c_size_t, [POINTER(BlockCfg), c_int, c_int]),
@@ -174,6 +176,13 @@ def ft_kv_append_int4(cfg, cache, max_batch, max_ctx, k_bits, v_bits, pos, B, T,
                       stream=None) -> int:
     return lib().ft_kv_append_int4(ctypes.byref(cfg), _ptr(cache), max_batch, max_ctx, _ptr(k_bits), _ptr(v_bits),
                                    _ptr(pos), B, T, _ptr(dev_status), _stream(stream))
+
+
+def ft_kv_append_ragged_int4(cfg, cache, max_batch, max_ctx, k_bits, v_bits, cu_seqlens, pos, B, total,
+                             dev_status=None, stream=None) -> int:
+    return lib().ft_kv_append_ragged_int4(ctypes.byref(cfg), _ptr(cache), max_batch, max_ctx, _ptr(k_bits),
+                                          _ptr(v_bits), _ptr(cu_seqlens), _ptr(pos), B, total, _ptr(dev_status),
+                                          _stream(stream))
 
 
 def ft_kv_unpack_int4(cfg, cache, max_batch, max_ctx, B, length, k_codes, v_codes, k_scales, v_scales,

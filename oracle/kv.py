@@ -48,6 +48,23 @@ class KVCacheOracle:
             self.ks[b, :, p0:p0 + t] = ks[b].transpose(1, 0, 2)
             self.vs[b, :, p0:p0 + t] = vs[b].transpose(1, 0, 2)
 
+    def append_ragged(self, k, v, cu_seqlens, pos):
+        """Packed variable-length requests (the prefill side's output): k, v [total, n_kv, d]
+        values (post-RoPE); request b owns rows cu_seqlens[b] .. cu_seqlens[b+1] - 1, which go
+        to positions pos[b] .. pos[b] + len_b - 1 of request b (summary page, "어떻게
+        동작하나": direct placement at offset(request, head, position, channel) from the
+        QKV epilogue).  Each token is quantised on its own, exactly as by append."""
+        k = np.asarray(k, dtype=np.float64)
+        v = np.asarray(v, dtype=np.float64)
+        for b in range(len(cu_seqlens) - 1):
+            lo, hi = int(cu_seqlens[b]), int(cu_seqlens[b + 1])
+            for i in range(lo, hi):
+                p = int(pos[b]) + (i - lo)
+                kc, ks, _ = kv_quantize(k[i], self.hb, self.kvg)
+                vc, vs, _ = kv_quantize(v[i], self.hb, self.kvg)
+                self.kc[b, :, p], self.ks[b, :, p] = kc, ks
+                self.vc[b, :, p], self.vs[b, :, p] = vc, vs
+
     def k_hat(self, b: int, h: int, n: int) -> np.ndarray:
         """Decoded (still rotated) keys of positions 0..n-1, FP64 [n, d]."""
         return dequantize_groups(self.kc[b, h, :n], self.ks[b, h, :n], self.kvg)

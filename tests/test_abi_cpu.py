@@ -152,3 +152,19 @@ def test_plan_partitions(ft):
     assert info(c70, 1, ft.FT_W_DOWN).whole == 0
     with pytest.raises(RuntimeError):
         info(c8, 33, ft.FT_W_QKV)
+
+
+def test_ragged_append_argument_checks(ft):
+    """Host-side checks of the ragged placement, before anything is enqueued."""
+    cfg = ft.cfg_from_shape(synth.TINY)
+    lib = ft.lib()
+    fake = 4096  # never dereferenced: every call below returns before a launch
+    call = lambda cache, mb, mc, k, cu, pos, B, total: lib.ft_kv_append_ragged_int4(
+        ctypes.byref(cfg), cache, mb, mc, k, k, cu, pos, B, total, None, None)
+    assert call(fake, 4, 16, fake, fake, fake, 5, 10) == ft.FT_ERR_CAPACITY       # B > max_batch
+    assert call(fake, 4, 16, fake, fake, fake, 2, -1) == ft.FT_ERR_INVALID_ARG    # negative total
+    assert call(None, 4, 16, fake, fake, fake, 2, 10) == ft.FT_ERR_INVALID_ARG    # no cache
+    assert call(fake, 4, 16, fake, None, fake, 2, 10) == ft.FT_ERR_INVALID_ARG    # no map
+    assert call(fake, 4, 16, None, fake, fake, 2, 10) == ft.FT_ERR_INVALID_ARG    # no rows
+    assert call(fake + 8, 4, 16, fake, fake, fake, 2, 10) == ft.FT_ERR_INVALID_ARG  # misaligned cache
+    assert call(fake, 4, 16, None, fake, fake, 2, 0) == ft.FT_OK                  # nothing to place

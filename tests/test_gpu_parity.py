@@ -101,6 +101,91 @@ def test_kv_append_capacity_flag(tiny):
     assert st.item() & ft.FT_DEV_CAPACITY
 
 
+@pytest.mark.parametrize("shape,cid", [(synth.TINY, 1), (synth.L8B, 2)])
+def test_kv_append_ragged_codes(shape, cid):
+    """Packed variable-length requests (zero-length ones included) placed through the
+    prefix-sum map: every request's rows land at pos[b] .. pos[b] + len_b - 1 with the
+    oracle's codes (the +-1 rule), and nothing else in the cache is written."""
+    cfg = ft.cfg_from_shape(shape)
+    lens = np.array([37, 0, 5, 64, 1, 19])
+    B, max_ctx = len(lens), 80
+    g = np.random.default_rng(cid)
+    pos = np.array([int(g.integers(0, max_ctx - n + 1)) for n in lens], np.int32)
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    total = int(cu[-1])
+    kb, kf = synth.kv_history(shape, cid, 1, total, which="k")     # [1, total, h, d]
+    vb, vf = synth.kv_history(shape, cid, 1, total, which="v")
+    cache = rt.alloc_cache(cfg, B, max_ctx)
+    cache.zero_()
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ft.check(ft.ft_kv_append_ragged_int4(cfg, cache, B, max_ctx, rt.bits_tensor(kb[0]), rt.bits_tensor(vb[0]),
+                                         torch.from_numpy(cu).cuda(), torch.from_numpy(pos).cuda(), B, total, st))
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    kc, vc, ks, vs = H.unpack_cache(H.Layer(shape, cfg, {}, {}), cache, B, max_ctx, B, max_ctx)
+    written = np.zeros((B, shape.n_kv, max_ctx), bool)
+    for b in range(B):
+        if lens[b] == 0:
+            continue
+        p0, p1 = pos[b], pos[b] + lens[b]
+        written[b, :, p0:p1] = True
+        for codes, scales, vals in ((kc, ks, kf), (vc, vs, vf)):
+            rows = vals[0, cu[b]:cu[b + 1]].astype(np.float64)                       # [len, h, d]
+            rot = oracle.blockdiag_apply(rows, shape.hb).astype(np.float32).transpose(1, 0, 2)
+            n_diff, _ = H.compare_codes(codes[b, :, p0:p1], scales[b, :, p0:p1], rot, shape.kvg)
+            assert n_diff <= max(2, rows.size // 20000)
+    assert np.all(kc[~written] == 0) and np.all(ks[~written] == 0)   # untouched (zeroed) entries
+    assert np.all(vc[~written] == 0) and np.all(vs[~written] == 0)
+
+
+def test_kv_append_ragged_equal_lengths_is_the_dense_append(tiny):
+    """With every request of length T the ragged placement writes the very bytes of the
+    dense [B, T, n_kv, d] append (same rotation, quantiser and offsets)."""
+    cfg, s = tiny.cfg, tiny.shape
+    B, T, max_ctx = 3, 21, 40
+    kb, _ = synth.kv_history(s, 5, B, T, which="k")
+    vb, _ = synth.kv_history(s, 5, B, T, which="v")
+    pos = torch.tensor([0, 7, 19], dtype=torch.int32, device="cuda")
+    dense = rt.alloc_cache(cfg, B, max_ctx)
+    ragged = rt.alloc_cache(cfg, B, max_ctx)
+    dense.zero_()
+    ragged.zero_()
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ft.check(ft.ft_kv_append_int4(cfg, dense, B, max_ctx, rt.bits_tensor(kb), rt.bits_tensor(vb), pos, B, T, st))
+    cu = torch.arange(0, (B + 1) * T, T, dtype=torch.int32, device="cuda")
+    flat = lambda x: rt.bits_tensor(np.ascontiguousarray(x.reshape(B * T, s.n_kv, s.head_dim)))
+    ft.check(ft.ft_kv_append_ragged_int4(cfg, ragged, B, max_ctx, flat(kb), flat(vb), cu, pos, B, B * T, st))
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert torch.equal(dense, ragged)
+
+
+def test_kv_append_ragged_flags(tiny):
+    """A request past the cache's end is skipped with FT_DEV_CAPACITY (the others are
+    written); a map that is not a prefix sum writes nothing and sets FT_DEV_RANGE."""
+    cfg, s = tiny.cfg, tiny.shape
+    B, max_ctx = 2, 16
+    k = torch.full((9, s.n_kv, s.head_dim), 0x3F80, dtype=torch.int16, device="cuda")   # BF16 1.0
+    cache = rt.alloc_cache(cfg, B, max_ctx)
+    cache.zero_()
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    cu = torch.tensor([0, 4, 9], dtype=torch.int32, device="cuda")
+    pos = torch.tensor([0, 12], dtype=torch.int32, device="cuda")            # 12 + 5 > 16
+    ft.check(ft.ft_kv_append_ragged_int4(cfg, cache, B, max_ctx, k, k, cu, pos, B, 9, st))
+    torch.cuda.synchronize()
+    assert st.item() & ft.FT_DEV_CAPACITY and not st.item() & ft.FT_DEV_RANGE
+    kc, _, ks, _ = H.unpack_cache(tiny, cache, B, max_ctx, B, max_ctx)
+    assert np.all(ks[0, :, :4] != 0) and np.all(ks[0, :, 4:] == 0) and np.all(ks[1] == 0)
+    for bad in ([0, 6, 3], [1, 4, 9], [0, 4, 8]):                             # decreasing, bad start, bad end
+        cache.zero_()
+        st.zero_()
+        cu_bad = torch.tensor(bad, dtype=torch.int32, device="cuda")
+        ft.check(ft.ft_kv_append_ragged_int4(cfg, cache, B, max_ctx, k, k, cu_bad,
+                                             torch.zeros(2, dtype=torch.int32, device="cuda"), B, 9, st))
+        torch.cuda.synchronize()
+        assert st.item() & ft.FT_DEV_RANGE, bad
+
+
 # ---------------------------------------------------------------- the block
 def test_block_tiny(tiny):
     pb = H.make_problem(tiny, 1, B=1, ctx=128)

@@ -491,3 +491,49 @@ def test_model_step_final_gain_axis_and_lm_head_orientation():
     _, res = oracle.model_step(s, layers, caches, emb, lm, gamma, tokens, np.array([L]), layer_inputs=[xin])
     np.testing.assert_allclose(res[0]["h1"] - res[0]["attn_delta"], xin, rtol=0, atol=1e-14)
     np.testing.assert_array_equal(res[0]["rho1"], rms_factor(xin, s.rms_eps))
+
+
+def test_kv_cache_append_ragged_places_each_token_and_matches_dense():
+    """Ragged placement: packed token i of request b (cu_seqlens[b] <= i < cu_seqlens[b+1])
+    lands at [b, head, pos[b] + i - cu_seqlens[b]]; zero-length requests write nothing;
+    with equal lengths it is the dense append."""
+    nkv, d, cap = 2, 8, 20
+    lens = np.array([3, 0, 5, 1])
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    pos = np.array([2, 7, 0, 19])
+    B, total = len(lens), int(cu[-1])
+    g = np.random.default_rng(9)
+    pat = g.standard_normal(d)
+    k = np.empty((total, nkv, d))
+    v = np.empty((total, nkv, d))
+    for i in range(total):
+        for h in range(nkv):
+            amp = 1.0 + 10 * i + h                     # a different scale for every row
+            k[i, h] = amp * pat
+            v[i, h] = -amp * pat[::-1]
+    c = KVCacheOracle(B, nkv, cap, d, d, d)
+    c.append_ragged(k, v, cu, pos)
+    seen = np.zeros((B, nkv, cap), bool)
+    for b in range(B):
+        for t in range(lens[b]):
+            for h in range(nkv):
+                p = pos[b] + t
+                row = cu[b] + t
+                for cache_c, cache_s, vals in ((c.kc, c.ks, k[row, h]), (c.vc, c.vs, v[row, h])):
+                    codes, sc, _ = kv_quantize(vals, d, d)
+                    np.testing.assert_array_equal(cache_c[b, h, p], codes)
+                    np.testing.assert_array_equal(cache_s[b, h, p], sc)
+                seen[b, h, p] = True
+    assert seen.sum() == total * nkv
+    assert np.all(c.kc[~seen] == 8) and np.all(c.ks[~seen] == 0)
+    # equal lengths: the same cache as the dense append of [B, T, n_kv, d]
+    T = 4
+    kd = g.standard_normal((3, T, nkv, d))
+    vd = g.standard_normal((3, T, nkv, d))
+    p3 = np.array([0, 6, 11])
+    a = KVCacheOracle(3, nkv, cap, d, d, d)
+    a.append(kd, vd, p3)
+    r = KVCacheOracle(3, nkv, cap, d, d, d)
+    r.append_ragged(kd.reshape(3 * T, nkv, d), vd.reshape(3 * T, nkv, d), np.arange(4) * T, p3)
+    for x, y in ((a.kc, r.kc), (a.vc, r.vc), (a.ks, r.ks), (a.vs, r.vs)):
+        np.testing.assert_array_equal(x, y)
