@@ -40,6 +40,7 @@ from .kv import kv_quantize, KVCacheOracle
 from .attention import attend, attend_split, merge_partials
 from .block import decode_block, BlockWeightsOracle
 from .model import model_step, embed, final_norm, lm_head
+from .fp8 import e4m3_decode, e4m3_encode, quantize_weight_e4m3, e4m3_matvec
 
 __all__ = [
     "bf16_rne", "bf16_bits", "bf16_from_bits",
@@ -48,4 +49,5 @@ __all__ = [
     "quantize_weight", "int4_matvec", "kv_quantize", "KVCacheOracle",
     "attend", "attend_split", "merge_partials",
     "decode_block", "BlockWeightsOracle", "model_step", "embed", "final_norm", "lm_head",
+    "e4m3_decode", "e4m3_encode", "quantize_weight_e4m3", "e4m3_matvec",
 ]

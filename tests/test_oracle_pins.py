@@ -537,3 +537,74 @@ def test_kv_cache_append_ragged_places_each_token_and_matches_dense():
     r.append_ragged(kd.reshape(3 * T, nkv, d), vd.reshape(3 * T, nkv, d), np.arange(4) * T, p3)
     for x, y in ((a.kc, r.kc), (a.vc, r.vc), (a.ks, r.ks), (a.vs, r.vs)):
         np.testing.assert_array_equal(x, y)
+
+
+# ---------------------------------------------------------------- E4M3 decode weights
+def test_e4m3_decode_hand_values_and_all_codes_against_torch():
+    """The codec against the format's definition: hand values, then all 256 codes
+    against torch's float8_e4m3fn (a library decoding of the same format)."""
+    from oracle.fp8 import e4m3_decode
+    hand = {0x00: 0.0, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x08: 2.0 ** -6, 0x38: 1.0, 0x3F: 1.875,
+            0x40: 2.0, 0x7E: 448.0, 0xB8: -1.0, 0xFE: -448.0}
+    for c, v in hand.items():
+        assert e4m3_decode(c) == v, hex(c)
+    assert np.isnan(e4m3_decode(0x7F)) and np.isnan(e4m3_decode(0xFF))
+    assert np.signbit(e4m3_decode(0x80)) and e4m3_decode(0x80) == 0.0
+    ref = torch.arange(256, dtype=torch.int32).to(torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = e4m3_decode(np.arange(256))
+    np.testing.assert_array_equal(np.isnan(got), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    np.testing.assert_array_equal(got[ok], ref[ok])
+
+
+def test_e4m3_encode_round_trip_ties_saturation_and_torch():
+    from oracle.fp8 import e4m3_decode, e4m3_encode
+    codes = np.array([c for c in range(256) if (c & 0x7F) != 0x7F])
+    vals = e4m3_decode(codes)
+    np.testing.assert_array_equal(e4m3_encode(vals), codes)             # every finite code, +-0 included
+    pos = e4m3_decode(np.arange(0x7F))
+    mid = (pos[:-1] + pos[1:]) / 2                                       # exact midpoints (FP64)
+    want = np.where(np.arange(1, 0x7F) % 2 == 0, np.arange(1, 0x7F), np.arange(0x7E))
+    np.testing.assert_array_equal(e4m3_encode(mid), want)                # ties go to the even code
+    np.testing.assert_array_equal(e4m3_encode(-mid), want | 0x80)
+    assert e4m3_encode(449.0) == 0x7E and e4m3_encode(1e9) == 0x7E and e4m3_encode(-1e9) == 0xFE
+    assert e4m3_encode(-1e-30) == 0x80 and e4m3_encode(1e-30) == 0x00
+    g = np.random.default_rng(3)
+    x = (g.standard_normal(20000) * np.exp(g.uniform(-12, 6, 20000))).astype(np.float32)
+    x = x[np.abs(x) <= 448.0]
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    np.testing.assert_array_equal(e4m3_encode(x.astype(np.float64)), ref)
+
+
+def test_e4m3_weight_quantiser_and_product():
+    """Per (row, 128 inputs): the group's largest magnitude decodes to +-448 s, every
+    weight to within half an E4M3 step, zero groups to zero; the product applies the
+    group scale after each group's sum (against brute force)."""
+    from oracle.fp8 import e4m3_decode, quantize_weight_e4m3, e4m3_matvec
+    g = np.random.default_rng(11)
+    w = (g.standard_normal((6, 384)) * 0.02).astype(np.float32)
+    w[2, 128:256] = 0.0
+    gamma = g.uniform(0.5, 1.5, 384).astype(np.float32)
+    codes, s = quantize_weight_e4m3(w, gamma)
+    wf = (w * gamma).astype(np.float32).astype(np.float64)
+    deq = e4m3_decode(codes).reshape(6, 3, 128) * s[..., None]
+    assert s[2, 1] == 0 and np.all(codes[2, 128:256] == 0)
+    amax_at = np.argmax(np.abs(wf.reshape(6, 3, 128)), axis=-1)
+    for o in range(6):
+        for k in range(3):
+            if s[o, k] == 0:
+                continue
+            c = codes[o, 128 * k + amax_at[o, k]]
+            assert e4m3_decode(c & 0x7F) == 448.0
+    err = np.abs(deq.reshape(6, 384) - wf)
+    bound = np.maximum(np.abs(wf) * 2.0 ** -4, np.repeat(s, 128, axis=1) * 2.0 ** -10) * (1 + 2 ** -7)
+    assert np.all(err <= bound + 1e-30)
+    x = g.standard_normal((3, 384))
+    y = e4m3_matvec(codes, s, x)
+    brute = np.zeros((3, 6))
+    for b in range(3):
+        for o in range(6):
+            for k in range(3):
+                part = sum(float(e4m3_decode(codes[o, 128 * k + i])) * x[b, 128 * k + i] for i in range(128))
+                brute[b, o] += float(s[o, k]) * part
+    np.testing.assert_allclose(y, brute, rtol=1e-12, atol=1e-12)
