@@ -53,12 +53,14 @@ def hbm_peak() -> tuple[float, str]:
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def algorithmic_bytes(shape, B: int, ctx: int) -> dict:
-    """Minimum bytes one step must move: INT4 codes + BF16 group scales of every
-    weight, the KV history read (codes + scales) and the new entry written, and
-    the BF16 activations in and out."""
+def algorithmic_bytes(shape, B: int, ctx: int, weight_format: int = 0) -> dict:
+    """Minimum bytes one step must move: the codes (INT4, or E4M3 with
+    weight_format 1) + BF16 group scales of every weight, the KV history read
+    (codes + scales) and the new entry written, and the BF16 activations in and
+    out."""
     import int4_weight_kv_gb300 as ft
     cfg = ft.cfg_from_shape(shape)
+    cfg.weight_format = weight_format
     w = {r: ft.ft_packed_weight_bytes(cfg, r) for r in ft.ROLES}
     kv_tok = shape.n_kv * 2 * (shape.head_dim // 2 + 2 * (shape.head_dim // shape.kvg))
     kv = B * ctx * kv_tok + B * kv_tok
@@ -308,6 +310,8 @@ def run_ours(args):
     g_all = graph_of(R)
     spread = _time_graph(g_all, max(10, min(args.steps, 200)), R)
     sweep = None if (args.profile or args.no_sweep) else run_sweep(args, device, hbm_peak()[0])
+    sweep_e4m3 = None if (args.profile or args.no_sweep) else run_sweep(args, device, hbm_peak()[0], SWEEP_E4M3,
+                                                                         weight_format=1, full_step=False)
 
     line = {
         "metric": METRIC, "value": round(us_step, 3), "unit": "us/step", "n_gpus": world, "steps": args.steps,
@@ -329,11 +333,12 @@ def run_ours(args):
                      "launch_us": round(dom_us, 3), "algorithmic_bytes": dom_bytes},
         "e2e": {"value": round(e2e_us, 3), "unit": "us/step", "h2d_bytes_per_step": B * s.hidden * 2 + B * 4,
                 "d2h_bytes_per_step": B * s.hidden * 2},
-        "gpu_launches": ft.ft_decode_block_launches(B) * args.steps,
+        "gpu_launches": ft.ft_decode_block_launches(cfg, B) * args.steps,
         "clocks": clk,
         "us_p10": round(float(np.percentile(spread, 10)), 3), "us_median": round(float(np.median(spread)), 3),
         "us_p90": round(float(np.percentile(spread, 90)), 3),
         "sweep": sweep,
+        "sweep_e4m3": sweep_e4m3,
     }
     if rank == 0:
         line["cpu_baseline"] = None if args.profile else cpu_baseline(wl)
@@ -351,6 +356,8 @@ def run_ours(args):
 # configuration), the 70B rows at context 2048 and 70B batch 1 at context 32768 (the split-KV reduction).
 SWEEP = (("8B", 2, ((1, 1024), (2, 1024), (4, 1024), (8, 1024), (16, 1024), (32, 1024), (32, 4096))),
          ("70B", 4, ((1, 2048), (2, 2048), (4, 2048), (8, 2048), (16, 2048), (32, 2048), (1, 32768))))
+# the same points with E4M3 decode weights (the pages' FP8 decode variant), beside the INT4 ones
+SWEEP_E4M3 = (("8B", 2, ((1, 1024), (32, 1024))), ("70B", 4, ((1, 2048), (32, 2048))))
 
 
 def stage_bytes(shape, B: int, ctx: int, per_role: dict) -> dict:
@@ -384,10 +391,10 @@ def _time_graph(g, n: int, per: int) -> list:
     return [evs[i].elapsed_time(evs[i + 1]) * 1000.0 / per for i in range(n)]
 
 
-def run_sweep(args, device, peak: float) -> list:
+def run_sweep(args, device, peak: float, sweep=SWEEP, weight_format: int = 0, full_step: bool = True) -> list:
     """Every (layer shape, batch, context) of the metric: one graph of R steps over R replicas
     (R * footprint >= 4x L2), per-replay CUDA events; the stage with the most algorithmic bytes timed
-    alone for its roofline."""
+    alone for its roofline.  weight_format 1 runs the points with E4M3 decode weights."""
     import torch
     import synth
     import int4_weight_kv_gb300 as ft
@@ -398,16 +405,18 @@ def run_sweep(args, device, peak: float) -> list:
     traffic = json.load(open(tr_path)) if os.path.exists(tr_path) else {}  # DRAM bytes per dominant launch (ncu)
     out = []
     n_rep = max(10, min(args.steps, 200))
-    for sname, cid, points in SWEEP:
+    tag = "_e4m3" if weight_format else ""
+    for sname, cid, points in sweep:
         s = shapes[sname]
         cfg = ft.cfg_from_shape(s)
+        cfg.weight_format = weight_format
         w = synth.device_layer_weights(s, cid, 0, device)
         packed = [rt.pack_layer(cfg, {k: v for k, v in w.items()}, device=device)]
         del w
         per_role = {r: ft.ft_packed_weight_bytes(cfg, r) for r in ft.ROLES}
         wbytes = sum(per_role.values())
         for B, ctx in points:
-            ab = algorithmic_bytes(s, B, ctx)
+            ab = algorithmic_bytes(s, B, ctx, weight_format)
             R = max(2, int(np.ceil(4 * l2 / (ab["weights"] + ab["kv"]))))
             while len(packed) < R:
                 packed.append({k: v.clone() for k, v in packed[0].items()})
@@ -462,7 +471,7 @@ def run_sweep(args, device, peak: float) -> list:
             dom_us = e0.elapsed_time(e1) * 1000.0 / n_dom
             ach = sb[dom] / dom_us / 1e3
             out.append({
-                "workload": f"{sname.lower()}_b{B}_ctx{ctx}", "batch": B, "ctx": ctx, "replicas": R,
+                "workload": f"{sname.lower()}_b{B}_ctx{ctx}{tag}", "batch": B, "ctx": ctx, "replicas": R,
                 "us_step": round(med, 2), "us_p10": round(float(np.percentile(ts, 10)), 2),
                 "us_p90": round(float(np.percentile(ts, 90)), 2), "replays": n_rep,
                 "algorithmic_bytes": ab["total"], "gbs": round(ab["total"] / med / 1e3, 1),
@@ -470,14 +479,15 @@ def run_sweep(args, device, peak: float) -> list:
                 "pct_of_8tbs": _pct(ab["total"] / med / 1e3, NOMINAL_HBM_GBS),
                 "dominant": {"stage": STAGE_NAMES[dom], "launch_us": round(dom_us, 2), "algorithmic_bytes": sb[dom],
                              "achieved_gbs": round(ach, 1), "frac": round(ach / peak, 3),
-                             "traffic": traffic.get(f"{sname.lower()}_b{B}_ctx{ctx}")},
+                             "traffic": traffic.get(f"{sname.lower()}_b{B}_ctx{ctx}{tag}")},
             })
             print(json.dumps(out[-1]), file=sys.stderr, flush=True)
             del reps, cache0, g
             torch.cuda.empty_cache()
         del packed
         torch.cuda.empty_cache()
-    out.append(run_full_step(args, device, peak))
+    if full_step:
+        out.append(run_full_step(args, device, peak))
     return out
 
 

@@ -52,6 +52,11 @@ enum {
 /* activation dtypes of the block input/output */
 enum { FT_BF16 = 0, FT_F32 = 1 };
 
+/* decode-weight formats (ft_block_cfg.weight_format): INT4 codes, or E4M3 codes
+ * (summary page, "전제와 한계": E4M3 decode weights as the FP8 variant of the
+ * decode path), both with one BF16 scale per (output row, 128 inputs) */
+enum { FT_WFMT_INT4 = 0, FT_WFMT_E4M3 = 1 };
+
 /* ---- configuration ------------------------------------------------------ */
 typedef struct {
   int32_t hidden;    /* H; multiple of 128                                      */
@@ -64,6 +69,7 @@ typedef struct {
   int32_t kv_group;  /* channels per KV scale; must equal head_dim             */
   float rms_eps;     /* RMSNorm epsilon                                        */
   float rope_base;   /* RoPE base                                              */
+  int32_t weight_format; /* FT_WFMT_INT4 (0) or FT_WFMT_E4M3                    */
 } ft_block_cfg;
 
 /* Projection roles.  Weights are given in the logical row-major [N_out, K_in]
@@ -91,12 +97,14 @@ int ft_weight_shape(const ft_block_cfg *cfg, int role, int32_t *n_out, int32_t *
  * 16-row tiles, per (tile, group) 1024 bytes of nibbles in the tensor-core
  * fragment order the decode kernels read, followed by the 16 BF16 scales. */
 
-/* Bytes of one packed role (codes P/2 + scales P/64 for P = N_out * K_in). */
+/* Bytes of one packed role in the configuration's weight format: INT4 codes
+ * P/2 + scales P/64, or E4M3 codes P + scales P/64, for P = N_out * K_in. */
 size_t ft_packed_weight_bytes(const ft_block_cfg *cfg, int role);
 
 /* W: FP32 [N_out, K_in] row-major.  gamma: FP32 [K_in] or NULL (treated as 1);
  * use gamma_attn for QKV and gamma_ffn for GATEUP.  packed: >= 16-byte aligned,
- * packed_bytes >= ft_packed_weight_bytes().  Overwrites packed entirely. */
+ * packed_bytes >= ft_packed_weight_bytes().  Overwrites packed entirely.
+ * cfg->weight_format must be FT_WFMT_INT4 (else FT_ERR_INVALID_ARG). */
 int ft_pack_weights_int4(const ft_block_cfg *cfg, int role, const float *W, const float *gamma,
                          void *packed, size_t packed_bytes, ft_stream stream);
 
@@ -173,8 +181,24 @@ int ft_kv_unpack_int4(const ft_block_cfg *cfg, const void *cache, int max_batch,
  * FP16), FP32 accumulation, epilogues and softmax.  Activations must stay
  * within the FP16 range (|x| < 65504; FT_DEV_RANGE otherwise).
  * 1 <= B <= min(32, max_batch); larger B -> FT_ERR_UNSUPPORTED. */
+/* E4M3 decode weights (summary page, "전제와 한계"; the abstract page compares
+ * the INT4 decode path with an FP8 one).  For each output row o and group of 128
+ * consecutive inputs: W'[o,i] = W[o,i] * gamma[i] (FP32), s = bf16_rne(amax /
+ * 448), code = E4M3(W' / s) rounded to nearest, ties to even, saturating at
+ * +-448, the sign of zero kept (FP32 division; s = 0 gives code 0x00).  Same
+ * row-tile-major layout as INT4 with 2048 bytes of codes per (tile, group) in
+ * the tensor-core fragment order, then the 16 BF16 scales.  Arguments as for
+ * ft_pack_weights_int4; cfg->weight_format must be FT_WFMT_E4M3. */
+int ft_pack_weights_e4m3(const ft_block_cfg *cfg, int role, const float *W, const float *gamma, void *packed,
+                         size_t packed_bytes, ft_stream stream);
+
+/* Inverse layout transform of ft_pack_weights_e4m3 (for tests): codes as E4M3
+ * bytes [N_out, K_in] and scales as BF16 bits [N_out, K_in/128]. */
+int ft_unpack_weights_e4m3(const ft_block_cfg *cfg, int role, const void *packed, uint8_t *codes,
+                           uint16_t *scales_bf16, ft_stream stream);
+
 typedef struct {
-  const void *qkv, *o, *gateup, *down; /* each from ft_pack_weights_int4 */
+  const void *qkv, *o, *gateup, *down; /* each from the pack call of cfg->weight_format */
 } ft_layer_weights;
 
 size_t ft_decode_workspace_bytes(const ft_block_cfg *cfg, int B, int max_ctx);
@@ -288,10 +312,11 @@ int ft_decode_block_static_ws(const ft_block_cfg *cfg, const ft_layer_weights *w
                               int32_t *dev_status, ft_stream stream);
 
 /* Number of kernels one ft_decode_block call with batch B launches: 7 for
- * B <= 16; 9 for 17 <= B <= 32, where the projections run on the tensor cores
- * and two small kernels finish gate/up (SwiGLU) and the block output from the
- * projections' per-piece partial sums. */
-int ft_decode_block_launches(int B);
+ * INT4 weights and B <= 16; 9 where the projections run on the tensor cores
+ * (17 <= B <= 32, or E4M3 weights at any batch) and two small kernels finish
+ * gate/up (SwiGLU) and the block output from the per-piece partial sums.
+ * 0 for an invalid configuration. */
+int ft_decode_block_launches(const ft_block_cfg *cfg, int B);
 
 /* Programmatic dependent launch between the block's kernels (default on).
  * Returns the previous setting. */

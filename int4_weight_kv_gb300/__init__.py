@@ -18,6 +18,7 @@ LIB_PATH = os.path.join(_PKG, "libft.so")
 FT_OK, FT_ERR_INVALID_ARG, FT_ERR_UNSUPPORTED, FT_ERR_WORKSPACE, FT_ERR_CAPACITY, FT_ERR_CUDA = 0, -1, -2, -3, -4, -5
 FT_DEV_CAPACITY, FT_DEV_TIMEOUT, FT_DEV_RANGE = 1, 2, 4
 FT_BF16, FT_F32 = 0, 1
+FT_WFMT_INT4, FT_WFMT_E4M3 = 0, 1
 FT_W_QKV, FT_W_O, FT_W_GATEUP, FT_W_DOWN = 0, 1, 2, 3
 FT_STAGE_PREP, FT_STAGE_QKV, FT_STAGE_ATTN, FT_STAGE_O = 1, 2, 4, 8
 FT_STAGE_MID, FT_STAGE_GU, FT_STAGE_DOWN, FT_STAGE_ALL = 16, 32, 64, 127
@@ -27,7 +28,7 @@ ROLES = (FT_W_QKV, FT_W_O, FT_W_GATEUP, FT_W_DOWN)
 class BlockCfg(ctypes.Structure):
     _fields_ = [("hidden", c_int32), ("n_q", c_int32), ("n_kv", c_int32), ("head_dim", c_int32),
                 ("inter", c_int32), ("w_group", c_int32), ("had_block", c_int32), ("kv_group", c_int32),
-                ("rms_eps", c_float), ("rope_base", c_float)]
+                ("rms_eps", c_float), ("rope_base", c_float), ("weight_format", c_int32)]
 
 
 class LayerWeights(ctypes.Structure):
@@ -60,6 +61,8 @@ _SIGS = {
     "ft_packed_weight_bytes": (c_size_t, [POINTER(BlockCfg), c_int]),
     "ft_pack_weights_int4": (c_int, [POINTER(BlockCfg), c_int, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
     "ft_unpack_weights_int4": (c_int, [POINTER(BlockCfg), c_int, c_void_p, c_void_p, c_void_p, c_void_p]),
+    "ft_pack_weights_e4m3": (c_int, [POINTER(BlockCfg), c_int, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]),
+    "ft_unpack_weights_e4m3": (c_int, [POINTER(BlockCfg), c_int, c_void_p, c_void_p, c_void_p, c_void_p]),
     "ft_kv_cache_bytes": (c_size_t, [POINTER(BlockCfg), c_int, c_int]),
     "ft_kv_append_int4": (c_int, [POINTER(BlockCfg), c_void_p, c_int, c_int, c_void_p, c_void_p, c_void_p,
                                   c_int, c_int, c_void_p, c_void_p]),
@@ -81,7 +84,7 @@ _SIGS = {
     "ft_rmsnorm_bf16": (c_int, [c_void_p, c_void_p, c_void_p, c_int, c_int, c_float, c_void_p]),
     "ft_read_device_status": (c_int, [c_void_p, c_void_p, c_void_p]),
     "ft_decode_plan_info": (c_int, [c_void_p, c_int, c_int, c_int, c_void_p]),
-    "ft_decode_block_launches": (c_int, [c_int]),
+    "ft_decode_block_launches": (c_int, [POINTER(BlockCfg), c_int]),
     "ft_set_pdl": (c_int, [c_int]),
 }
 
@@ -122,16 +125,17 @@ def _stream(stream):
 
 
 def make_cfg(hidden, n_q, n_kv, head_dim, inter, had_block=0, kv_group=0, rms_eps=1e-5, rope_base=500000.0,
-             w_group=128) -> BlockCfg:
+             w_group=128, weight_format=0) -> BlockCfg:
     hb = had_block or head_dim
-    return BlockCfg(hidden, n_q, n_kv, head_dim, inter, w_group, hb, kv_group or head_dim, rms_eps, rope_base)
+    return BlockCfg(hidden, n_q, n_kv, head_dim, inter, w_group, hb, kv_group or head_dim, rms_eps, rope_base,
+                    weight_format)
 
 
 def cfg_from_shape(shape) -> BlockCfg:
     """BlockCfg from any object with the BlockShape attribute names."""
     return make_cfg(shape.hidden, shape.n_q, shape.n_kv, shape.head_dim, shape.inter,
                     getattr(shape, "had_block", 0), getattr(shape, "kv_group", 0),
-                    shape.rms_eps, shape.rope_base)
+                    shape.rms_eps, shape.rope_base, weight_format=getattr(shape, "weight_format", 0))
 
 
 def check(status: int, what: str = "ft") -> None:
@@ -165,6 +169,16 @@ def ft_pack_weights_int4(cfg, role, W, gamma, packed, stream=None) -> int:
 
 def ft_unpack_weights_int4(cfg, role, packed, codes, scales, stream=None) -> int:
     return lib().ft_unpack_weights_int4(ctypes.byref(cfg), role, _ptr(packed), _ptr(codes), _ptr(scales),
+                                        _stream(stream))
+
+
+def ft_pack_weights_e4m3(cfg, role, W, gamma, packed, stream=None) -> int:
+    return lib().ft_pack_weights_e4m3(ctypes.byref(cfg), role, _ptr(W), _ptr(gamma), _ptr(packed),
+                                      packed.numel() * packed.element_size(), _stream(stream))
+
+
+def ft_unpack_weights_e4m3(cfg, role, packed, codes, scales, stream=None) -> int:
+    return lib().ft_unpack_weights_e4m3(ctypes.byref(cfg), role, _ptr(packed), _ptr(codes), _ptr(scales),
                                         _stream(stream))
 
 
@@ -260,8 +274,8 @@ def ft_decode_plan_info(cfg, B: int, max_ctx: int, role: int) -> GemvInfo:
     return out
 
 
-def ft_decode_block_launches(B: int = 1) -> int:
-    return lib().ft_decode_block_launches(int(B))
+def ft_decode_block_launches(cfg, B: int = 1) -> int:
+    return lib().ft_decode_block_launches(ctypes.byref(cfg), int(B))
 
 
 def ft_set_pdl(enabled: bool) -> bool:

@@ -52,6 +52,7 @@ int check_cfg(const ft_block_cfg* c) {
   if (c->hidden % 128 || c->inter % 128) return FT_ERR_UNSUPPORTED;
   if ((c->n_q * c->head_dim) % 128) return FT_ERR_UNSUPPORTED;
   if (((c->n_q + 2 * c->n_kv) * c->head_dim) % 128) return FT_ERR_UNSUPPORTED;
+  if (c->weight_format != FT_WFMT_INT4 && c->weight_format != FT_WFMT_E4M3) return FT_ERR_INVALID_ARG;
   return FT_OK;
 }
 
@@ -90,7 +91,7 @@ int ft_weight_shape(const ft_block_cfg* c, int role, int32_t* n_out, int32_t* k_
 size_t ft_packed_weight_bytes(const ft_block_cfg* c, int role) {
   int32_t n, k;
   if (ft_weight_shape(c, role, &n, &k) != FT_OK) return 0;
-  return (size_t)(n / ft::kRowTile) * (size_t)(k / ft::kWGroup) * ft::kSlabBytes;
+  return (size_t)(n / ft::kRowTile) * (size_t)(k / ft::kWGroup) * (size_t)ft::slab_bytes_of(c->weight_format);
 }
 
 int ft_set_pdl(int enabled) { return ft_host::g_pdl.exchange(enabled ? 1 : 0); }

@@ -27,6 +27,7 @@ struct GemvPlan {
   unsigned long long rcp_per1, rcp_per;
   int divs_exact;  // 0: the partition is too large for that division (refused)
   int umma;        // 1: the tensor-core (tcgen05) kernel, 128-row sets, every role may split sets
+  int slab;        // bytes of one (row tile, group) slab: kSlabBytes (INT4) or kSlabBytesE4 (E4M3)
 };
 
 __host__ __device__ __forceinline__ int plan_u0(const GemvPlan& p, int c) {
@@ -233,7 +234,7 @@ __host__ __device__ __forceinline__ int rms_parts(int H) { return (H / 8 + kPrep
 cudaError_t launch_gemv(int role, const GemvParams& p, cudaStream_t st, bool pdl);
 cudaError_t launch_umma(int role, const GemvParams& p, cudaStream_t st, bool pdl);
 // Partition for the tensor-core kernel (batches of 17-32): 128-row sets.
-GemvPlan make_umma_plan(int role, int N, int K, int B, int sms, int smem_budget);
+GemvPlan make_umma_plan(int role, int N, int K, int B, int sms, int smem_budget, int weight_format);
 int ft_umma_warps();  // warps per CTA of the tensor-core kernel
 cudaError_t launch_attn(const AttnParams& p, int head_dim, cudaStream_t st, bool pdl);
 constexpr int kAttnWarps = 4;  // warps per attention CTA (16-position tiles strided over them)

@@ -449,6 +449,7 @@ static void shape_of(int NT, int& RT, int& NCW) {
 
 GemvPlan make_gemv_plan(int role, int N, int K, int B, int sms, int smem_budget) {
   GemvPlan p = {};
+  p.slab = kSlabBytes;
   p.N = N;
   p.K = K;
   p.NT = (B + 7) / 8;

@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 #include <cuda_fp16.h>
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <stdint.h>
 
 #include "ft.h"
@@ -21,6 +22,11 @@ constexpr int kTilesPerBlock = 8;
 constexpr int kSlabCodes = 1024;     // nibbles of one (row tile, group): 16 x 128 / 2
 constexpr int kSlabBytes = 1056;     // + 16 BF16 scales
 constexpr int kBlockGroupBytes = kTilesPerBlock * kSlabBytes;  // one (row block, group)
+constexpr int kSlabCodesE4 = 2048;   // E4M3 codes of one (row tile, group): 16 x 128 bytes
+constexpr int kSlabBytesE4 = 2080;   // + 16 BF16 scales
+__host__ __device__ __forceinline__ int slab_bytes_of(int weight_format) {
+  return weight_format == FT_WFMT_E4M3 ? kSlabBytesE4 : kSlabBytes;
+}
 
 // bounded waits: a wait that exceeds this many nanoseconds gives up
 constexpr unsigned long long kWaitLimitNs = 4000000000ull;
@@ -369,6 +375,35 @@ __device__ __forceinline__ uint32_t quant_code(float x, float s) {
   float t = rintf(__fdiv_rn(x, s));
   t = fminf(fmaxf(t, -8.0f), 7.0f);
   return (uint32_t)((int)t + 8);
+}
+
+// E4M3 decode weights: s = bf16(amax / 448) (448 = the largest E4M3 magnitude),
+// code = E4M3(x / s) rounded to nearest even, saturating at +-448; s = 0 gives 0.
+__device__ __forceinline__ uint16_t quant_scale_bits_e4m3(float amax) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(__fdiv_rn(amax, 448.0f)));
+}
+__device__ __forceinline__ uint32_t quant_code_e4m3(float x, float s) {
+  if (s == 0.0f) return 0u;
+  return (uint32_t)__nv_cvt_float_to_fp8(__fdiv_rn(x, s), __NV_SATFINITE, __NV_E4M3);
+}
+// Two E4M3 codes (low byte first) -> an FP16 pair (every E4M3 value is exact in FP16).
+__device__ __forceinline__ uint32_t e4m3x2_to_h2(uint32_t two) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two & 0xFFFFu), __NV_E4M3);
+  return (uint32_t)h.x | ((uint32_t)h.y << 16);
+}
+// The four A-fragment registers of one k-step from its 8 packed E4M3 codes
+// (lo: row g inputs c, c+1, c+8, c+9; hi: row g+8, the same inputs), in the
+// order the INT4 decode produces them (rows g | g+8 x inputs c.. | c+8..), the
+// inputs 8..15 of the step scaled by 16 to match the activation operand (x / 16).
+__device__ __forceinline__ void e4m3_words(uint32_t lo, uint32_t hi, uint32_t* r) {
+  const __half2 x16 = __floats2half2_rn(16.0f, 16.0f);
+  const uint32_t u1 = e4m3x2_to_h2(lo >> 16), u3 = e4m3x2_to_h2(hi >> 16);
+  const __half2 a2 = __hmul2(*reinterpret_cast<const __half2*>(&u1), x16);
+  const __half2 a3 = __hmul2(*reinterpret_cast<const __half2*>(&u3), x16);
+  r[0] = e4m3x2_to_h2(lo);
+  r[1] = *reinterpret_cast<const uint32_t*>(&a2);
+  r[2] = e4m3x2_to_h2(hi);
+  r[3] = *reinterpret_cast<const uint32_t*>(&a3);
 }
 
 // Fast Walsh-Hadamard transform of a d-vector held stride-32 across a warp:

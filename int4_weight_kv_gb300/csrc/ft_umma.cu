@@ -122,8 +122,12 @@ struct Smem {
 
 using namespace umma;
 
-template <int ROLE>
+// FMT: FT_WFMT_INT4 (nibbles decoded by the FP16 magic-number trick, offsets S
+// removed per token) or FT_WFMT_E4M3 (bytes converted exactly to FP16, no offset).
+template <int ROLE, int FMT>
 __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const GemvParams p) {
+  constexpr bool E4 = FMT == FT_WFMT_E4M3;
+  constexpr int kSlab = E4 ? kSlabBytesE4 : kSlabBytes, kCodes = E4 ? kSlabCodesE4 : kSlabCodes;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   uint8_t* sm = smem_raw + ((1024 - (raw & 1023)) & 1023);  // 1024-byte aligned (swizzle atoms)
@@ -193,12 +197,12 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const GemvParams p) {
         break;
       }
       if (lane == 0)
-        mbar_arrive_expect_tx(full(slot), (uint32_t)(8 * st.ng * kSlabBytes + 2 * st.ng * p.B * 128 + st.ng * 256));
+        mbar_arrive_expect_tx(full(slot), (uint32_t)(8 * st.ng * kSlab + 2 * st.ng * p.B * 128 + st.ng * 256));
       __syncwarp();
       const uint32_t sb = smem_u32(slots + slot * pl.slot);
       if (lane < 8)
-        bulk_g2s(sb + lane * pl.ng * kSlabBytes, p.w + ((size_t)(st.set * 8 + lane) * pl.NKG + st.kg) * kSlabBytes,
-                 st.ng * kSlabBytes, full(slot));
+        bulk_g2s(sb + lane * pl.ng * kSlab, p.w + ((size_t)(st.set * 8 + lane) * pl.NKG + st.kg) * kSlab,
+                 st.ng * kSlab, full(slot));
       __syncwarp();
       if (waited) issue_x(slot, st.kg, st.ng);
       if (!waited && (si == S - 1 || st.u + st.ng >= u1)) {
@@ -287,7 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const GemvParams p) {
         if (half == 0) {  // this quarter's 32 row scales of the group, for the epilogue
           const int rr = lane & 15;
           const uint16_t sb = *reinterpret_cast<const uint16_t*>(
-              ws + ((2 * q + (lane >> 4)) * pl.ng + kgl) * kSlabBytes + kSlabCodes + 4 * (rr & 7) + 2 * (rr >> 3));
+              ws + ((2 * q + (lane >> 4)) * pl.ng + kgl) * kSlab + kCodes + 4 * (rr & 7) + 2 * (rr >> 3));
           scl[a * 128 + 32 * q + lane] = bf16_bits_to_f32(sb);
         } else if (q == 3) {  // the group's token offsets S (one per token; absent tokens 0)
           const sfix_t* ss = reinterpret_cast<const sfix_t*>(ws + pl.soff);
@@ -296,17 +300,26 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const GemvParams p) {
 #pragma unroll
         for (int s2 = 0; s2 < 2; ++s2) {
           const int T = 2 * q + s2;  // row tile: rows 16 T .. 16 T + 15 = tensor-memory lanes
-          const uint4 w4 = *reinterpret_cast<const uint4*>(ws + (T * pl.ng + kgl) * kSlabBytes + half * 512 + lane * 16);
-          const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
           uint32_t r[16];
+          if constexpr (E4) {  // 4 k-steps x 8 codes: two 16-byte loads
+            const uint4* w8 = reinterpret_cast<const uint4*>(ws + (T * pl.ng + kgl) * kSlab + half * 1024 + lane * 32);
+            const uint4 wa = w8[0], wb = w8[1];
+            e4m3_words(wa.x, wa.y, r);
+            e4m3_words(wa.z, wa.w, r + 4);
+            e4m3_words(wb.x, wb.y, r + 8);
+            e4m3_words(wb.z, wb.w, r + 12);
+          } else {
+            const uint4 w4 = *reinterpret_cast<const uint4*>(ws + (T * pl.ng + kgl) * kSlab + half * 512 + lane * 16);
+            const uint32_t wv[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks) {
-            uint32_t m[4];
-            magic_word(wv[ks], m);
-            r[4 * ks] = m[0];
-            r[4 * ks + 1] = m[1];
-            r[4 * ks + 2] = m[2];
-            r[4 * ks + 3] = m[3];
+            for (int ks = 0; ks < 4; ++ks) {
+              uint32_t m[4];
+              magic_word(wv[ks], m);
+              r[4 * ks] = m[0];
+              r[4 * ks + 1] = m[1];
+              r[4 * ks + 2] = m[2];
+              r[4 * ks + 3] = m[3];
+            }
           }
           tmem_st16x256b_x4(tmem + kACol + 64 * ab + 32 * half + ((uint32_t)(16 * T) << 16), r);
         }
@@ -348,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const GemvParams p) {
         float s4[32];
 #pragma unroll
         for (int t4 = 0; t4 < 8; ++t4) {
-          const float4 v = reinterpret_cast<const float4*>(sof + a * 32)[t4];
+          const float4 v = E4 ? make_float4(0.0f, 0.0f, 0.0f, 0.0f) : reinterpret_cast<const float4*>(sof + a * 32)[t4];
           s4[4 * t4] = v.x;
           s4[4 * t4 + 1] = v.y;
           s4[4 * t4 + 2] = v.z;
@@ -381,28 +394,36 @@ __global__ void __launch_bounds__(kThreads, 1) umma_kernel(const GemvParams p) {
   if (warp == kMma) tmem_dealloc(tmem);
 }
 
-template <int ROLE>
+template <int ROLE, int FMT>
 static cudaError_t launch_umma_role(const GemvParams& p, cudaStream_t st, bool pdl) {
   static int attr_smem[64] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (attr_smem[dev] < p.plan.smem) {
-    cudaError_t e = cudaFuncSetAttribute(umma_kernel<ROLE>, cudaFuncAttributeMaxDynamicSharedMemorySize, p.plan.smem);
+    cudaError_t e =
+        cudaFuncSetAttribute(umma_kernel<ROLE, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, p.plan.smem);
     if (e != cudaSuccess) return e;
     attr_smem[dev] = p.plan.smem;
   }
-  return launch_ex(umma_kernel<ROLE>, dim3(p.plan.C), dim3(kThreads), (size_t)p.plan.smem, st, pdl, p);
+  return launch_ex(umma_kernel<ROLE, FMT>, dim3(p.plan.C), dim3(kThreads), (size_t)p.plan.smem, st, pdl, p);
+}
+
+template <int FMT>
+static cudaError_t launch_umma_fmt(int role, const GemvParams& p, cudaStream_t st, bool pdl) {
+  switch (role) {
+    case kRoleQKV: return launch_umma_role<kRoleQKV, FMT>(p, st, pdl);
+    case kRoleO: return launch_umma_role<kRoleO, FMT>(p, st, pdl);
+    case kRoleGU: return launch_umma_role<kRoleGU, FMT>(p, st, pdl);
+    case kRoleDown: return launch_umma_role<kRoleDown, FMT>(p, st, pdl);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 cudaError_t launch_umma(int role, const GemvParams& p, cudaStream_t st, bool pdl) {
-  switch (role) {
-    case kRoleQKV: return launch_umma_role<kRoleQKV>(p, st, pdl);
-    case kRoleO: return launch_umma_role<kRoleO>(p, st, pdl);
-    case kRoleGU: return launch_umma_role<kRoleGU>(p, st, pdl);
-    case kRoleDown: return launch_umma_role<kRoleDown>(p, st, pdl);
-    default: return cudaErrorInvalidValue;
-  }
+  if (p.plan.slab == kSlabBytesE4) return launch_umma_fmt<FT_WFMT_E4M3>(role, p, st, pdl);
+  if (p.plan.slab == kSlabBytes) return launch_umma_fmt<FT_WFMT_INT4>(role, p, st, pdl);
+  return cudaErrorInvalidValue;
 }
 
 int ft_umma_warps() { return kWarps; }
@@ -410,8 +431,9 @@ int ft_umma_warps() { return kWarps; }
 // Partition of a projection for the tensor-core kernel: 128-row blocks as
 // sets, 3 groups per stage, units (set, group) spread evenly over the CTAs
 // (sets split along K); every piece writes its partial sums to its own slab.
-GemvPlan make_umma_plan(int role, int N, int K, int B, int sms, int smem_budget) {
+GemvPlan make_umma_plan(int role, int N, int K, int B, int sms, int smem_budget, int weight_format) {
   GemvPlan p = {};
+  p.slab = slab_bytes_of(weight_format);
   p.N = N;
   p.K = K;
   p.NT = 4;
@@ -435,9 +457,11 @@ GemvPlan make_umma_plan(int role, int N, int K, int B, int sms, int smem_budget)
   p.npmax = 1;
   if (!whole_sets)
     for (int set = 0; set < p.NSET; ++set) p.npmax = std::max(p.npmax, plan_pieces(p, set));
-  p.ng = std::min(3, p.NKG);  // 3 groups per stage: fewer ring hand-offs than 1 or 2 at the same depth; 4 leaves 3 coarse stages
+  // 3 groups per stage: fewer ring hand-offs than 1 or 2 at the same depth (4 leaves 3 coarse
+  // stages); E4M3 slabs are twice as large, so 2 groups keep 3 stages
+  p.ng = std::min(weight_format == FT_WFMT_E4M3 ? 2 : 3, p.NKG);
   // slot: weight slabs of 8 tiles, activation half-group tiles (1024-aligned), offsets
-  p.xoff = (int)align_up((size_t)8 * p.ng * kSlabBytes, 1024);
+  p.xoff = (int)align_up((size_t)8 * p.ng * p.slab, 1024);
   p.soff = p.xoff + 2 * p.ng * kXTile;
   p.slot = (int)align_up((size_t)p.soff + (size_t)p.ng * 256, 1024);
   p.xstride = 0;

@@ -6,9 +6,9 @@ from __future__ import annotations
 import numpy as np
 import torch
 
-from . import (FT_F32, FT_W_QKV, FT_W_O, FT_W_GATEUP, FT_W_DOWN, check, ft_decode_block, ft_decode_workspace_bytes,
-               ft_embed_bf16, ft_kv_append_int4, ft_kv_cache_bytes, ft_lm_head_bf16, ft_pack_weights_int4,
-               ft_packed_weight_bytes)
+from . import (FT_F32, FT_W_QKV, FT_W_O, FT_W_GATEUP, FT_W_DOWN, FT_WFMT_E4M3, check, ft_decode_block,
+               ft_decode_workspace_bytes, ft_embed_bf16, ft_kv_append_int4, ft_kv_cache_bytes, ft_lm_head_bf16,
+               ft_pack_weights_e4m3, ft_pack_weights_int4, ft_packed_weight_bytes)
 
 ROLE_KEYS = {FT_W_QKV: ("wqkv", "gamma_attn"), FT_W_O: ("wo", None), FT_W_GATEUP: ("wgu", "gamma_ffn"),
              FT_W_DOWN: ("wdown", None)}
@@ -29,7 +29,10 @@ def pack_layer(cfg, w: dict, device="cuda", stream=None) -> dict:
         W = _dev(w[wk], device=device)
         g = _dev(w[gk], device=device) if gk else None
         packed = torch.empty(ft_packed_weight_bytes(cfg, role), dtype=torch.uint8, device=device)
-        check(ft_pack_weights_int4(cfg, role, W, g, packed, stream), "ft_pack_weights_int4")
+        if cfg.weight_format == FT_WFMT_E4M3:
+            check(ft_pack_weights_e4m3(cfg, role, W, g, packed, stream), "ft_pack_weights_e4m3")
+        else:
+            check(ft_pack_weights_int4(cfg, role, W, g, packed, stream), "ft_pack_weights_int4")
         out[ROLE_NAMES[role]] = packed
         del W, g
     return out

@@ -25,6 +25,7 @@ from __future__ import annotations
 import numpy as np
 
 from .weights import quantize_weight, int4_matvec
+from .fp8 import quantize_weight_e4m3, e4m3_matvec
 from .kv import kv_quantize, KVCacheOracle
 from .quant import dequantize_groups
 from .hadamard import blockdiag_apply
@@ -33,14 +34,19 @@ from .attention import attend
 
 
 class BlockWeightsOracle:
-    """Codes and scales of one block's four projections, re-derived from FP32."""
+    """Codes and scales of one block's four projections, re-derived from FP32:
+    INT4 (``fmt="int4"``) or E4M3 decode weights (``fmt="e4m3"``, summary page,
+    "전제와 한계"); the rest of the block is the same for both."""
 
-    def __init__(self, shape, w: dict):
+    def __init__(self, shape, w: dict, fmt: str = "int4"):
         self.shape = shape
-        self.qkv = quantize_weight(w["wqkv"], w["gamma_attn"])
-        self.o = quantize_weight(w["wo"], None)
-        self.gu = quantize_weight(w["wgu"], w["gamma_ffn"])
-        self.down = quantize_weight(w["wdown"], None)
+        self.fmt = fmt
+        quant = {"int4": quantize_weight, "e4m3": quantize_weight_e4m3}[fmt]
+        self.matvec = {"int4": int4_matvec, "e4m3": e4m3_matvec}[fmt]
+        self.qkv = quant(w["wqkv"], w["gamma_attn"])
+        self.o = quant(w["wo"], None)
+        self.gu = quant(w["wgu"], w["gamma_ffn"])
+        self.down = quant(w["wdown"], None)
 
 
 def rms_factor(x, eps: float) -> np.ndarray:
@@ -68,7 +74,7 @@ def decode_block(shape, wts: BlockWeightsOracle, cache: KVCacheOracle, x, pos,
     res = {"rows": rows}
 
     rho1 = rms_factor(xs, s.rms_eps)
-    qkv = rho1[:, None] * int4_matvec(*wts.qkv, xs)
+    qkv = rho1[:, None] * wts.matvec(*wts.qkv, xs)
     res["rho1"], res["qkv"] = rho1, qkv
     q = qkv[:, : nq * d].reshape(len(rows), nq, d)
     k = qkv[:, nq * d: (nq + nkv) * d].reshape(len(rows), nkv, d)
@@ -99,13 +105,13 @@ def decode_block(shape, wts: BlockWeightsOracle, cache: KVCacheOracle, x, pos,
                 o[i, h * d:(h + 1) * d] = blockdiag_apply(ot, hb)
     res.update(o=o, k_codes=kc_new, v_codes=vc_new, k_scales=ks_new, v_scales=vs_new)
 
-    attn_delta = int4_matvec(*wts.o, o)
+    attn_delta = wts.matvec(*wts.o, o)
     h1 = xs + attn_delta
     rho2 = rms_factor(h1, s.rms_eps)
-    gu = rho2[:, None] * int4_matvec(*wts.gu, h1)
+    gu = rho2[:, None] * wts.matvec(*wts.gu, h1)
     g, u = gu[:, : s.inter], gu[:, s.inter:]
     a = g / (1.0 + np.exp(-g)) * u
-    mlp_delta = int4_matvec(*wts.down, a)
+    mlp_delta = wts.matvec(*wts.down, a)
     out = h1 + mlp_delta
     res.update(attn_delta=attn_delta, h1=h1, rho2=rho2, a=a, mlp_delta=mlp_delta, out=out)
     return res

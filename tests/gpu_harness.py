@@ -28,12 +28,14 @@ class Layer:
 
     def oracle_weights(self) -> BlockWeightsOracle:
         if self.wts is None:
-            self.wts = BlockWeightsOracle(self.shape, self.w32)
+            fmt = "e4m3" if self.cfg.weight_format == ft.FT_WFMT_E4M3 else "int4"
+            self.wts = BlockWeightsOracle(self.shape, self.w32, fmt)
         return self.wts
 
 
-def make_layer(shape: synth.BlockShape, config_id: int, layer: int = 0) -> Layer:
+def make_layer(shape: synth.BlockShape, config_id: int, layer: int = 0, weight_format: int = 0) -> Layer:
     cfg = ft.cfg_from_shape(shape)
+    cfg.weight_format = weight_format
     w = synth.layer_weights(shape, config_id, layer)
     packed = rt.pack_layer(cfg, w)
     torch.cuda.synchronize()
@@ -185,8 +187,8 @@ def unpack_weights(layer: Layer, role: int):
     n, k = ft.ft_weight_shape(layer.cfg, role)
     codes = torch.empty((n, k), dtype=torch.uint8, device="cuda")
     scales = torch.empty((n, k // 128), dtype=torch.int16, device="cuda")
-    ft.check(ft.ft_unpack_weights_int4(layer.cfg, role, layer.packed[rt.ROLE_NAMES[role]], codes, scales),
-             "ft_unpack_weights_int4")
+    unpack = ft.ft_unpack_weights_e4m3 if layer.cfg.weight_format == ft.FT_WFMT_E4M3 else ft.ft_unpack_weights_int4
+    ft.check(unpack(layer.cfg, role, layer.packed[rt.ROLE_NAMES[role]], codes, scales), "unpack weights")
     torch.cuda.synchronize()
     return codes.cpu().numpy(), scales.cpu().numpy().view(np.uint16)
 

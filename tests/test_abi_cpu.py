@@ -113,8 +113,21 @@ def test_argument_errors_return_before_launch(ft):
     assert lib.ft_kv_append_int4(ctypes.byref(c), 4096, 2, 64, 16, 16, 16, 1, 65, None, None) == ft.FT_ERR_CAPACITY
     assert lib.ft_kv_append_int4(ctypes.byref(c), 4097, 2, 64, 16, 16, 16, 1, 1, None, None) == ft.FT_ERR_INVALID_ARG
     assert lib.ft_kv_unpack_int4(ctypes.byref(c), 4096, 2, 64, 3, 8, 16, 16, 16, 16, None) == ft.FT_ERR_INVALID_ARG
-    assert ft.ft_decode_block_launches(1) == 7 and ft.ft_decode_block_launches(16) == 7
-    assert ft.ft_decode_block_launches(17) == 9 and ft.ft_decode_block_launches(32) == 9
+    assert ft.ft_decode_block_launches(c, 1) == 7 and ft.ft_decode_block_launches(c, 16) == 7
+    assert ft.ft_decode_block_launches(c, 17) == 9 and ft.ft_decode_block_launches(c, 32) == 9
+    assert ft.ft_decode_block_launches(c, 33) == 0
+    # E4M3 decode weights: the tensor-core path at every batch; packs need the matching format
+    e4 = ft.BlockCfg(*[getattr(c, f) for f, _ in ft.BlockCfg._fields_])
+    e4.weight_format = ft.FT_WFMT_E4M3
+    assert ft.ft_validate_cfg(e4) == ft.FT_OK
+    assert ft.ft_decode_block_launches(e4, 1) == 9
+    assert ft.ft_packed_weight_bytes(e4, 0) == ft.ft_packed_weight_bytes(c, 0) * 2080 // 1056
+    assert lib.ft_pack_weights_int4(ctypes.byref(e4), 0, 4096, None, 8192, 1 << 30, None) == ft.FT_ERR_INVALID_ARG
+    assert lib.ft_pack_weights_e4m3(ctypes.byref(c), 0, 4096, None, 8192, 1 << 30, None) == ft.FT_ERR_INVALID_ARG
+    assert lib.ft_pack_weights_e4m3(ctypes.byref(e4), 0, 4096, None, 8192, 16, None) == ft.FT_ERR_WORKSPACE
+    bad = ft.BlockCfg(*[getattr(c, f) for f, _ in ft.BlockCfg._fields_])
+    bad.weight_format = 7
+    assert ft.ft_validate_cfg(bad) == ft.FT_ERR_INVALID_ARG
     # model-step helpers
     assert lib.ft_rmsnorm_bf16(None, 4096, 8192, 1, 64, ctypes.c_float(1e-5), None) == ft.FT_ERR_INVALID_ARG
     assert lib.ft_rmsnorm_bf16(4096, 4096, 8192, 0, 64, ctypes.c_float(1e-5), None) == ft.FT_ERR_INVALID_ARG

@@ -418,6 +418,53 @@ def test_rotation_ablation(l8b):
     assert errs[128] < 0.75 * errs[1]
 
 
+# ---------------------------------------------------------------- E4M3 decode weights
+@pytest.fixture(scope="module")
+def tiny_e4():
+    return H.make_layer(synth.TINY, 1, weight_format=ft.FT_WFMT_E4M3)
+
+
+@pytest.fixture(scope="module")
+def l8b_e4():
+    return H.make_layer(synth.L8B, 2, weight_format=ft.FT_WFMT_E4M3)
+
+
+@pytest.mark.parametrize("role", ft.ROLES)
+def test_pack_e4m3_codes_bit_exact(tiny_e4, l8b_e4, role):
+    """E4M3 codes (round to nearest even, saturating, sign of zero kept) and BF16 scales
+    bit-exact against the oracle, at the tiny and the 8B shapes."""
+    for lay in (tiny_e4, l8b_e4):
+        codes, scales = H.unpack_weights(lay, role)
+        wk, gk = rt.ROLE_KEYS[role]
+        ref_c, ref_s = oracle.quantize_weight_e4m3(lay.w32[wk], lay.w32[gk] if gk else None)
+        np.testing.assert_array_equal(codes, ref_c)
+        np.testing.assert_array_equal(synth.bf16_bits_to_f32(scales), ref_s)
+
+
+@pytest.mark.parametrize("B", [1, 5, 32])
+def test_block_e4m3_tiny(tiny_e4, B):
+    """The decode block with E4M3 weights (the tensor-core projections at every batch,
+    attention and cache unchanged) against the oracle's E4M3 block; ragged positions."""
+    assert ft.ft_decode_block_launches(tiny_e4.cfg, B) == 9
+    pos = synth.positions(B, 129, ragged=True, seed=B + 3)
+    pb = H.make_problem(tiny_e4, 1, B=B, ctx=129, pos=pos, max_ctx=140)
+    g = H.run_gpu(pb)
+    rows = sorted({0, B // 2, B - 1})
+    o = H.run_oracle(pb, rows=rows)
+    H.assert_block_close(g, o, rows)
+    np.testing.assert_array_equal(H.run_gpu(pb).out, g.out)
+
+
+@pytest.mark.parametrize("B", [1, 32])
+def test_block_e4m3_8b(l8b_e4, B):
+    pos = synth.positions(B, 300, ragged=True, seed=B + 7)
+    pb = H.make_problem(l8b_e4, 2, B=B, ctx=300, pos=pos)
+    g = H.run_gpu(pb)
+    rows = sorted({0, B - 1})
+    o = H.run_oracle(pb, rows=rows)
+    H.assert_block_close(g, o, rows)
+
+
 # ---------------------------------------------------------------- full-size configurations
 def test_block_8b_b32_ctx4096(l8b):
     """Llama-3-8B layer, batch 32, context 4096 (attention-dominated, split-KV);
