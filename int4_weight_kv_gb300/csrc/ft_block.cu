@@ -253,12 +253,12 @@ static WsPlan make_plan(const ft_block_cfg& c, int B, int max_ctx) {
   int sms = ft_host::num_sms();
   if (sms <= 0) sms = 148;
   const int nqkv = (c.n_q + 2 * c.n_kv) * c.head_dim;
-  // batches of 17-32, and E4M3 weights at any batch, run the projections on the tensor
-  // cores (tcgen05)
+  // batches of 17-32 run the projections on the tensor cores (tcgen05); INT4 and E4M3
+  // weights alike
   const int fmt = c.weight_format;
   auto plan = [&](int role, int N, int K, int B_, int sms_, int budget) {
-    return B_ > 16 || fmt == FT_WFMT_E4M3 ? make_umma_plan(role, N, K, B_, sms_, budget, fmt)
-                                          : make_gemv_plan(role, N, K, B_, sms_, budget);
+    return B_ > 16 ? make_umma_plan(role, N, K, B_, sms_, budget, fmt)
+                   : make_gemv_plan(role, N, K, B_, sms_, budget, fmt);
   };
   // the partition (hence the QKV pieces attention stages) does not depend on the budget
   const int np_qkv = plan(kRoleQKV, nqkv, c.hidden, B, sms, 200 * 1024).npmax;
@@ -571,7 +571,7 @@ int ft_decode_block_stages(const ft_block_cfg* c, const ft_layer_weights* w, voi
 
 int ft_decode_block_launches(const ft_block_cfg* c, int B) {
   if (ft_host::check_cfg(c) != FT_OK || B < 1 || B > 32) return 0;
-  return B > 16 || c->weight_format == FT_WFMT_E4M3 ? 9 : 7;
+  return B > 16 ? 9 : 7;
 }
 
 }  // extern "C"

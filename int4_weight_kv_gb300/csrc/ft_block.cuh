@@ -270,7 +270,7 @@ int attn_ctas_per_sm(int G, int d, int npmax);
 int attn_max_cluster(int G, int d);
 // Gate/up CTAs own whole row-tile sets; QKV and O split sets over CTAs along K
 // (each piece's partial sums go to its own slab); down does either.
-GemvPlan make_gemv_plan(int role, int N, int K, int B, int sms, int smem_budget);
+GemvPlan make_gemv_plan(int role, int N, int K, int B, int sms, int smem_budget, int weight_format);
 
 template <typename... Args>
 cudaError_t launch_ex(void (*kernel)(Args...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool pdl,

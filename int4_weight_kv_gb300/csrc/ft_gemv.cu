@@ -139,14 +139,14 @@ __device__ __forceinline__ void gemv_produce(const GemvParams& p, uint8_t* slots
     const int nrt = min(RT, pl.NTILE - st.set * RT);
     if (lane == 0)
       mbar_arrive_expect_tx(full0 + 8 * slot,
-                            (uint32_t)(nrt * st.ng * kSlabBytes + p.B * st.ng * kWGroup * 2 + st.ng * 256));
+                            (uint32_t)(nrt * st.ng * pl.slab + p.B * st.ng * kWGroup * 2 + st.ng * 256));
     __syncwarp();
     // one bulk copy per row tile, issued by lane rt (a single thread issuing them
     // one after another limits the stage rate for wide sets)
     const uint32_t sb = smem_u32(slots + slot * pl.slot);
     for (int rt = lane; rt < nrt; rt += 32)
-      bulk_g2s(sb + rt * pl.ng * kSlabBytes, p.w + ((size_t)(st.set * RT + rt) * pl.NKG + st.kg) * kSlabBytes,
-               st.ng * kSlabBytes, full0 + 8 * slot);
+      bulk_g2s(sb + rt * pl.ng * pl.slab, p.w + ((size_t)(st.set * RT + rt) * pl.NKG + st.kg) * pl.slab,
+               st.ng * pl.slab, full0 + 8 * slot);
     __syncwarp();
     if (waited) issue_x(slot, st.kg, st.ng);
     if (!waited && (s == S - 1 || st.u + st.ng >= u1)) {
@@ -167,8 +167,12 @@ __device__ __forceinline__ void gemv_produce(const GemvParams& p, uint8_t* slots
   }
 }
 
-template <int NT, int ROLE>
+// FMT: FT_WFMT_INT4 (nibbles, FP16 magic-number decode, each group's chain started at
+// -S) or FT_WFMT_E4M3 (bytes converted exactly to FP16, chains start at 0).
+template <int NT, int ROLE, int FMT>
 __global__ void __launch_bounds__((GemvShape<NT>::NCW + 2) * 32, 1) gemv_kernel(const GemvParams p) {
+  constexpr bool E4 = FMT == FT_WFMT_E4M3;
+  constexpr int kSlab = E4 ? kSlabBytesE4 : kSlabBytes, kCodes = E4 ? kSlabCodesE4 : kSlabCodes;
   constexpr int RT = gemv_rt<NT, ROLE>(), NCW = GemvShape<NT>::NCW;
   constexpr int PRODUCER = NCW, EPILOGUE = NCW + 1;
   extern __shared__ __align__(128) uint8_t smem[];
@@ -302,10 +306,10 @@ __global__ void __launch_bounds__((GemvShape<NT>::NCW + 2) * 32, 1) gemv_kernel(
         xr[j] = on ? sw + pl.xoff + (2 * kgl * p.B + row) * 128 : zero_row + kgl * (kWGroup * 2);
         xh[j] = on ? p.B * 128 : 128;
         const longlong2 sv = *reinterpret_cast<const longlong2*>(ss + kgl * 32 + t);
-        c0[j][0] = (t < p.B) ? -sfix_to_f32(sv.x) : 0.0f;
-        c0[j][1] = (t + 1 < p.B) ? -sfix_to_f32(sv.y) : 0.0f;
+        c0[j][0] = (!E4 && t < p.B) ? -sfix_to_f32(sv.x) : 0.0f;
+        c0[j][1] = (!E4 && t + 1 < p.B) ? -sfix_to_f32(sv.y) : 0.0f;
       }
-      const uint8_t* slab0 = sw + kgl * kSlabBytes;
+      const uint8_t* slab0 = sw + kgl * kSlab;
       // k-steps 0-3 and 4-7 of the group run as two independent MMA chains
       // (the second starts at 0) where registers allow, halving the chain depth
       constexpr bool kTwoChains = NT <= 2;
@@ -314,13 +318,20 @@ __global__ void __launch_bounds__((GemvShape<NT>::NCW + 2) * 32, 1) gemv_kernel(
       float acc2[kTwoChains ? RT : 1][kTwoChains ? NT : 1][4];
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
-        uint32_t wd[RT][4];
+        uint32_t wd[RT][E4 ? 8 : 4];  // INT4: one word per k-step; E4M3: two
 #pragma unroll
         for (int rt = 0; rt < RT; ++rt) {
-          const uint8_t* slab = slab0 + rt * pl.ng * kSlabBytes;
-          const uint4 q = *reinterpret_cast<const uint4*>(slab + half * 512 + lane * 16);
-          wd[rt][0] = q.x; wd[rt][1] = q.y; wd[rt][2] = q.z; wd[rt][3] = q.w;
-          if (half == 0) sc[rt] = *reinterpret_cast<const uint32_t*>(slab + kSlabCodes + 4 * g);
+          const uint8_t* slab = slab0 + rt * pl.ng * kSlab;
+          if constexpr (E4) {
+            const uint4* q = reinterpret_cast<const uint4*>(slab + half * 1024 + lane * 32);
+            const uint4 qa = q[0], qb = q[1];
+            wd[rt][0] = qa.x; wd[rt][1] = qa.y; wd[rt][2] = qa.z; wd[rt][3] = qa.w;
+            wd[rt][4] = qb.x; wd[rt][5] = qb.y; wd[rt][6] = qb.z; wd[rt][7] = qb.w;
+          } else {
+            const uint4 q = *reinterpret_cast<const uint4*>(slab + half * 512 + lane * 16);
+            wd[rt][0] = q.x; wd[rt][1] = q.y; wd[rt][2] = q.z; wd[rt][3] = q.w;
+          }
+          if (half == 0) sc[rt] = *reinterpret_cast<const uint32_t*>(slab + kCodes + 4 * g);
         }
 #pragma unroll
         for (int kq = 0; kq < 4; ++kq) {
@@ -335,7 +346,10 @@ __global__ void __launch_bounds__((GemvShape<NT>::NCW + 2) * 32, 1) gemv_kernel(
 #pragma unroll
           for (int rt = 0; rt < RT; ++rt) {
             uint32_t r[4];
-            magic_word(wd[rt][kq], r);
+            if constexpr (E4)
+              e4m3_words(wd[rt][2 * kq], wd[rt][2 * kq + 1], r);
+            else
+              magic_word(wd[rt][kq], r);
             const uint32_t a[4] = {r[0], r[2], r[1], r[3]};
 #pragma unroll
             for (int j = 0; j < NT; ++j) {
@@ -403,7 +417,7 @@ __device__ __forceinline__ void consumer_sync(int nthreads) {
   asm volatile("bar.sync 2, %0;" ::"r"(nthreads) : "memory");
 }
 
-template <int NT, int ROLE>
+template <int NT, int ROLE, int FMT>
 static cudaError_t launch_one(const GemvParams& p, cudaStream_t st, bool pdl) {
   constexpr int THREADS = (GemvShape<NT>::NCW + 2) * 32;
   static int attr_smem[64] = {0};
@@ -412,20 +426,27 @@ static cudaError_t launch_one(const GemvParams& p, cudaStream_t st, bool pdl) {
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (attr_smem[dev] < p.plan.smem) {
     cudaError_t e =
-        cudaFuncSetAttribute(gemv_kernel<NT, ROLE>, cudaFuncAttributeMaxDynamicSharedMemorySize, p.plan.smem);
+        cudaFuncSetAttribute(gemv_kernel<NT, ROLE, FMT>, cudaFuncAttributeMaxDynamicSharedMemorySize, p.plan.smem);
     if (e != cudaSuccess) return e;
     attr_smem[dev] = p.plan.smem;
   }
-  return launch_ex(gemv_kernel<NT, ROLE>, dim3(p.plan.C), dim3(THREADS), (size_t)p.plan.smem, st, pdl, p);
+  return launch_ex(gemv_kernel<NT, ROLE, FMT>, dim3(p.plan.C), dim3(THREADS), (size_t)p.plan.smem, st, pdl, p);
+}
+
+template <int ROLE, int FMT>
+static cudaError_t launch_role_fmt(const GemvParams& p, cudaStream_t st, bool pdl) {
+  switch (p.plan.NT) {
+    case 1: return launch_one<1, ROLE, FMT>(p, st, pdl);
+    case 2: return launch_one<2, ROLE, FMT>(p, st, pdl);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 template <int ROLE>
 static cudaError_t launch_role(const GemvParams& p, cudaStream_t st, bool pdl) {
-  switch (p.plan.NT) {
-    case 1: return launch_one<1, ROLE>(p, st, pdl);
-    case 2: return launch_one<2, ROLE>(p, st, pdl);
-    default: return cudaErrorInvalidValue;
-  }
+  if (p.plan.slab == kSlabBytesE4) return launch_role_fmt<ROLE, FT_WFMT_E4M3>(p, st, pdl);
+  if (p.plan.slab == kSlabBytes) return launch_role_fmt<ROLE, FT_WFMT_INT4>(p, st, pdl);
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_gemv(int role, const GemvParams& p, cudaStream_t st, bool pdl) {
@@ -447,9 +468,9 @@ static void shape_of(int NT, int& RT, int& NCW) {
   }
 }
 
-GemvPlan make_gemv_plan(int role, int N, int K, int B, int sms, int smem_budget) {
+GemvPlan make_gemv_plan(int role, int N, int K, int B, int sms, int smem_budget, int weight_format) {
   GemvPlan p = {};
-  p.slab = kSlabBytes;
+  p.slab = slab_bytes_of(weight_format);
   p.N = N;
   p.K = K;
   p.NT = (B + 7) / 8;
@@ -467,7 +488,7 @@ GemvPlan make_gemv_plan(int role, int N, int K, int B, int sms, int smem_budget)
     const long c_split = std::min<long>(sms, units), c_whole = std::min<long>(sms, p.NSET);
     const double avg = (double)units / (double)c_split;
     const long max_whole = (p.NSET + c_whole - 1) / c_whole * (long)p.NKG;
-    whole_sets = ((double)max_whole - avg) * p.RT * kSlabBytes <= 64.0 * 1024.0;
+    whole_sets = ((double)max_whole - avg) * p.RT * p.slab <= 64.0 * 1024.0;
   }
   p.whole = whole_sets ? 1 : 0;
   const int units = whole_sets ? p.NSET : p.NSET * p.NKG;
@@ -483,15 +504,21 @@ GemvPlan make_gemv_plan(int role, int N, int K, int B, int sms, int smem_budget)
     for (int set = 0; set < p.NSET; ++set) p.npmax = std::max(p.npmax, plan_pieces(p, set));
   p.ng = p.NCW * 4 / p.RT;  // stages of 4 row tiles x NCW groups (a group per warp for RT = 4)
   if (p.ng > p.NKG) p.ng = p.NKG;
-  p.xstride = p.ng * kWGroup * 2;  // bytes of one token row of a stage (grouped rows, no padding)
-  const int wbytes = p.RT * p.ng * kSlabBytes;
-  p.xoff = (int)align_up((size_t)wbytes, 16);
-  p.soff = (int)align_up((size_t)p.xoff + (size_t)B * p.xstride, 16);
-  p.slot = (int)align_up((size_t)p.soff + (size_t)p.ng * 256, 128);
-  p.redoff = 256;
-  const int redbytes = p.NCW * p.RT * p.NT * 128 * 4;
-  p.zerooff = (int)align_up((size_t)p.redoff + (size_t)redbytes, 128);
-  p.slotoff = (int)align_up((size_t)p.zerooff + (size_t)p.ng * kWGroup * 2, 128);
+  // (E4M3 slabs are twice as large: where two such stages would not fit, stages carry fewer
+  // groups, and some consumer warps sit out a stage)
+  for (;;) {
+    p.xstride = p.ng * kWGroup * 2;  // bytes of one token row of a stage (grouped rows, no padding)
+    const int wbytes = p.RT * p.ng * p.slab;
+    p.xoff = (int)align_up((size_t)wbytes, 16);
+    p.soff = (int)align_up((size_t)p.xoff + (size_t)B * p.xstride, 16);
+    p.slot = (int)align_up((size_t)p.soff + (size_t)p.ng * 256, 128);
+    p.redoff = 256;
+    const int redbytes = p.NCW * p.RT * p.NT * 128 * 4;
+    p.zerooff = (int)align_up((size_t)p.redoff + (size_t)redbytes, 128);
+    p.slotoff = (int)align_up((size_t)p.zerooff + (size_t)p.ng * kWGroup * 2, 128);
+    if (p.ng == 1 || p.slotoff + 2 * p.slot <= smem_budget) break;
+    p.ng = (p.ng + 1) / 2;
+  }
   int stages = (smem_budget - p.slotoff) / p.slot;
   if (stages > 8) stages = 8;
   if (stages < 2) stages = 2;

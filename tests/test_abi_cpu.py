@@ -120,7 +120,7 @@ def test_argument_errors_return_before_launch(ft):
     e4 = ft.BlockCfg(*[getattr(c, f) for f, _ in ft.BlockCfg._fields_])
     e4.weight_format = ft.FT_WFMT_E4M3
     assert ft.ft_validate_cfg(e4) == ft.FT_OK
-    assert ft.ft_decode_block_launches(e4, 1) == 9
+    assert ft.ft_decode_block_launches(e4, 1) == 7 and ft.ft_decode_block_launches(e4, 17) == 9
     assert ft.ft_packed_weight_bytes(e4, 0) == ft.ft_packed_weight_bytes(c, 0) * 2080 // 1056
     assert lib.ft_pack_weights_int4(ctypes.byref(e4), 0, 4096, None, 8192, 1 << 30, None) == ft.FT_ERR_INVALID_ARG
     assert lib.ft_pack_weights_e4m3(ctypes.byref(c), 0, 4096, None, 8192, 1 << 30, None) == ft.FT_ERR_INVALID_ARG

@@ -441,11 +441,12 @@ def test_pack_e4m3_codes_bit_exact(tiny_e4, l8b_e4, role):
         np.testing.assert_array_equal(synth.bf16_bits_to_f32(scales), ref_s)
 
 
-@pytest.mark.parametrize("B", [1, 5, 32])
+@pytest.mark.parametrize("B", [1, 5, 12, 32])
 def test_block_e4m3_tiny(tiny_e4, B):
-    """The decode block with E4M3 weights (the tensor-core projections at every batch,
-    attention and cache unchanged) against the oracle's E4M3 block; ragged positions."""
-    assert ft.ft_decode_block_launches(tiny_e4.cfg, B) == 9
+    """The decode block with E4M3 weights (the legacy-MMA projections up to 16 tokens, the
+    tensor-core ones above; attention and cache unchanged) against the oracle's E4M3 block;
+    ragged positions."""
+    assert ft.ft_decode_block_launches(tiny_e4.cfg, B) == (9 if B > 16 else 7)
     pos = synth.positions(B, 129, ragged=True, seed=B + 3)
     pb = H.make_problem(tiny_e4, 1, B=B, ctx=129, pos=pos, max_ctx=140)
     g = H.run_gpu(pb)
@@ -455,7 +456,7 @@ def test_block_e4m3_tiny(tiny_e4, B):
     np.testing.assert_array_equal(H.run_gpu(pb).out, g.out)
 
 
-@pytest.mark.parametrize("B", [1, 32])
+@pytest.mark.parametrize("B", [1, 9, 32])
 def test_block_e4m3_8b(l8b_e4, B):
     pos = synth.positions(B, 300, ragged=True, seed=B + 7)
     pb = H.make_problem(l8b_e4, 2, B=B, ctx=300, pos=pos)
