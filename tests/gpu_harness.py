@@ -163,7 +163,8 @@ def max_abs_over_rms(y, ref) -> float:
 
 
 def assert_block_close(gpu: GpuResult, orc: dict, rows, tol_rms=5e-3, tol_max=2e-2) -> dict:
-    """North-star gates on `out`; the sublayer deltas are gated at the same relative RMS."""
+    """The block-output gates on `out` (rel RMS and max-abs over RMS); the sublayer deltas are gated at
+    the same relative RMS."""
     rows = list(rows)
     out = gpu.out[rows]
     x = orc["h1"] - orc["attn_delta"]
