@@ -256,7 +256,7 @@ def test_swiglu_closed_form():
 MINI = BlockShape(hidden=256, n_q=8, n_kv=2, head_dim=16, inter=256, rope_base=10000.0)
 
 
-def _mini_setup(shape=MINI, B=2, L=5, seed=12, zero=()):
+def _mini_setup(shape=MINI, B=2, L=5, seed=12, zero=(), fmt="int4"):
     g = np.random.default_rng(seed)
     w = {
         "wqkv": g.normal(0, 0.05, (shape.n_qkv, shape.hidden)).astype(np.float32),
@@ -268,7 +268,7 @@ def _mini_setup(shape=MINI, B=2, L=5, seed=12, zero=()):
     }
     for z in zero:
         w[z][:] = 0
-    wts = BlockWeightsOracle(shape, w)
+    wts = BlockWeightsOracle(shape, w, fmt)
     cache = KVCacheOracle(B, shape.n_kv, L + 4, shape.head_dim, shape.hb, shape.kvg)
     if L:
         cache.append(g.standard_normal((B, L, shape.n_kv, shape.head_dim)),
@@ -353,7 +353,12 @@ def _brute_block(shape, wts, cache, x, L):
     s = shape
     H, d, nq, nkv = s.hidden, s.head_dim, s.n_q, s.n_kv
     G = nq // nkv
-    W = {k: oracle.dequantize_groups(*getattr(wts, k), 128) for k in ("qkv", "o", "gu", "down")}
+    def dequant(codes, scales):
+        if wts.fmt == "e4m3":   # E4M3 values times the group scale, element by element
+            return [[float(oracle.e4m3_decode(codes[r][i])) * float(scales[r][i // 128]) for i in range(len(codes[r]))]
+                    for r in range(len(codes))]
+        return oracle.dequantize_groups(codes, scales, 128)
+    W = {k: dequant(*getattr(wts, k)) for k in ("qkv", "o", "gu", "down")}
     rho = 1 / math.sqrt(sum(v * v for v in x) / H + s.rms_eps)
     y = [rho * sum(W["qkv"][r][i] * x[i] for i in range(H)) for r in range(s.n_qkv)]
 
@@ -396,12 +401,37 @@ def _brute_block(shape, wts, cache, x, L):
     return [h1[r] + sum(W["down"][r][i] * a[i] for i in range(s.inter)) for r in range(H)]
 
 
-def test_block_brute_force_tiny():
+@pytest.mark.parametrize("fmt", ["int4", "e4m3"])
+def test_block_brute_force_tiny(fmt):
+    """The whole block (INT4 or E4M3 decode weights) against explicit loops."""
     shape = BlockShape(hidden=128, n_q=16, n_kv=4, head_dim=8, inter=128, rope_base=10000.0)
-    w, wts, cache, x = _mini_setup(shape=shape, B=1, L=3, seed=13)
+    w, wts, cache, x = _mini_setup(shape=shape, B=1, L=3, seed=13, fmt=fmt)
     r = decode_block(shape, wts, cache, x, np.array([3]), write_cache=False)
     want = _brute_block(shape, wts, cache, list(x[0]), 3)
     np.testing.assert_allclose(r["out"][0], want, rtol=1e-11, atol=1e-12)
+
+
+def test_block_e4m3_residual_only_and_closer_to_dense():
+    """E4M3 decode weights: zero output weights leave the residual; with the same FP32 weights
+    the E4M3 block's MLP lies closer to the unquantised FP64 MLP (on the same h1) than the
+    INT4 one (finer codes)."""
+    w, wts, cache, x = _mini_setup(zero=("wo", "wdown"), fmt="e4m3")
+    r = decode_block(MINI, wts, cache, x, np.array([5, 5]), write_cache=False)
+    np.testing.assert_array_equal(r["out"], x)
+
+    def mlp_error(fmt):
+        w32, wq, cq, xq = _mini_setup(fmt=fmt, seed=21)
+        res = decode_block(MINI, wq, cq, xq, np.array([5, 5]), write_cache=False)
+        h1 = res["h1"]
+        rho2 = 1.0 / np.sqrt(np.mean(h1 * h1, axis=-1) + MINI.rms_eps)
+        wgu = w32["wgu"].astype(np.float64) * w32["gamma_ffn"].astype(np.float64)[None, :]
+        gu = rho2[:, None] * (h1 @ wgu.T)
+        g_, u_ = gu[:, :MINI.inter], gu[:, MINI.inter:]
+        dense = (g_ / (1 + np.exp(-g_)) * u_) @ w32["wdown"].astype(np.float64).T
+        return np.linalg.norm(res["mlp_delta"] - dense) / np.linalg.norm(dense)
+
+    e8, e4 = mlp_error("e4m3"), mlp_error("int4")
+    assert e8 < 0.5 * e4, (e8, e4)
 
 
 # ---------------------------------------------------------------- KV cache placement
