@@ -30,6 +30,9 @@
 //    slabs to h1 and writing the output (completion ticket, never waits).
 //  * batches of 17-32 run on the tensor-core kernel (tcgen05, ft_umma.cu)
 //    instead; this kernel serves 1-16 tokens (one or two column tiles).
+//  * E4M3 decode weights (summary page, "전제와 한계") take the same path with
+//    2080-byte slabs: two codes at a time convert exactly to an FP16 pair, and
+//    there is no decode offset to remove.
 #include <algorithm>
 
 #include "ft_block.cuh"
