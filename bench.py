@@ -144,13 +144,14 @@ def max_over_ranks(value: float, device, world: int) -> float:
 
 
 # ---------------------------------------------------------------------------- our arm
-def setup_replicas(wl, R: int, device):
+def setup_replicas(wl, R: int, device, weight_format: int = 0):
     import torch
     import synth
     import int4_weight_kv_gb300 as ft
     from int4_weight_kv_gb300 import runtime as rt
     s = wl.shape
     cfg = ft.cfg_from_shape(s)
+    cfg.weight_format = weight_format
     w = synth.layer_weights(s, wl.config_id, 0)
     packed = rt.pack_layer(cfg, w, device=device)
     del w
@@ -196,11 +197,12 @@ def run_ours(args):
 
     wl = synth.workload(args.workload)
     s, B, ctx = wl.shape, wl.batch, wl.ctx
-    ab = algorithmic_bytes(s, B, ctx)
+    wfmt = 1 if args.weights == "e4m3" else 0
+    ab = algorithmic_bytes(s, B, ctx, wfmt)
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
     footprint = ab["weights"] + ab["kv"]
     R = max(2, int(np.ceil(4 * l2 / footprint)))
-    cfg, reps, pos, status, max_ctx, xb = setup_replicas(wl, R, device)
+    cfg, reps, pos, status, max_ctx, xb = setup_replicas(wl, R, device, wfmt)
     stream = torch.cuda.current_stream(device)
 
     def step(r):
@@ -285,7 +287,7 @@ def run_ours(args):
     tr_path = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(tr_path):
         with open(tr_path) as f:
-            traffic = json.load(f).get(args.workload)
+            traffic = json.load(f).get(args.workload + ("_e4m3" if wfmt else ""))
 
     # end to end through the C ABI with host buffers (pinned), copies inside the timed region
     n_e2e = R if args.profile else min(args.steps, 500)
@@ -321,8 +323,9 @@ def run_ours(args):
         "config": {"workload": args.workload, "hidden": s.hidden, "n_q": s.n_q, "n_kv": s.n_kv,
                    "head_dim": s.head_dim, "inter": s.inter, "batch": B, "ctx": ctx, "replicas": R,
                    "l2": f"inputs larger than L2: {R} replicas of weights+KV ({R * footprint / 1e6:.0f} MB) cycled",
-                   "graph": True, "pdl": True, "precision": "INT4 weights and KV (BF16 scales), FP16 MMA "
-                                                            "operands, FP32 accumulate, BF16 block I/O"},
+                   "graph": True, "pdl": True, "weights": args.weights,
+                   "precision": ("E4M3" if wfmt else "INT4") + " weights and INT4 KV (BF16 scales), FP16 MMA "
+                                "operands, FP32 accumulate, BF16 block I/O"},
         "block_gbs": round(ab["total"] / us_step / 1e3, 1),
         "pct_of_8tbs": round(100.0 * ab["total"] / us_step / 1e3 / NOMINAL_HBM_GBS, 1),
         "pct_of_measured_hbm": round(100.0 * ab["total"] / us_step / 1e3 / peak, 1),
@@ -649,6 +652,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--weights", choices=["int4", "e4m3"], default="int4",
+                    help="decode-weight format of the headline workload (the sweep reports both)")
     ap.add_argument("--no-sweep", action="store_true",
                     help="only the headline workload (skip the batch 1-32 sweep and the full 32-layer step)")
     ap.add_argument("--profile", action="store_true",
