@@ -416,10 +416,6 @@ __global__ void __launch_bounds__((GemvShape<NT>::NCW + 2) * 32, 1) gemv_kernel(
   }
 }
 
-__device__ __forceinline__ void consumer_sync(int nthreads) {
-  asm volatile("bar.sync 2, %0;" ::"r"(nthreads) : "memory");
-}
-
 template <int NT, int ROLE, int FMT>
 static cudaError_t launch_one(const GemvParams& p, cudaStream_t st, bool pdl) {
   constexpr int THREADS = (GemvShape<NT>::NCW + 2) * 32;

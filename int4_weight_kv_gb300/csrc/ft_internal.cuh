@@ -17,11 +17,8 @@ namespace ft {
 // ------------------------------------------------------------------ layout
 constexpr int kWGroup = 128;         // weight group along the input axis
 constexpr int kRowTile = 16;         // rows per MMA tile
-constexpr int kRowBlock = 128;       // rows per packed row block (8 tiles)
-constexpr int kTilesPerBlock = 8;
 constexpr int kSlabCodes = 1024;     // nibbles of one (row tile, group): 16 x 128 / 2
 constexpr int kSlabBytes = 1056;     // + 16 BF16 scales
-constexpr int kBlockGroupBytes = kTilesPerBlock * kSlabBytes;  // one (row block, group)
 constexpr int kSlabCodesE4 = 2048;   // E4M3 codes of one (row tile, group): 16 x 128 bytes
 constexpr int kSlabBytesE4 = 2080;   // + 16 BF16 scales
 __host__ __device__ __forceinline__ int slab_bytes_of(int weight_format) {
