@@ -181,3 +181,20 @@ def test_ragged_append_argument_checks(ft):
     assert call(fake, 4, 16, None, fake, fake, 2, 10) == ft.FT_ERR_INVALID_ARG    # no rows
     assert call(fake + 8, 4, 16, fake, fake, fake, 2, 10) == ft.FT_ERR_INVALID_ARG  # misaligned cache
     assert call(fake, 4, 16, None, fake, fake, 2, 0) == ft.FT_OK                  # nothing to place
+
+
+@pytest.mark.parametrize("fmt", [0, 1])
+def test_plans_fit_shared_memory_for_every_batch(ft, fmt):
+    """Host plans for INT4 and E4M3 weights at every batch 1..32 and the three shapes: every
+    projection ring fits one SM's shared memory with at least two stages, and the partition
+    covers every (row set, group) unit once (no launch could fail on its shared memory)."""
+    for shape in (synth.TINY, synth.L8B, synth.L70B):
+        cfg = ft.cfg_from_shape(shape)
+        cfg.weight_format = fmt
+        for B in range(1, 33):
+            for role in ft.ROLES:
+                g = ft.ft_decode_plan_info(cfg, B, 2049, role)
+                assert 0 < g.smem_bytes <= 227 * 1024, (shape.hidden, B, role, g.smem_bytes)
+                assert g.stages >= 2 and g.groups_per_stage >= 1
+                assert g.tensor_core == (1 if B > 16 else 0)
+            assert ft.ft_decode_block_launches(cfg, B) == (9 if B > 16 else 7)
