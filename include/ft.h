@@ -113,6 +113,22 @@ int ft_pack_weights_int4(const ft_block_cfg *cfg, int role, const float *W, cons
 int ft_unpack_weights_int4(const ft_block_cfg *cfg, int role, const void *packed, uint8_t *codes,
                            uint16_t *scales_bf16, ft_stream stream);
 
+/* E4M3 decode weights (summary page, "전제와 한계"; the abstract page compares
+ * the INT4 decode path with an FP8 one).  For each output row o and group of 128
+ * consecutive inputs: W'[o,i] = W[o,i] * gamma[i] (FP32), s = bf16_rne(amax /
+ * 448), code = E4M3(W' / s) rounded to nearest, ties to even, saturating at
+ * +-448, the sign of zero kept (FP32 division; s = 0 gives code 0x00).  Same
+ * row-tile-major layout as INT4 with 2048 bytes of codes per (tile, group) in
+ * the tensor-core fragment order, then the 16 BF16 scales.  Arguments as for
+ * ft_pack_weights_int4; cfg->weight_format must be FT_WFMT_E4M3. */
+int ft_pack_weights_e4m3(const ft_block_cfg *cfg, int role, const float *W, const float *gamma, void *packed,
+                         size_t packed_bytes, ft_stream stream);
+
+/* Inverse layout transform of ft_pack_weights_e4m3 (for tests): codes as E4M3
+ * bytes [N_out, K_in] and scales as BF16 bits [N_out, K_in/128]. */
+int ft_unpack_weights_e4m3(const ft_block_cfg *cfg, int role, const void *packed, uint8_t *codes,
+                           uint16_t *scales_bf16, ft_stream stream);
+
 /* ---- KV cache -----------------------------------------------------------
  * One layer's cache for max_batch requests x n_kv heads x max_ctx positions.
  * Entry (request, head, position) holds d/2 bytes of K nibbles, d/2 bytes of V
@@ -180,23 +196,8 @@ int ft_kv_unpack_int4(const ft_block_cfg *cfg, const void *cache, int max_batch,
  * Arithmetic: tensor-core FP16 operands (codes exact, activations rounded to
  * FP16), FP32 accumulation, epilogues and softmax.  Activations must stay
  * within the FP16 range (|x| < 65504; FT_DEV_RANGE otherwise).
+ * The projection weights are in cfg->weight_format (INT4 or E4M3 codes).
  * 1 <= B <= min(32, max_batch); larger B -> FT_ERR_UNSUPPORTED. */
-/* E4M3 decode weights (summary page, "전제와 한계"; the abstract page compares
- * the INT4 decode path with an FP8 one).  For each output row o and group of 128
- * consecutive inputs: W'[o,i] = W[o,i] * gamma[i] (FP32), s = bf16_rne(amax /
- * 448), code = E4M3(W' / s) rounded to nearest, ties to even, saturating at
- * +-448, the sign of zero kept (FP32 division; s = 0 gives code 0x00).  Same
- * row-tile-major layout as INT4 with 2048 bytes of codes per (tile, group) in
- * the tensor-core fragment order, then the 16 BF16 scales.  Arguments as for
- * ft_pack_weights_int4; cfg->weight_format must be FT_WFMT_E4M3. */
-int ft_pack_weights_e4m3(const ft_block_cfg *cfg, int role, const float *W, const float *gamma, void *packed,
-                         size_t packed_bytes, ft_stream stream);
-
-/* Inverse layout transform of ft_pack_weights_e4m3 (for tests): codes as E4M3
- * bytes [N_out, K_in] and scales as BF16 bits [N_out, K_in/128]. */
-int ft_unpack_weights_e4m3(const ft_block_cfg *cfg, int role, const void *packed, uint8_t *codes,
-                           uint16_t *scales_bf16, ft_stream stream);
-
 typedef struct {
   const void *qkv, *o, *gateup, *down; /* each from the pack call of cfg->weight_format */
 } ft_layer_weights;
